@@ -1,0 +1,349 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+No expected value here comes from the CUDA library.  Each pin is an
+independent route to the same number: a hand-derived closed form, a special
+case that reduces to a textbook computation (prefix sum, geometric decay,
+numpy's correlate), the brute-force chunk form of TensorRT-Model-Connect
+#2207 ("Implementation") against the row-by-row recurrence of TensorSharp
+"nemotron.md" section 4.1, or an invariant (linearity, group expansion,
+split invariance).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import ssd_inputs as si
+
+TINY = si.TINY
+
+
+def _tiny_problem(seed=0, z=False, h0=False, shape=TINY, stress=False):
+    p = si.params(shape, seed=seed, stress=stress)
+    a = si.prefill_inputs(shape, seed=seed, act_dtype=__import__("torch").float32,
+                          initial_state=h0, with_z=z, stress=stress)
+    conv = {k: p[k].double().numpy() for k in ("conv_w", "conv_b")}
+    xbc_raw = a["xbc"].double().numpy()
+    xbc, _ = oracle.conv1d(xbc_raw, conv["conv_w"], conv["conv_b"], None)
+    out = dict(xbc=xbc, dt_raw=a["dt_raw"].double().numpy(),
+               dt_bias=p["dt_bias"].double().numpy(), A=p["A"].double().numpy(),
+               D=p["D"].double().numpy(),
+               z=None if a["z"] is None else a["z"].double().numpy(),
+               h0=None if a["ssm_state"] is None else a["ssm_state"].double().numpy())
+    return out
+
+
+def _dims(shape):
+    return dict(H=shape.nheads, P=shape.headdim, N=shape.dstate, G=shape.ngroups)
+
+
+def _relerr(a, b):
+    den = np.max(np.abs(b))
+    return float(np.max(np.abs(a - b)) / (den if den > 0 else 1.0))
+
+
+# --------------------------------------------------------------------------
+# hand-derived closed forms (H = P = N = G = 1)
+
+def _scalar_xbc(xs, Bs, Cs):
+    return np.array([[[x, b, c] for x, b, c in zip(xs, Bs, Cs)]], dtype=np.float64)
+
+
+def test_single_step_hand_values():
+    # dt passed directly, A = -ln 2 so the decay is exactly 1/2.
+    # h1 = 0.5*2 + 1*1*2 = 3 ; y1 = 3*3 + 0.5*1 = 9.5   (post-update state)
+    # h2 = 0.5*3 + 1*2*2 = 5.5 ; y2 = 3*5.5 + 0.5*2 = 17.5
+    xbc = _scalar_xbc([1.0, 2.0], [2.0, 2.0], [3.0, 3.0])
+    dt = np.ones((1, 2, 1))
+    y, hS = oracle.ssd_sequential(xbc, dt, np.array([-math.log(2.0)]), H=1, P=1, N=1, G=1,
+                                  D=np.array([0.5]), h0=np.array([[[[2.0]]]]),
+                                  dt_softplus=False)
+    assert y[0, :, 0, 0] == pytest.approx([9.5, 17.5], abs=1e-14)
+    assert hS[0, 0, 0, 0] == pytest.approx(5.5, abs=1e-14)
+
+
+def test_softplus_and_bias_hand_values():
+    # dt = softplus(0.3 + 0.2) = ln(1 + e^0.5); decay e^{dt*A}; N = P = 1
+    sp = math.log1p(math.exp(0.5))
+    A = -0.7
+    h1 = math.exp(sp * A) * 1.5 + sp * 0.4 * -1.1
+    y1 = 0.9 * h1
+    xbc = _scalar_xbc([0.4], [-1.1], [0.9])
+    y, hS = oracle.ssd_sequential(xbc, np.full((1, 1, 1), 0.3), np.array([A]), H=1, P=1,
+                                  N=1, G=1, dt_bias=np.array([0.2]),
+                                  h0=np.array([[[[1.5]]]]))
+    assert y[0, 0, 0, 0] == pytest.approx(y1, rel=1e-14)
+    assert hS[0, 0, 0, 0] == pytest.approx(h1, rel=1e-14)
+
+
+def test_three_step_unrolled_sum():
+    # Three steps unrolled by hand into the convolutional sum:
+    # h3 = e^{a1+a2+a3} h0 + e^{a2+a3} dt1 x1 B1 + e^{a3} dt2 x2 B2 + dt3 x3 B3
+    rng = np.random.default_rng(3)
+    xs, Bs, Cs = rng.normal(size=3), rng.normal(size=3), rng.normal(size=3)
+    dts = rng.uniform(0.1, 1.0, size=3)
+    A, h0 = -0.8, 0.37
+    a = dts * A
+    h3 = (math.exp(a.sum()) * h0 + math.exp(a[1] + a[2]) * dts[0] * xs[0] * Bs[0]
+          + math.exp(a[2]) * dts[1] * xs[1] * Bs[1] + dts[2] * xs[2] * Bs[2])
+    h2 = (math.exp(a[0] + a[1]) * h0 + math.exp(a[1]) * dts[0] * xs[0] * Bs[0]
+          + dts[1] * xs[1] * Bs[1])
+    y, hS = oracle.ssd_sequential(_scalar_xbc(xs, Bs, Cs), dts.reshape(1, 3, 1),
+                                  np.array([A]), H=1, P=1, N=1, G=1,
+                                  h0=np.array([[[[h0]]]]), dt_softplus=False)
+    assert hS[0, 0, 0, 0] == pytest.approx(h3, rel=1e-13)
+    assert y[0, 1, 0, 0] == pytest.approx(Cs[1] * h2, rel=1e-13)
+
+
+# --------------------------------------------------------------------------
+# special cases with textbook answers
+
+def test_dt_zero_leaves_state_unchanged():
+    prob = _tiny_problem(h0=True)
+    dt0 = np.zeros_like(prob["dt_raw"])
+    y, hS = oracle.ssd_sequential(prob["xbc"], dt0, prob["A"], **_dims(TINY), D=prob["D"],
+                                  h0=prob["h0"], dt_softplus=False)
+    assert np.array_equal(hS, prob["h0"])
+    H, P, N, G = TINY.nheads, TINY.headdim, TINY.dstate, TINY.ngroups
+    x = prob["xbc"][..., : H * P].reshape(1, -1, H, P)
+    Cm = prob["xbc"][..., H * P + G * N:].reshape(1, -1, G, N)
+    Ch = np.repeat(Cm, H // G, axis=2)
+    expect = np.einsum("bthn,bhpn->bthp", Ch, prob["h0"]) + prob["D"][None, None, :, None] * x
+    assert _relerr(y, expect) < 1e-13
+
+
+def test_zero_input_is_geometric_decay():
+    prob = _tiny_problem(h0=True)
+    H, P = TINY.nheads, TINY.headdim
+    xbc = prob["xbc"].copy()
+    xbc[..., : H * P] = 0.0
+    y, hS = oracle.ssd_sequential(xbc, prob["dt_raw"], prob["A"], **_dims(TINY),
+                                  dt_bias=prob["dt_bias"], h0=prob["h0"])
+    dt = np.log1p(np.exp(prob["dt_raw"] + prob["dt_bias"]))  # softplus, moderate values
+    total = dt.sum(axis=1)[0]  # [H]
+    expect = np.exp(prob["A"] * total)[:, None, None] * prob["h0"][0]
+    assert _relerr(hS[0], expect) < 1e-12
+
+
+def test_A_zero_is_prefix_sum():
+    prob = _tiny_problem(h0=True)
+    H, P, N, G = TINY.nheads, TINY.headdim, TINY.dstate, TINY.ngroups
+    A0 = np.zeros(H)
+    y, hS = oracle.ssd_sequential(prob["xbc"], prob["dt_raw"], A0, **_dims(TINY),
+                                  dt_bias=prob["dt_bias"], D=prob["D"], h0=prob["h0"])
+    dt = np.log1p(np.exp(prob["dt_raw"] + prob["dt_bias"]))[0]  # [S,H]
+    x = prob["xbc"][0, :, : H * P].reshape(-1, H, P)
+    Bm = np.repeat(prob["xbc"][0, :, H * P: H * P + G * N].reshape(-1, G, N), H // G, axis=1)
+    Cm = np.repeat(prob["xbc"][0, :, H * P + G * N:].reshape(-1, G, N), H // G, axis=1)
+    inc = dt[:, :, None, None] * x[:, :, :, None] * Bm[:, :, None, :]  # [S,H,P,N]
+    states = prob["h0"][0][None] + np.cumsum(inc, axis=0)
+    assert _relerr(hS[0], states[-1]) < 1e-13
+    y_expect = np.einsum("thn,thpn->thp", Cm, states) + prob["D"][None, :, None] * x
+    assert _relerr(y[0], y_expect) < 1e-13
+
+
+# --------------------------------------------------------------------------
+# chunk form == recurrence (TensorRT-Model-Connect #2207: 11 rows as 7 + 4)
+
+@pytest.mark.parametrize("parts", [[11], [7, 4], [1] * 11, [3, 1, 5, 2], [4, 7]])
+@pytest.mark.parametrize("with_z", [False, True])
+def test_chunked_equals_sequential(parts, with_z):
+    prob = _tiny_problem(z=with_z, h0=True)
+    kw = dict(dt_bias=prob["dt_bias"], D=prob["D"], z=prob["z"], h0=prob["h0"])
+    y1, h1 = oracle.ssd_sequential(prob["xbc"], prob["dt_raw"], prob["A"], **_dims(TINY), **kw)
+    y2, h2 = oracle.ssd_chunked(prob["xbc"], prob["dt_raw"], prob["A"], parts, **_dims(TINY),
+                                **kw)
+    assert y1.size == 1 * 11 * 4 * 16 and h1.size == 4 * 16 * 16
+    assert _relerr(y2, y1) < 1e-12
+    assert _relerr(h2, h1) < 1e-12
+
+
+def test_chunked_rejects_bad_partition():
+    prob = _tiny_problem()
+    with pytest.raises(ValueError):
+        oracle.ssd_chunked(prob["xbc"], prob["dt_raw"], prob["A"], [5, 5], **_dims(TINY))
+
+
+def test_split_calls_equal_one_call():
+    """Two calls chained through the final state == one call over all rows."""
+    prob = _tiny_problem(h0=True)
+    kw = dict(dt_bias=prob["dt_bias"], D=prob["D"])
+    y, h = oracle.ssd_sequential(prob["xbc"], prob["dt_raw"], prob["A"], **_dims(TINY),
+                                 h0=prob["h0"], **kw)
+    ya, ha = oracle.ssd_sequential(prob["xbc"][:, :7], prob["dt_raw"][:, :7], prob["A"],
+                                   **_dims(TINY), h0=prob["h0"], **kw)
+    yb, hb = oracle.ssd_sequential(prob["xbc"][:, 7:], prob["dt_raw"][:, 7:], prob["A"],
+                                   **_dims(TINY), h0=ha, **kw)
+    assert np.array_equal(np.concatenate([ya, yb], axis=1), y)
+    assert np.array_equal(hb, h)
+
+
+# --------------------------------------------------------------------------
+# decay of about 1e6 per row (TensorRT-Model-Connect #2207 Tests)
+
+@pytest.mark.parametrize("form", ["sequential", "chunked"])
+def test_huge_decay_limit(form):
+    shape = TINY.with_(seqlen=9)
+    prob = _tiny_problem(h0=True, shape=shape, stress=True)
+    dt_raw = np.full_like(prob["dt_raw"], 300.0)  # dt ~ 300, |A| >= 1e3 -> |dt A| >= 3e5
+    kw = dict(dt_bias=prob["dt_bias"], D=prob["D"], h0=prob["h0"])
+    if form == "sequential":
+        y, hS = oracle.ssd_sequential(prob["xbc"], dt_raw, prob["A"], **_dims(shape), **kw)
+    else:
+        y, hS = oracle.ssd_chunked(prob["xbc"], dt_raw, prob["A"], [4, 5], **_dims(shape), **kw)
+    assert np.all(np.isfinite(y)) and np.all(np.isfinite(hS))
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    dt = dt_raw[0] + prob["dt_bias"][None, :]  # softplus(v) == v to 1e-130 at v ~ 300
+    x = prob["xbc"][0, :, : H * P].reshape(-1, H, P)
+    Bm = np.repeat(prob["xbc"][0, :, H * P: H * P + G * N].reshape(-1, G, N), H // G, axis=1)
+    Cm = np.repeat(prob["xbc"][0, :, H * P + G * N:].reshape(-1, G, N), H // G, axis=1)
+    h_last = dt[-1][:, None, None] * x[-1][:, :, None] * Bm[-1][:, None, :]
+    assert _relerr(hS[0], h_last) < 1e-12
+    cb = np.einsum("thn,thn->th", Cm, Bm)
+    y_expect = (cb * dt)[:, :, None] * x + prob["D"][None, :, None] * x
+    assert _relerr(y[0], y_expect) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# invariants
+
+def test_linearity_in_x_and_h0():
+    prob = _tiny_problem(h0=True)
+    H, P = TINY.nheads, TINY.headdim
+    kw = dict(dt_bias=prob["dt_bias"], D=prob["D"])
+    y, h = oracle.ssd_sequential(prob["xbc"], prob["dt_raw"], prob["A"], **_dims(TINY),
+                                 h0=prob["h0"], **kw)
+    xbc2 = prob["xbc"].copy()
+    xbc2[..., : H * P] *= -2.5
+    y2, h2 = oracle.ssd_sequential(xbc2, prob["dt_raw"], prob["A"], **_dims(TINY),
+                                   h0=-2.5 * prob["h0"], **kw)
+    assert _relerr(y2, -2.5 * y) < 1e-13
+    assert _relerr(h2, -2.5 * h) < 1e-13
+
+
+def test_group_mapping_equals_expanded_groups():
+    """G=2 over H=4 (heads_per_group 2) == G=4 with each head's group copied
+    (the head -> group map of vllm.cpp #1362: g = h / heads_per_group)."""
+    shape = TINY.with_(ngroups=2)
+    prob = _tiny_problem(h0=True, shape=shape)
+    H, P, N = shape.nheads, shape.headdim, shape.dstate
+    xbc = prob["xbc"]
+    x = xbc[..., : H * P]
+    Bm = xbc[..., H * P: H * P + 2 * N].reshape(1, -1, 2, N)
+    Cm = xbc[..., H * P + 2 * N:].reshape(1, -1, 2, N)
+    gmap = [h // (H // 2) for h in range(H)]
+    Bx = Bm[:, :, gmap, :].reshape(1, -1, H * N)
+    Cx = Cm[:, :, gmap, :].reshape(1, -1, H * N)
+    xbc_exp = np.concatenate([x, Bx, Cx], axis=-1)
+    kw = dict(dt_bias=prob["dt_bias"], D=prob["D"], h0=prob["h0"])
+    y1, h1 = oracle.ssd_sequential(xbc, prob["dt_raw"], prob["A"], H=H, P=P, N=N, G=2, **kw)
+    y2, h2 = oracle.ssd_sequential(xbc_exp, prob["dt_raw"], prob["A"], H=H, P=P, N=N, G=H,
+                                   **kw)
+    assert np.array_equal(y1, y2) and np.array_equal(h1, h2)
+    # heads of different groups must see different B/C (guards a clamped index)
+    assert not np.allclose(y1[..., 0, :], y1[..., 3, :])
+
+
+def test_z_gate_is_silu_product():
+    prob = _tiny_problem(z=True, h0=True)
+    kw = dict(dt_bias=prob["dt_bias"], D=prob["D"], h0=prob["h0"])
+    y0, _ = oracle.ssd_sequential(prob["xbc"], prob["dt_raw"], prob["A"], **_dims(TINY), **kw)
+    yz, _ = oracle.ssd_sequential(prob["xbc"], prob["dt_raw"], prob["A"], **_dims(TINY),
+                                  z=prob["z"], **kw)
+    zz = prob["z"].reshape(y0.shape)
+    assert _relerr(yz, y0 * zz * 0.5 * (1.0 + np.tanh(0.5 * zz))) < 1e-13
+
+
+# --------------------------------------------------------------------------
+# conv
+
+def test_conv_matches_numpy_correlate():
+    rng = np.random.default_rng(5)
+    B, S, C, W = 2, 9, 5, 4
+    xbc = rng.normal(size=(B, S, C))
+    w = rng.normal(size=(C, W))
+    bias = rng.normal(size=C)
+    st = rng.normal(size=(B, W - 1, C))
+    out, st_out = oracle.conv1d(xbc, w, bias, st, apply_silu=False)
+    for b in range(B):
+        for c in range(C):
+            u = np.concatenate([st[b, :, c], xbc[b, :, c]])
+            ref = np.correlate(u, w[c], mode="valid") + bias[c]
+            assert np.allclose(out[b, :, c], ref, rtol=1e-13, atol=1e-13)
+    assert np.array_equal(st_out, xbc[:, -(W - 1):, :])
+    out_s, _ = oracle.conv1d(xbc, w, bias, st, apply_silu=True)
+    assert np.allclose(out_s, out / (1.0 + np.exp(-out)), rtol=1e-14, atol=1e-15)
+
+
+def test_conv_impulse_returns_reversed_taps():
+    W, C = 4, 3
+    w = np.arange(1.0, 1.0 + C * W).reshape(C, W)
+    xbc = np.zeros((1, 6, C))
+    xbc[0, 1, :] = 1.0
+    out, _ = oracle.conv1d(xbc, w, None, None, apply_silu=False)
+    # the impulse at row 1 meets tap W-1 (newest) at row 1, tap 0 at row 1+W-1
+    for c in range(C):
+        assert np.array_equal(out[0, 1:1 + W, c], w[c, ::-1])
+        assert out[0, 0, c] == 0.0 and out[0, 5, c] == 0.0
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 5])
+def test_conv_split_invariance(split):
+    rng = np.random.default_rng(11)
+    xbc = rng.normal(size=(2, 8, 6))
+    w = rng.normal(size=(6, 4))
+    st = rng.normal(size=(2, 3, 6))
+    out, so = oracle.conv1d(xbc, w, None, st)
+    o1, s1 = oracle.conv1d(xbc[:, :split], w, None, st)
+    o2, s2 = oracle.conv1d(xbc[:, split:], w, None, s1)
+    assert np.array_equal(np.concatenate([o1, o2], axis=1), out)
+    assert np.array_equal(s2, so)
+
+
+def test_conv_state_short_call_keeps_old_rows():
+    rng = np.random.default_rng(2)
+    st = rng.normal(size=(1, 3, 2))
+    xbc = rng.normal(size=(1, 1, 2))
+    _, so = oracle.conv1d(xbc, rng.normal(size=(2, 4)), None, st)
+    assert np.array_equal(so[0, :2], st[0, 1:]) and np.array_equal(so[0, 2], xbc[0, 0])
+
+
+# --------------------------------------------------------------------------
+# decode at slots == one row of the recurrence
+
+def test_decode_steps_equal_sequential_rows():
+    shape = TINY.with_(ngroups=2)
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    prob = _tiny_problem(h0=True, z=True, shape=shape)
+    pool = np.random.default_rng(1).normal(size=(5, H, P, N))
+    slot = 3
+    pool[slot] = prob["h0"][0]
+    before = pool.copy()
+    ys = []
+    for t in range(shape.seqlen):
+        y, pool, rc = oracle.decode_step(prob["xbc"][0, t:t + 1], prob["dt_raw"][0, t:t + 1],
+                                         prob["A"], [slot], pool, H=H, P=P, N=N, G=G,
+                                         dt_bias=prob["dt_bias"], D=prob["D"],
+                                         z=prob["z"][0, t:t + 1])
+        assert rc == 0
+        ys.append(y[0])
+    yseq, hseq = oracle.ssd_sequential(prob["xbc"], prob["dt_raw"], prob["A"], H=H, P=P, N=N,
+                                       G=G, dt_bias=prob["dt_bias"], D=prob["D"],
+                                       z=prob["z"], h0=prob["h0"])
+    assert np.array_equal(np.stack(ys), yseq[0])
+    assert np.array_equal(pool[slot], hseq[0])
+    for s in (0, 1, 2, 4):
+        assert np.array_equal(pool[s], before[s])
+
+
+def test_decode_rejects_out_of_range_slot():
+    shape = TINY
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    prob = _tiny_problem()
+    pool = np.zeros((2, H, P, N))
+    _, pool2, rc = oracle.decode_step(prob["xbc"][0, :2], prob["dt_raw"][0, :2], prob["A"],
+                                      [1, 7], pool, H=H, P=P, N=N, G=G)
+    assert rc == -1
+    assert not np.array_equal(pool2[1], pool[1])  # the valid row still ran
+    assert np.array_equal(pool2[0], pool[0])
