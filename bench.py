@@ -1,0 +1,461 @@
+"""Benchmark of the SSD mixer core on GB300: chunked prefill tokens/s per layer
+and decode-step state GB/s, each against the HBM roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one ssd_chunk_scan call (conv + SiLU + chunked scan + z gate, with
+carried conv/SSM state) over the Nemotron-H-8B-shaped prefill workload
+(B=1 sequence, S=2048 rows, 128-row chunks, H=128, P=64, N=128, G=8, W=4, bf16
+activations, fp32 state).  Inputs rotate over several resident sets whose
+total exceeds the 129 MB L2, so no step reads its inputs from L2.  The decode
+step (256 rows at slots of a 1024-slot fp32 pool [1024,128,64,128], conv pool
+fused, 64 successive steps) is measured in the same run and reported under
+"decode".  Under torchrun every rank runs its own replica (independent
+sequences: weak scaling, no collective on the data path); the times are the
+max over ranks.
+
+--impl reference times the fp64 CPU oracle (the reference implementation of
+this repository) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import ssd_inputs as si  # noqa: E402
+
+METRIC = "SSD chunked-prefill tokens/s per layer; decode-step state GB/s vs HBM peak"
+HBM_FALLBACK_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what one launch must move at minimum)
+
+def prefill_bytes(shape: si.Shape, with_z=True) -> dict:
+    """Per row: raw xBC + z + dt read, y written.  Per sequence: SSM state in
+    and out (fp32) and conv state in and out."""
+    e = 2  # bf16
+    H, P, N, G, W = shape.nheads, shape.headdim, shape.dstate, shape.ngroups, shape.conv_width
+    per_row = shape.cdim * e + (H * P * e if with_z else 0) + H * 4 + H * P * e
+    per_seq = 2 * H * P * N * 4 + 2 * (W - 1) * shape.cdim * e
+    total = shape.batch * (shape.seqlen * per_row + per_seq)
+    return {"per_row": per_row, "per_seq": per_seq, "per_launch": total}
+
+
+def decode_state_bytes(rows, shape: si.Shape) -> int:
+    return 2 * rows * shape.nheads * shape.headdim * shape.dstate * 4
+
+
+def decode_other_bytes(rows, shape: si.Shape) -> int:
+    e = 2
+    H, P, C, W = shape.nheads, shape.headdim, shape.cdim, shape.conv_width
+    return rows * (C * e + H * P * e + H * 4 + H * P * e + 2 * (W - 1) * C * e)
+
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    cdir = os.path.join(ROOT, "ssd_scan_gb300", "csrc")
+    for n in sorted(os.listdir(cdir)):
+        if n.endswith((".cu", ".cuh")):
+            with open(os.path.join(cdir, n), "rb") as f:
+                h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kind: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            tr = json.load(f)
+        ent = tr.get(kind)
+        if ent and ent.get("source_sha") == kernel_source_sha():
+            return ent.get("bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.t:
+                self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def make_prefill_sets(shape, nsets, seed_base, device):
+    import ssd_scan_gb300 as ssd
+    prm = {k: v.to(device) for k, v in si.params(shape, seed=seed_base).items()}
+    sets = []
+    d = ssd.dims(shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate,
+                 shape.ngroups, shape.conv_width, shape.chunk)
+    flags = ssd.SSD_DT_SOFTPLUS | ssd.SSD_HAS_Z
+    for i in range(nsets):
+        inp = si.prefill_inputs(shape, seed=seed_base + 1 + i, device=device)
+        B, S, H, P, N = shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate
+        out = {
+            "y": torch.empty((B, S, H, P), dtype=torch.bfloat16, device=device),
+            "hS": torch.empty((B, H, P, N), dtype=torch.float32, device=device),
+            "cs": torch.empty((B, shape.conv_width - 1, shape.cdim), dtype=torch.bfloat16,
+                              device=device),
+        }
+        ws = ssd.workspace_for(d, ssd.SSD_BF16, flags, True, device)
+        sets.append((inp, out, ws))
+    return prm, sets, d, flags
+
+
+def prefill_call(ssd, d, flags, prm, inp, out, ws, stream):
+    ssd.ssd_chunk_scan(d, ssd.SSD_BF16, flags, inp["xbc"], prm["conv_w"], prm["conv_b"],
+                       inp["conv_state"], out["cs"], inp["dt_raw"], prm["dt_bias"], prm["A"],
+                       prm["D"], inp["z"], inp["ssm_state"], out["y"], out["hS"], ws, stream)
+
+
+def bench_ours(args):
+    import ssd_scan_gb300 as ssd
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    ssd.load_library()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    shape = si.PREFILL
+    pb = prefill_bytes(shape)
+    set_bytes = pb["per_launch"]
+    nsets = max(3, -(-2 * L2_BYTES // set_bytes))  # rotate over > 2x L2 of inputs+outputs
+    prm, sets, d, flags = make_prefill_sets(shape, nsets, 1000 * rank, dev)
+
+    # ---- warm-up, then K timed steps (one ssd_chunk_scan call each)
+    for i in range(args.warmup):
+        inp, out, ws = sets[i % nsets]
+        prefill_call(ssd, d, flags, prm, inp, out, ws, stream)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = ssd.ssd_launch_counts()
+    with ClockSampler(local) as clk:
+        _barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            inp, out, ws = sets[i % nsets]
+            prefill_call(ssd, d, flags, prm, inp, out, ws, stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        _barrier(world)
+    launches1 = ssd.ssd_launch_counts()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = _max_over_ranks(ms, world)
+    gpu_launches = sum(launches1[k] - launches0[k] for k in launches0)
+    tokens_per_step = world * shape.batch * shape.seqlen
+    value = tokens_per_step / (ms / 1e3)
+
+    hbm, hbm_src = measured_peaks()
+    achieved = pb["per_launch"] / (ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": ncu_traffic("prefill"),
+                "peak_source": hbm_src,
+                "kernel": "ssd_chunk_scan call (all its kernels, events around the call)",
+                "algorithmic_bytes_per_launch": pb["per_launch"]}
+    # ---- end to end through the C-ABI from pinned host buffers
+    e2e = bench_e2e(ssd, shape, d, flags, prm, sets[0], stream, args)
+
+    # ---- decode step (config: 256 rows, 1024-slot pool, 64 steps)
+    dec = bench_decode(ssd, dev, stream, world, args)
+
+    out = None
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "nemotron-h-8b mixer prefill: B=1 x S=2048 rows per GPU, "
+                                   "chunk 128, H=128 P=64 N=128 G=8 W=4, conv+SiLU and z-gate "
+                                   "fused, carried conv/ssm state",
+                       "batch_per_gpu": shape.batch, "seq_len": shape.seqlen,
+                       "parallelism": f"replicas x{world} (independent sequences)",
+                       "l2": f"inputs rotate over {nsets} resident sets "
+                             f"({nsets * set_bytes / 1e6:.0f} MB > 129 MB L2)"},
+            "roofline": roofline,
+            "e2e": e2e,
+            "gpu_launches": gpu_launches,
+            "clocks": clk.summary(),
+            "decode": dec,
+        }
+    return out
+
+
+def bench_e2e(ssd, shape, d, flags, prm, dset, stream, args):
+    inp, out, ws = dset
+    host_in = {k: v.cpu().pin_memory() for k, v in inp.items() if v is not None}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    dev_in = {k: torch.empty_like(v, device="cuda") for k, v in host_in.items()}
+
+    def step():
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        prefill_call(ssd, d, flags, prm, dev_in, out, ws, stream)
+        for k, v in out.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 20))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(n):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / n
+    return {"value": round(shape.batch * shape.seqlen / (ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4)}
+
+
+def bench_decode(ssd, dev, stream, world, args):
+    shape = si.DECODE
+    R, nslots = si.DECODE_ROWS, si.DECODE_SLOTS
+    prm = {k: v.to(dev) for k, v in si.params(shape).items()}
+    pools = {k: v.to(dev) for k, v in si.decode_pools(shape, nslots, device=dev).items()}
+    nin = 8
+    ins = [{k: v.to(dev) for k, v in si.decode_inputs(shape, t, device=dev).items()}
+           for t in range(nin)]
+    y = torch.empty((R, shape.nheads, shape.headdim), dtype=torch.bfloat16, device=dev)
+    d = ssd.dims(R, 1, shape.nheads, shape.headdim, shape.dstate, shape.ngroups,
+                 shape.conv_width)
+    flags = ssd.SSD_DT_SOFTPLUS | ssd.SSD_HAS_Z
+
+    def step(t):
+        inp = ins[t % nin]
+        ssd.ssd_decode_step(d, ssd.SSD_BF16, flags, inp["xbc"], prm["conv_w"], prm["conv_b"],
+                            pools["conv_pool"], inp["dt_raw"], prm["dt_bias"], prm["A"],
+                            prm["D"], inp["z"], pools["slot_ids"], nslots, pools["ssm_pool"], y,
+                            stream)
+
+    for t in range(max(3, args.warmup)):
+        step(t)
+    torch.cuda.synchronize()
+    steps = si.DECODE_STEPS
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    ev0.record(stream)
+    for t in range(steps):
+        step(t)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = _max_over_ranks(ev0.elapsed_time(ev1) / steps, world)
+    hbm, src = measured_peaks()
+    sb = decode_state_bytes(R, shape)
+    gbs = sb / (ms / 1e3) / 1e9
+    total = (sb + decode_other_bytes(R, shape)) / (ms / 1e3) / 1e9
+    assert ssd.ssd_read_device_error(stream) == ssd.SSD_OK
+    return {"metric": "decode-step state GB/s", "value": round(gbs * world, 1), "unit": "GB/s",
+            "per_gpu_gbs": round(gbs, 1), "ms_per_step": round(ms, 5), "steps": steps,
+            "rows": R, "slots": nslots, "state_bytes_per_step": sb,
+            "all_bytes_gbs": round(total, 1), "peak": hbm, "peak_source": src,
+            "frac": round(gbs / hbm, 4), "traffic": ncu_traffic("decode")}
+
+
+# ---------------------------------------------------------------------------
+# the fp64 oracle on the host cores
+
+def oracle_sample_rows() -> int:
+    return int(os.environ.get("SSD_BENCH_ORACLE_ROWS", "128"))
+
+
+def oracle_prefill_sample(rows: int):
+    """Time the oracle on the first ``rows`` rows of the prefill workload (all
+    heads: conv + SiLU + recurrence + gate).  Returns (seconds, threads)."""
+    import oracle
+    import numpy as np
+    shape = si.PREFILL.with_(seqlen=rows)
+    prm = si.params(shape, seed=0)
+    inp = si.prefill_inputs(shape, seed=1)
+    f = lambda t: None if t is None else t.to(torch.float64).numpy()  # noqa: E731
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    args = (f(inp["xbc"]), f(prm["conv_w"]), f(inp["dt_raw"]), f(prm["A"]))
+    kw = dict(H=H, P=P, N=N, G=G, conv_b=f(prm["conv_b"]), conv_state=f(inp["conv_state"]),
+              dt_bias=f(prm["dt_bias"]), D=f(prm["D"]), z=f(inp["z"]), h0=f(inp["ssm_state"]))
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    y, h, c = oracle.mixer_prefill(*args, nthreads=threads, **kw)
+    dt = time.perf_counter() - t0
+    assert np.isfinite(y).all()
+    return dt, threads
+
+
+def cpu_baseline() -> dict:
+    rows = oracle_sample_rows()
+    dt, threads = oracle_prefill_sample(rows)
+    return {"value": round(rows / dt, 2), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {rows} of the 2048 rows of the prefill workload, all 128 heads "
+                      f"(conv + recurrence + gate, fp64), {dt:.2f} s"}
+
+
+def bench_reference(args):
+    rank, world, local = _dist()
+    if rank != 0:
+        return None
+    rows = oracle_sample_rows()
+    for _ in range(args.warmup):
+        oracle_prefill_sample(rows)
+    times = []
+    threads = 1
+    for _ in range(args.steps):
+        dt, threads = oracle_prefill_sample(rows)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = rows / (ms / 1e3)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "nemotron-h-8b mixer prefill (as the main arm); each step is a "
+                               f"bounded sample: the first {rows} rows, all 128 heads",
+                   "batch_per_gpu": 1, "seq_len": rows, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": threads,
+                         "kind": "oracle", "sample": f"first {rows} rows x 128 heads per step"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        res = bench_reference(args)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    res = bench_ours(args)
+    rank, world, _ = _dist()
+    if rank == 0 and res is not None:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+/*
+ * ssd.h -- C-ABI of the GB300 (sm_103a) Mamba-2 / SSD mixer core.
+ *
+ * Three operations, each one call on a CUDA stream:
+ *   ssd_conv1d_rows  causal depthwise conv1d + SiLU over [conv state ; rows]
+ *   ssd_chunk_scan   the chunked SSD scan over S prefill rows (optionally with
+ *                    the conv fused in front), with carried conv/SSM state
+ *   ssd_decode_step  one recurrent step for R rows at slot-indexed states,
+ *                    updated in place
+ *
+ * Sources (page title, section):
+ *   TensorRT-Model-Connect PR #2207 "perf(nemotron_h): prefill single-GPU
+ *     prompts in multi-token chunks", "Implementation": the chunk form
+ *     (a_t = dt_t A, gamma_t = cumulative sum of a, gamma_S taken from the
+ *     last cumulative-sum element, every exponent clamped at <= 0, 128-row
+ *     chunks) and add_short_conv_rows (conv over previous state plus chunk).
+ *   TensorSharp "docs/models/nemotron.md", 4.1 "Mamba2 SSM layer": the
+ *     single-step recurrence dA = exp(softplus(dt + dt_bias) A),
+ *     state = dA state + dt x B, y = state . C + D x; section 3 "Forward
+ *     graph": conv, SiLU, scan, gate; section 6: parameter shapes; section
+ *     10/11: conv state of convKernel-1 rows, per-slot state pools.
+ *   vllm.cpp PR #1362 "NemotronH decodes on the single-step recurrent
+ *     kernels": the x | B | C split of the conv output, the head -> group map
+ *     g = h / (H / G), and the in-place state update at the state slot.
+ *
+ * Conventions shared by every call:
+ *   - Every data pointer is DEVICE memory owned by the caller; the library
+ *     keeps no pointer after the call returns and allocates nothing.  The only
+ *     state the library holds is one device error word per GPU (see
+ *     ssd_read_device_error).
+ *   - Arrays are dense, row-major, contiguous, in the layouts stated below.
+ *     Data pointers must be 16-byte aligned and the row lengths a multiple of
+ *     16 bytes (Cdim * sizeof(act) and H * P * sizeof(act)); otherwise the
+ *     call returns SSD_ERR_INVALID_ARG.
+ *   - Calls are asynchronous on `stream`.  All argument checks run on the host
+ *     before anything is launched; on any error nothing is launched and no
+ *     memory is touched.
+ *   - A = the per-head decay rate, stored NEGATIVE (decay exp(dt A) <= 1).
+ *   - dt = softplus(dt_raw + dt_bias) when SSD_DT_SOFTPLUS is set, else dt_raw
+ *     (dt_bias ignored).  softplus has no threshold.
+ *   - Conv: tap k = W-1 multiplies the newest row; the conv state holds the
+ *     W-1 most recent raw (pre-conv) rows, oldest first, in the activation
+ *     dtype.
+ *   - The SSM state is always fp32, layout [.., H, P, N] (N fastest).
+ *   - With SSD_HAS_Z, y is multiplied by silu(z) (the gate of the gated norm;
+ *     the group RMSNorm itself is not part of these calls).
+ */
+#ifndef SSD_GB300_SSD_H
+#define SSD_GB300_SSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, bad flag   */
+    SSD_ERR_UNSUPPORTED = 2,  /* valid problem that no kernel here implements  */
+    SSD_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, query)     */
+    SSD_ERR_BAD_SLOT = 4,     /* device error word: a slot id out of range      */
+    SSD_ERR_TIMEOUT = 5       /* device error word: a bounded wait ran out      */
+} ssd_status;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype; /* activation dtype */
+
+enum {
+    SSD_DT_SOFTPLUS = 1u,  /* dt = softplus(dt_raw + dt_bias)                    */
+    SSD_HAS_Z = 2u         /* multiply y by silu(z)                              */
+};
+
+/*
+ * Problem dimensions.  Cdim = nheads*headdim + 2*ngroups*dstate is the width
+ * of the x | B | C stream.  nheads % ngroups == 0.  conv_width W in [1, 8].
+ * chunk: rows per chunk of the chunk form; 0 selects 128.  The bf16 path runs
+ * 128-row chunks only (other values -> SSD_ERR_UNSUPPORTED); the fp32 path
+ * is exact in any chunking and ignores it.
+ */
+typedef struct {
+    int batch, seqlen, nheads, headdim, dstate, ngroups, conv_width, chunk;
+} ssd_dims;
+
+/*
+ * ssd_conv1d_rows -- causal depthwise conv1d with SiLU over S rows.
+ * (TensorRT-Model-Connect #2207 "Implementation", add_short_conv_rows;
+ *  TensorSharp nemotron.md section 3, Conv1dStep + SiLU.)
+ *
+ *   u = [conv_state_in ; xbc_in]   (W-1+S rows per sequence)
+ *   xbc_out[b,t,c] = silu(conv_b[c] + sum_k conv_w[c,k] * u[b,t+k,c])
+ *   conv_state_out[b] = the last W-1 rows of u
+ *
+ * xbc_in          [B,S,Cdim] act   raw rows
+ * conv_w          [Cdim,W]   fp32
+ * conv_b          [Cdim]     fp32, or NULL (no bias)
+ * conv_state_in   [B,W-1,Cdim] act, or NULL (zeros: a fresh sequence)
+ * xbc_out         [B,S,Cdim] act   (must not overlap xbc_in)
+ * conv_state_out  [B,W-1,Cdim] act, or NULL (not written); may alias
+ *                 conv_state_in exactly
+ * Only batch, seqlen, conv_width and Cdim (from nheads, headdim, dstate,
+ * ngroups) of `dims` are used.  S = 0 is valid (the state is copied).
+ */
+SSD_API ssd_status ssd_conv1d_rows(const ssd_dims* dims, ssd_dtype act,
+                           const void* xbc_in, const float* conv_w, const float* conv_b,
+                           const void* conv_state_in, void* xbc_out, void* conv_state_out,
+                           cudaStream_t stream);
+
+/*
+ * ssd_chunk_scan -- the SSD scan over S prefill rows per sequence.
+ * (TensorRT-Model-Connect #2207 "Implementation": chunk form, gamma_S from
+ *  the last cumulative-sum element, exponents clamped <= 0; TensorSharp
+ *  nemotron.md 4.1: the recurrence it equals.)
+ *
+ * For each sequence b and head h (group g = h / (H/G)), rows t = 0..S-1:
+ *   dt_t = softplus(dt[b,t,h] + dt_bias[h])            (flag SSD_DT_SOFTPLUS)
+ *   state = exp(dt_t A[h]) state + dt_t x_t B_t^T       state [P,N]
+ *   y[b,t,h,:] = state C_t + D[h] x_t   (times silu(z) with SSD_HAS_Z)
+ * computed in 128-row chunks (bf16) or exactly row by row (fp32).
+ *
+ * xbc             [B,S,Cdim] act: raw rows when conv_w != NULL (the conv of
+ *                 ssd_conv1d_rows runs first), else already post-conv rows.
+ *                 Columns: x [H*P] | B [G*N] | C [G*N].
+ * conv_w, conv_b  as in ssd_conv1d_rows (conv_b may be NULL); conv_w NULL
+ *                 means no conv (conv_state_* must then be NULL).
+ * conv_state_in   [B,W-1,Cdim] act or NULL (zeros)
+ * conv_state_out  [B,W-1,Cdim] act or NULL; may alias conv_state_in
+ * dt              [B,S,H]  fp32 (raw dt before the bias/softplus)
+ * dt_bias         [H] fp32 or NULL (zero)
+ * A               [H] fp32 (negative)
+ * D               [H] fp32 or NULL (no skip term)
+ * z               [B,S,H*P] act; required iff SSD_HAS_Z
+ * ssm_state_in    [B,H,P,N] fp32 or NULL (zeros: a fresh request)
+ * y               [B,S,H,P] act
+ * ssm_state_out   [B,H,P,N] fp32; may alias ssm_state_in exactly
+ * workspace       device scratch of at least ssd_chunk_scan_workspace_size()
+ *                 bytes (may be NULL when that size is 0); contents on entry
+ *                 are ignored, on exit undefined.  Two calls in flight at the
+ *                 same time must not share one workspace.
+ *
+ * Calls chain: feeding ssm_state_out / conv_state_out of one call into the
+ * next call as *_in continues the same sequences (any split of the rows).
+ */
+SSD_API ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned flags,
+                          const void* xbc, const float* conv_w, const float* conv_b,
+                          const void* conv_state_in, void* conv_state_out,
+                          const float* dt, const float* dt_bias, const float* A,
+                          const float* D, const void* z, const float* ssm_state_in,
+                          void* y, float* ssm_state_out,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Scratch bytes ssd_chunk_scan needs for these dims, activation dtype and
+ * whether the conv is fused (conv_fused != 0 <=> conv_w != NULL).  Writes the
+ * size to *bytes.  Returns SSD_ERR_INVALID_ARG for invalid dims.
+ */
+SSD_API ssd_status ssd_chunk_scan_workspace_size(const ssd_dims* dims, ssd_dtype act, unsigned flags,
+                                         int conv_fused, size_t* bytes);
+
+/*
+ * ssd_decode_step -- one recurrent step for R rows at slot-indexed states.
+ * (TensorSharp nemotron.md 4.1 and section 11 "Batched / paged forward":
+ *  per-slot conv + SSM state pool; vllm.cpp #1362: the update runs in place
+ *  at the state slot, no gather/scatter copies.)
+ *
+ * dims->batch = R rows, dims->seqlen must be 1.  For row i, s = slot_ids[i]:
+ *   if conv_w != NULL:  u = [conv_pool[s] ; xbc[i]],  x|B|C = silu(conv(u)),
+ *                       conv_pool[s] = last W-1 rows of u        (in place)
+ *   else                x|B|C = xbc[i]
+ *   ssm_pool[s,h] = exp(dt A[h]) ssm_pool[s,h] + dt x_h B_g^T     (in place)
+ *   y[i,h,:] = ssm_pool[s,h] C_g + D[h] x_h   (times silu(z) with SSD_HAS_Z)
+ *
+ * xbc        [R,Cdim] act (raw when conv_w != NULL)
+ * conv_pool  [num_slots,W-1,Cdim] act; required iff conv_w != NULL
+ * dt         [R,H] fp32;  dt_bias, A, D, z as in ssd_chunk_scan ([R,H*P] for z)
+ * slot_ids   [R] int32, DEVICE memory.  Ids must be distinct (not checked:
+ *            duplicate ids race).  An id outside [0, num_slots) sets the
+ *            device error word to SSD_ERR_BAD_SLOT and that row writes
+ *            nothing (neither pool nor y); other rows are unaffected.
+ * ssm_pool   [num_slots,H,P,N] fp32, updated in place
+ * y          [R,H,P] act
+ */
+SSD_API ssd_status ssd_decode_step(const ssd_dims* dims, ssd_dtype act, unsigned flags,
+                           const void* xbc, const float* conv_w, const float* conv_b,
+                           void* conv_pool, const float* dt, const float* dt_bias,
+                           const float* A, const float* D, const void* z,
+                           const int32_t* slot_ids, int num_slots, float* ssm_pool, void* y,
+                           cudaStream_t stream);
+
+/*
+ * Kernel-launch counters, for observability (which path ran, how many
+ * kernels a call launched).  Host-side, process-wide, monotonically
+ * increasing; one counter per kernel kind below.  Copies min(n,
+ * SSD_KERNEL_KINDS) counters into out[] and returns SSD_KERNEL_KINDS.
+ */
+enum {
+    SSD_KERNEL_CONV_ROWS = 0,      /* conv1d + SiLU over rows               */
+    SSD_KERNEL_CONV_STATE = 1,     /* conv state = last W-1 raw rows        */
+    SSD_KERNEL_SCAN_SIMT = 2,      /* fp32-pipe scan (exact row order)      */
+    SSD_KERNEL_SCAN_TC = 3,        /* tensor-core chunk scan (bf16)         */
+    SSD_KERNEL_BC_CONV = 4,        /* conv of the B|C columns for the scan  */
+    SSD_KERNEL_DECODE_STEP = 5,    /* slot-indexed decode step              */
+    SSD_KERNEL_DECODE_CONV = 6,    /* conv-pool roll of the decode step     */
+    SSD_KERNEL_KINDS = 7
+};
+SSD_API int ssd_launch_counts(uint64_t* out, int n);
+
+/* Static text for a status code (never NULL). */
+SSD_API const char* ssd_status_string(ssd_status status);
+
+/*
+ * Synchronises `stream`, then returns and clears the device error word of the
+ * current device: SSD_OK, SSD_ERR_BAD_SLOT or SSD_ERR_TIMEOUT (the first
+ * error kind recorded since the last read), or SSD_ERR_CUDA if a CUDA call
+ * failed.
+ */
+SSD_API ssd_status ssd_read_device_error(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_GB300_SSD_H */

@@ -1,0 +1,229 @@
+"""Python binding of the GB300 SSD mixer-core library (``libssd_gb300.so``).
+
+The functions below carry the names of the C-ABI entry points declared in
+``include/ssd.h`` and only marshal arguments: torch tensors (device memory,
+used for allocation and streams only) become raw pointers, ``None`` becomes
+NULL, and a non-OK status raises :class:`SsdError`.  Every step of the
+computation runs in the library's CUDA kernels; there is no other path.  If
+the library has not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libssd_gb300.so")
+
+SSD_OK = 0
+SSD_ERR_INVALID_ARG = 1
+SSD_ERR_UNSUPPORTED = 2
+SSD_ERR_CUDA = 3
+SSD_ERR_BAD_SLOT = 4
+SSD_ERR_TIMEOUT = 5
+
+SSD_F32 = 0
+SSD_BF16 = 1
+
+SSD_DT_SOFTPLUS = 1
+SSD_HAS_Z = 2
+
+# every symbol include/ssd.h declares
+EXPORTED = ("ssd_conv1d_rows", "ssd_chunk_scan", "ssd_chunk_scan_workspace_size",
+            "ssd_decode_step", "ssd_status_string", "ssd_read_device_error",
+            "ssd_launch_counts")
+
+KERNEL_KINDS = ("conv_rows", "conv_state", "scan_simt", "scan_tc", "bc_conv", "decode_step",
+                "decode_conv")
+
+
+class SsdError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {ssd_status_string(status)} (status {status})")
+
+
+class ssd_dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("batch", "seqlen", "nheads", "headdim", "dstate",
+                                            "ngroups", "conv_width", "chunk")]
+
+    @property
+    def cdim(self) -> int:
+        return self.nheads * self.headdim + 2 * self.ngroups * self.dstate
+
+
+def dims(batch, seqlen, nheads, headdim, dstate, ngroups, conv_width=4, chunk=128) -> ssd_dims:
+    return ssd_dims(batch, seqlen, nheads, headdim, dstate, ngroups, conv_width, chunk)
+
+
+_lib = None
+_lock = threading.Lock()
+_vp = ctypes.c_void_p
+
+
+def load_library():
+    """Load libssd_gb300.so (raises if it is missing: there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with `python -m ssd_scan_gb300.build` "
+                    "(nvcc, sm_103a); the SSD library has no CPU fallback")
+            lib = ctypes.CDLL(LIB_PATH)
+            P = ctypes.POINTER(ssd_dims)
+            ci, cu, sz = ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
+            lib.ssd_conv1d_rows.argtypes = [P, ci, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+            lib.ssd_chunk_scan.argtypes = [P, ci, cu] + [_vp] * 14 + [sz, _vp]
+            lib.ssd_chunk_scan_workspace_size.argtypes = [P, ci, cu, ci, ctypes.POINTER(sz)]
+            lib.ssd_decode_step.argtypes = [P, ci, cu] + [_vp] * 10 + [ci, _vp, _vp, _vp]
+            lib.ssd_status_string.argtypes = [ci]
+            lib.ssd_status_string.restype = ctypes.c_char_p
+            lib.ssd_read_device_error.argtypes = [_vp]
+            lib.ssd_launch_counts.argtypes = [ctypes.POINTER(ctypes.c_uint64), ci]
+            for n in EXPORTED:
+                if n != "ssd_status_string":
+                    getattr(lib, n).restype = ci
+            _lib = lib
+    return _lib
+
+
+def ssd_status_string(status: int) -> str:
+    return load_library().ssd_status_string(int(status)).decode()
+
+
+_ACT = {SSD_F32: torch.float32, SSD_BF16: torch.bfloat16}
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor or None")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA (device) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    return _vp(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return _vp(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return _vp(stream.cuda_stream)
+    return _vp(int(stream))
+
+
+def _check(status, where):
+    if status != SSD_OK:
+        raise SsdError(status, where)
+
+
+def act_of(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SSD_BF16
+    if t.dtype == torch.float32:
+        return SSD_F32
+    raise TypeError(f"unsupported activation dtype {t.dtype}")
+
+
+def ssd_conv1d_rows(d: ssd_dims, act: int, xbc_in, conv_w, conv_b, conv_state_in, xbc_out,
+                    conv_state_out, stream=None) -> None:
+    a = _ACT[act]
+    f = torch.float32
+    _check(load_library().ssd_conv1d_rows(
+        ctypes.byref(d), act, _ptr(xbc_in, a, "xbc_in"), _ptr(conv_w, f, "conv_w"),
+        _ptr(conv_b, f, "conv_b"), _ptr(conv_state_in, a, "conv_state_in"),
+        _ptr(xbc_out, a, "xbc_out"), _ptr(conv_state_out, a, "conv_state_out"),
+        _stream(stream)), "ssd_conv1d_rows")
+
+
+def ssd_chunk_scan_workspace_size(d: ssd_dims, act: int, flags: int, conv_fused: bool) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().ssd_chunk_scan_workspace_size(ctypes.byref(d), act, flags,
+                                                         1 if conv_fused else 0,
+                                                         ctypes.byref(out)),
+           "ssd_chunk_scan_workspace_size")
+    return int(out.value)
+
+
+def ssd_chunk_scan(d: ssd_dims, act: int, flags: int, xbc, conv_w, conv_b, conv_state_in,
+                   conv_state_out, dt, dt_bias, A, D, z, ssm_state_in, y, ssm_state_out,
+                   workspace=None, stream=None) -> None:
+    a = _ACT[act]
+    f = torch.float32
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().ssd_chunk_scan(
+        ctypes.byref(d), act, flags, _ptr(xbc, a, "xbc"), _ptr(conv_w, f, "conv_w"),
+        _ptr(conv_b, f, "conv_b"), _ptr(conv_state_in, a, "conv_state_in"),
+        _ptr(conv_state_out, a, "conv_state_out"), _ptr(dt, f, "dt"),
+        _ptr(dt_bias, f, "dt_bias"), _ptr(A, f, "A"), _ptr(D, f, "D"), _ptr(z, a, "z"),
+        _ptr(ssm_state_in, f, "ssm_state_in"), _ptr(y, a, "y"),
+        _ptr(ssm_state_out, f, "ssm_state_out"), _ptr(workspace, None, "workspace"),
+        ws_bytes, _stream(stream)), "ssd_chunk_scan")
+
+
+def ssd_decode_step(d: ssd_dims, act: int, flags: int, xbc, conv_w, conv_b, conv_pool, dt,
+                    dt_bias, A, D, z, slot_ids, num_slots: int, ssm_pool, y,
+                    stream=None) -> None:
+    a = _ACT[act]
+    f = torch.float32
+    _check(load_library().ssd_decode_step(
+        ctypes.byref(d), act, flags, _ptr(xbc, a, "xbc"), _ptr(conv_w, f, "conv_w"),
+        _ptr(conv_b, f, "conv_b"), _ptr(conv_pool, a, "conv_pool"), _ptr(dt, f, "dt"),
+        _ptr(dt_bias, f, "dt_bias"), _ptr(A, f, "A"), _ptr(D, f, "D"), _ptr(z, a, "z"),
+        _ptr(slot_ids, torch.int32, "slot_ids"), int(num_slots),
+        _ptr(ssm_pool, f, "ssm_pool"), _ptr(y, a, "y"), _stream(stream)), "ssd_decode_step")
+
+
+def ssd_launch_counts() -> dict:
+    """Process-wide number of kernels the library launched, per kernel kind."""
+    buf = (ctypes.c_uint64 * len(KERNEL_KINDS))()
+    n = load_library().ssd_launch_counts(buf, len(KERNEL_KINDS))
+    assert n == len(KERNEL_KINDS), n
+    return {k: int(buf[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def ssd_read_device_error(stream=None) -> int:
+    """Synchronise the stream; return and clear the device error word (a status)."""
+    return int(load_library().ssd_read_device_error(_stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# allocation helpers (torch allocates; the library computes)
+
+def workspace_for(d: ssd_dims, act: int, flags: int, conv_fused: bool, device) -> torch.Tensor | None:
+    n = ssd_chunk_scan_workspace_size(d, act, flags, conv_fused)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def chunk_scan(xbc, dt, A, *, nheads, headdim, dstate, ngroups, conv_w=None, conv_b=None,
+               conv_state=None, dt_bias=None, D=None, z=None, ssm_state=None,
+               dt_softplus=True, out=None, workspace=None, stream=None):
+    """Allocate outputs and call ssd_chunk_scan.  Returns (y, ssm_state_out,
+    conv_state_out or None)."""
+    B, S, _ = xbc.shape
+    W = conv_w.shape[1] if conv_w is not None else 4
+    d = dims(B, S, nheads, headdim, dstate, ngroups, W, 128)
+    act = act_of(xbc)
+    flags = (SSD_DT_SOFTPLUS if dt_softplus else 0) | (SSD_HAS_Z if z is not None else 0)
+    if out is None:
+        y = torch.empty((B, S, nheads, headdim), dtype=xbc.dtype, device=xbc.device)
+        hs = torch.empty((B, nheads, headdim, dstate), dtype=torch.float32, device=xbc.device)
+        cs = (torch.empty((B, W - 1, d.cdim), dtype=xbc.dtype, device=xbc.device)
+              if conv_w is not None else None)
+    else:
+        y, hs, cs = out
+    if workspace is None:
+        workspace = workspace_for(d, act, flags, conv_w is not None, xbc.device)
+    ssd_chunk_scan(d, act, flags, xbc, conv_w, conv_b, conv_state, cs, dt, dt_bias, A, D, z,
+                   ssm_state, y, hs, workspace, stream)
+    return y, hs, cs

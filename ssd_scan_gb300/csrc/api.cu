@@ -1,0 +1,247 @@
+// api.cu -- the C-ABI of include/ssd.h: argument checks, dispatch, the
+// per-device error word.  Every check runs before any launch; on error the
+// call returns without touching device memory.
+#include "../../include/ssd.h"
+#include "internal.cuh"
+
+#include <stdint.h>
+
+#include <atomic>
+
+namespace {
+
+using namespace ssd;
+
+// One error word per device (each device that loads the module has its own
+// copy).  Kernels receive its address; ssd_read_device_error reads & clears.
+__device__ unsigned g_ssd_error_word;
+
+constexpr int kMaxDevices = 64;
+unsigned* g_err_addr[kMaxDevices];  // host cache of each device's symbol address
+
+ssd_status error_word_address(unsigned** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
+    if (g_err_addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_ssd_error_word) != cudaSuccess) return SSD_ERR_CUDA;
+        g_err_addr[dev] = static_cast<unsigned*>(ptr);
+    }
+    *out = g_err_addr[dev];
+    return SSD_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Checks common to all calls.  Cdim is written on success.
+ssd_status check_dims(const ssd_dims* d, ssd_dtype act, long long* cdim)
+{
+    if (d == nullptr) return SSD_ERR_INVALID_ARG;
+    if (act != SSD_F32 && act != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    if (d->batch < 0 || d->seqlen < 0 || d->nheads <= 0 || d->headdim <= 0 || d->dstate <= 0 ||
+        d->ngroups <= 0 || d->nheads % d->ngroups != 0 || d->conv_width < 1 ||
+        d->conv_width > 8 || d->chunk < 0)
+        return SSD_ERR_INVALID_ARG;
+    const long long c = (long long)d->nheads * d->headdim + 2LL * d->ngroups * d->dstate;
+    if (c > (1LL << 30)) return SSD_ERR_INVALID_ARG;
+    const long long esize = act == SSD_BF16 ? 2 : 4;
+    if ((c * esize) % 16 != 0) return SSD_ERR_INVALID_ARG;
+    // every flat index used by the kernels fits in 63 bits
+    const long long rows = (long long)d->batch * d->seqlen;
+    if (rows > 0 && c > (1LL << 62) / rows) return SSD_ERR_INVALID_ARG;
+    *cdim = c;
+    return SSD_OK;
+}
+
+ssd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
+
+std::atomic<uint64_t> g_launches[SSD_KERNEL_KINDS];
+
+// Records one launch of `kind` when it succeeded (kernels that a launcher
+// skips for empty work are not launched and not counted).
+ssd_status counted(cudaError_t e, int kind, bool launched = true)
+{
+    if (e == cudaSuccess && launched) g_launches[kind].fetch_add(1, std::memory_order_relaxed);
+    return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssd_launch_counts(uint64_t* out, int n)
+{
+    for (int i = 0; out != nullptr && i < n && i < SSD_KERNEL_KINDS; ++i)
+        out[i] = g_launches[i].load(std::memory_order_relaxed);
+    return SSD_KERNEL_KINDS;
+}
+
+const char* ssd_status_string(ssd_status s)
+{
+    switch (s) {
+        case SSD_OK: return "ok";
+        case SSD_ERR_INVALID_ARG: return "invalid argument";
+        case SSD_ERR_UNSUPPORTED: return "unsupported problem shape or dtype";
+        case SSD_ERR_CUDA: return "CUDA runtime error";
+        case SSD_ERR_BAD_SLOT: return "slot id out of range (device)";
+        case SSD_ERR_TIMEOUT: return "bounded device wait ran out (device)";
+    }
+    return "unknown status";
+}
+
+ssd_status ssd_read_device_error(cudaStream_t stream)
+{
+    unsigned* addr = nullptr;
+    if (error_word_address(&addr) != SSD_OK) return SSD_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return SSD_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, addr, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SSD_ERR_CUDA;
+    const unsigned zero = 0;
+    if (cudaMemcpy(addr, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (v & kErrBadSlot) return SSD_ERR_BAD_SLOT;
+    if (v & kErrTimeout) return SSD_ERR_TIMEOUT;
+    return SSD_OK;
+}
+
+ssd_status ssd_conv1d_rows(const ssd_dims* dims, ssd_dtype act, const void* xbc_in,
+                           const float* conv_w, const float* conv_b, const void* conv_state_in,
+                           void* xbc_out, void* conv_state_out, cudaStream_t stream)
+{
+    long long cdim = 0;
+    ssd_status s = check_dims(dims, act, &cdim);
+    if (s != SSD_OK) return s;
+    const bool any_rows = dims->batch > 0 && dims->seqlen > 0;
+    if (conv_w == nullptr || !aligned4(conv_w) || (conv_b && !aligned4(conv_b)))
+        return SSD_ERR_INVALID_ARG;
+    if (any_rows && (xbc_in == nullptr || xbc_out == nullptr || !aligned16(xbc_in) ||
+                     !aligned16(xbc_out) || xbc_in == xbc_out))
+        return SSD_ERR_INVALID_ARG;
+    if ((conv_state_in && !aligned16(conv_state_in)) ||
+        (conv_state_out && !aligned16(conv_state_out)))
+        return SSD_ERR_INVALID_ARG;
+    if (dims->batch == 0) return SSD_OK;
+    ConvParams p{dims->batch, dims->seqlen, (int)cdim, dims->conv_width,
+                 xbc_in, conv_w, conv_b, conv_state_in, xbc_out, conv_state_out};
+    const bool bf16 = act == SSD_BF16;
+    s = counted(launch_conv1d_rows(p, bf16, stream), SSD_KERNEL_CONV_ROWS,
+                dims->seqlen > 0);
+    if (s != SSD_OK) return s;
+    return counted(launch_conv_state(p, bf16, stream), SSD_KERNEL_CONV_STATE,
+                   conv_state_out != nullptr && dims->conv_width > 1);
+}
+
+ssd_status ssd_chunk_scan_workspace_size(const ssd_dims* dims, ssd_dtype act, unsigned flags,
+                                         int conv_fused, size_t* bytes)
+{
+    long long cdim = 0;
+    if (bytes == nullptr) return SSD_ERR_INVALID_ARG;
+    ssd_status s = check_dims(dims, act, &cdim);
+    if (s != SSD_OK) return s;
+    if (flags & ~(unsigned)(SSD_DT_SOFTPLUS | SSD_HAS_Z)) return SSD_ERR_INVALID_ARG;
+    (void)conv_fused;
+    *bytes = 0;
+    return SSD_OK;
+}
+
+ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned flags, const void* xbc,
+                          const float* conv_w, const float* conv_b, const void* conv_state_in,
+                          void* conv_state_out, const float* dt, const float* dt_bias,
+                          const float* A, const float* D, const void* z,
+                          const float* ssm_state_in, void* y, float* ssm_state_out,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    long long cdim = 0;
+    ssd_status s = check_dims(dims, act, &cdim);
+    if (s != SSD_OK) return s;
+    if (flags & ~(unsigned)(SSD_DT_SOFTPLUS | SSD_HAS_Z)) return SSD_ERR_INVALID_ARG;
+    const bool rows = dims->batch > 0 && dims->seqlen > 0;
+    const bool has_z = (flags & SSD_HAS_Z) != 0;
+    if (rows && (xbc == nullptr || dt == nullptr || y == nullptr || !aligned16(xbc) ||
+                 !aligned16(y) || !aligned4(dt)))
+        return SSD_ERR_INVALID_ARG;
+    if (A == nullptr || !aligned4(A) || (dt_bias && !aligned4(dt_bias)) || (D && !aligned4(D)))
+        return SSD_ERR_INVALID_ARG;
+    if (has_z && rows && (z == nullptr || !aligned16(z))) return SSD_ERR_INVALID_ARG;
+    if (ssm_state_out == nullptr || !aligned16(ssm_state_out) ||
+        (ssm_state_in && !aligned16(ssm_state_in)))
+        return SSD_ERR_INVALID_ARG;
+    if (conv_w == nullptr && (conv_state_in || conv_state_out || conv_b))
+        return SSD_ERR_INVALID_ARG;
+    if (conv_w && !aligned4(conv_w)) return SSD_ERR_INVALID_ARG;
+    if ((conv_state_in && !aligned16(conv_state_in)) ||
+        (conv_state_out && !aligned16(conv_state_out)))
+        return SSD_ERR_INVALID_ARG;
+    size_t need = 0;
+    s = ssd_chunk_scan_workspace_size(dims, act, flags, conv_w != nullptr, &need);
+    if (s != SSD_OK) return s;
+    if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned16(workspace))))
+        return SSD_ERR_INVALID_ARG;
+    const int chunk = dims->chunk == 0 ? 128 : dims->chunk;
+    if (act == SSD_BF16 && chunk != 128) return SSD_ERR_UNSUPPORTED;
+    if (!scan_simt_supports(dims->headdim, dims->dstate)) return SSD_ERR_UNSUPPORTED;
+    if (dims->batch == 0) return SSD_OK;
+
+    unsigned* err = nullptr;
+    s = error_word_address(&err);
+    if (s != SSD_OK) return s;
+    const bool bf16 = act == SSD_BF16;
+    ScanParams p{dims->batch, dims->seqlen, dims->nheads, dims->headdim, dims->dstate,
+                 dims->ngroups, dims->conv_width, flags, xbc, conv_w, conv_b, conv_state_in,
+                 dt, dt_bias, A, D, has_z ? z : nullptr, ssm_state_in, y, ssm_state_out, err};
+    s = counted(launch_scan_simt(p, bf16, stream), SSD_KERNEL_SCAN_SIMT);
+    if (s != SSD_OK) return s;
+    if (conv_w != nullptr && conv_state_out != nullptr) {
+        ConvParams cp{dims->batch, dims->seqlen, (int)cdim, dims->conv_width,
+                      xbc, conv_w, conv_b, conv_state_in, nullptr, conv_state_out};
+        s = counted(launch_conv_state(cp, bf16, stream), SSD_KERNEL_CONV_STATE,
+                    dims->conv_width > 1);
+    }
+    return s;
+}
+
+ssd_status ssd_decode_step(const ssd_dims* dims, ssd_dtype act, unsigned flags, const void* xbc,
+                           const float* conv_w, const float* conv_b, void* conv_pool,
+                           const float* dt, const float* dt_bias, const float* A,
+                           const float* D, const void* z, const int32_t* slot_ids,
+                           int num_slots, float* ssm_pool, void* y, cudaStream_t stream)
+{
+    long long cdim = 0;
+    ssd_status s = check_dims(dims, act, &cdim);
+    if (s != SSD_OK) return s;
+    if (dims->seqlen != 1) return SSD_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)(SSD_DT_SOFTPLUS | SSD_HAS_Z)) return SSD_ERR_INVALID_ARG;
+    const bool rows = dims->batch > 0;
+    const bool has_z = (flags & SSD_HAS_Z) != 0;
+    if (num_slots < 0 || (rows && num_slots == 0)) return SSD_ERR_INVALID_ARG;
+    if (rows && (xbc == nullptr || dt == nullptr || y == nullptr || slot_ids == nullptr ||
+                 ssm_pool == nullptr || !aligned16(xbc) || !aligned16(y) || !aligned4(dt) ||
+                 !aligned4(slot_ids) || !aligned16(ssm_pool)))
+        return SSD_ERR_INVALID_ARG;
+    if (A == nullptr || !aligned4(A) || (dt_bias && !aligned4(dt_bias)) || (D && !aligned4(D)))
+        return SSD_ERR_INVALID_ARG;
+    if (has_z && rows && (z == nullptr || !aligned16(z))) return SSD_ERR_INVALID_ARG;
+    if (conv_w == nullptr && (conv_pool || conv_b)) return SSD_ERR_INVALID_ARG;
+    if (conv_w && (!aligned4(conv_w) || conv_pool == nullptr || !aligned16(conv_pool)))
+        return SSD_ERR_INVALID_ARG;
+    if (dims->dstate % 4 != 0 || dims->headdim % 4 != 0) return SSD_ERR_UNSUPPORTED;
+    if (sizeof(float) * (size_t)(dims->headdim + 2 * dims->dstate) > 200 * 1024)
+        return SSD_ERR_UNSUPPORTED;
+    if (!rows) return SSD_OK;
+
+    unsigned* err = nullptr;
+    s = error_word_address(&err);
+    if (s != SSD_OK) return s;
+    const bool bf16 = act == SSD_BF16;
+    DecodeParams p{dims->batch, dims->nheads, dims->headdim, dims->dstate, dims->ngroups,
+                   dims->conv_width, flags, xbc, conv_w, conv_b, conv_pool, dt, dt_bias, A, D,
+                   has_z ? z : nullptr, slot_ids, num_slots, ssm_pool, y, err};
+    s = counted(launch_decode_step(p, bf16, stream), SSD_KERNEL_DECODE_STEP);
+    if (s != SSD_OK) return s;
+    return counted(launch_decode_conv_roll(p, bf16, stream), SSD_KERNEL_DECODE_CONV,
+                   conv_w != nullptr && dims->conv_width > 1);
+}
+
+}  // extern "C"

@@ -1,0 +1,172 @@
+// conv1d.cu -- causal depthwise conv1d + SiLU over [conv state ; rows].
+//
+// TensorRT-Model-Connect #2207 "Implementation" (add_short_conv_rows: the
+// causal depthwise conv over the previous conv state plus the chunk) and
+// TensorSharp nemotron.md section 3 (Conv1dStep then SiLU), section 6
+// (ssm_conv1d.weight [xBCSize, convKernel], optional bias).
+//
+// HBM-bound: every raw element is read once and every output written once.
+// One thread owns 16 bytes of channels (8 bf16 / 4 fp32) and walks a run of
+// rows, keeping the last W-1 raw rows of its channels in registers, so a
+// warp reads and writes 512 contiguous bytes per row.
+#include "internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kRowsPerThread = 64;
+
+template <typename T> struct Vec16;
+template <> struct Vec16<__nv_bfloat16> {
+    static constexpr int n = 8;
+    __device__ static void load(const __nv_bfloat16* p, float* v)
+    {
+        uint4 r = __ldg(reinterpret_cast<const uint4*>(p));
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(h[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+    __device__ static void store(__nv_bfloat16* p, const float* v)
+    {
+        uint4 r;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&r);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        *reinterpret_cast<uint4*>(p) = r;
+    }
+};
+template <> struct Vec16<float> {
+    static constexpr int n = 4;
+    __device__ static void load(const float* p, float* v)
+    {
+        float4 r = __ldg(reinterpret_cast<const float4*>(p));
+        v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
+    }
+    __device__ static void store(float* p, const float* v)
+    {
+        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+};
+
+template <typename T, int W>
+__global__ void __launch_bounds__(128) conv1d_rows_kernel(ConvParams p)
+{
+    constexpr int V = Vec16<T>::n;
+    const int nvec = p.C / V;
+    const int cv = blockIdx.x * blockDim.x + threadIdx.x;
+    if (cv >= nvec) return;
+    const int b = blockIdx.z;
+    const int t0 = blockIdx.y * kRowsPerThread;
+    const int t1 = min(t0 + kRowsPerThread, p.S);
+    const int c0 = cv * V;
+    const T* x = static_cast<const T*>(p.x);
+    const T* st = static_cast<const T*>(p.st_in);
+    T* out = static_cast<T*>(p.out);
+
+    float w[W][V], bias[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        bias[j] = p.bias ? __ldg(p.bias + c0 + j) : 0.0f;
+#pragma unroll
+        for (int k = 0; k < W; ++k) w[k][j] = __ldg(p.w + (size_t)(c0 + j) * W + k);
+    }
+    // hist[k] = raw row t0-(W-1)+k of these channels (from the state when < 0)
+    float hist[W > 1 ? W - 1 : 1][V];
+#pragma unroll
+    for (int k = 0; k < W - 1; ++k) {
+        const int r = t0 - (W - 1) + k;
+        if (r >= 0) {
+            Vec16<T>::load(x + ((size_t)b * p.S + r) * p.C + c0, hist[k]);
+        } else if (st) {
+            Vec16<T>::load(st + ((size_t)b * (W - 1) + (r + W - 1)) * p.C + c0, hist[k]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < V; ++j) hist[k][j] = 0.0f;
+        }
+    }
+    for (int t = t0; t < t1; ++t) {
+        float cur[V], o[V];
+        Vec16<T>::load(x + ((size_t)b * p.S + t) * p.C + c0, cur);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            float v = bias[j];
+#pragma unroll
+            for (int k = 0; k < W - 1; ++k) v = fmaf(w[k][j], hist[k][j], v);
+            v = fmaf(w[W - 1][j], cur[j], v);
+            o[j] = silu_f32(v);
+        }
+        Vec16<T>::store(out + ((size_t)b * p.S + t) * p.C + c0, o);
+#pragma unroll
+        for (int k = 0; k + 1 < W - 1; ++k)
+#pragma unroll
+            for (int j = 0; j < V; ++j) hist[k][j] = hist[k + 1][j];
+        if (W > 1) {
+#pragma unroll
+            for (int j = 0; j < V; ++j) hist[W > 1 ? W - 2 : 0][j] = cur[j];
+        }
+    }
+}
+
+// conv_state_out[b, j, c] = u[b, S + j, c] with u = [state_in ; x].  One
+// thread per (b, c) walks j upwards, so an in-place call (st_out == st_in)
+// only ever overwrites rows it has already read.
+template <typename T>
+__global__ void conv_state_kernel(ConvParams p)
+{
+    const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (size_t)p.B * p.C) return;
+    const int b = (int)(idx / p.C), c = (int)(idx % p.C);
+    const int nh = p.W - 1;
+    const T* x = static_cast<const T*>(p.x);
+    const T* st = static_cast<const T*>(p.st_in);
+    T* so = static_cast<T*>(p.st_out);
+    for (int j = 0; j < nh; ++j) {
+        const int r = p.S + j;  // index into u
+        T v;
+        if (r < nh) v = st ? st[((size_t)b * nh + r) * p.C + c] : from_f32<T>(0.0f);
+        else v = x[((size_t)b * p.S + (r - nh)) * p.C + c];
+        so[((size_t)b * nh + j) * p.C + c] = v;
+    }
+}
+
+template <typename T>
+cudaError_t launch_rows_t(const ConvParams& p, cudaStream_t st)
+{
+    constexpr int V = Vec16<T>::n;
+    const int nvec = p.C / V;
+    dim3 block(128);
+    dim3 grid((nvec + 127) / 128, (p.S + kRowsPerThread - 1) / kRowsPerThread, p.B);
+    switch (p.W) {
+#define SSD_CONV_CASE(w) \
+    case w: conv1d_rows_kernel<T, w><<<grid, block, 0, st>>>(p); break;
+        SSD_CONV_CASE(1) SSD_CONV_CASE(2) SSD_CONV_CASE(3) SSD_CONV_CASE(4)
+        SSD_CONV_CASE(5) SSD_CONV_CASE(6) SSD_CONV_CASE(7) SSD_CONV_CASE(8)
+#undef SSD_CONV_CASE
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_conv1d_rows(const ConvParams& p, bool bf16, cudaStream_t st)
+{
+    if (p.B == 0 || p.S == 0 || p.C == 0) return cudaSuccess;
+    return bf16 ? launch_rows_t<__nv_bfloat16>(p, st) : launch_rows_t<float>(p, st);
+}
+
+cudaError_t launch_conv_state(const ConvParams& p, bool bf16, cudaStream_t st)
+{
+    if (p.B == 0 || p.W <= 1 || p.C == 0 || p.st_out == nullptr) return cudaSuccess;
+    const size_t n = (size_t)p.B * p.C;
+    dim3 grid((unsigned)((n + 255) / 256));
+    if (bf16) conv_state_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
+    else conv_state_kernel<float><<<grid, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ssd

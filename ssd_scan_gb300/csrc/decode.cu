@@ -1,0 +1,165 @@
+// decode.cu -- one recurrent step at slot-indexed states, in place.
+//
+// TensorSharp nemotron.md 4.1 (the single-step update dA = exp(dt A),
+// state = dA state + dt x B^T, y = state . C + D x) and section 11 (per-slot
+// conv + SSM state pool); vllm.cpp #1362 (the update runs at the state slot
+// in place, with no gather/scatter copies of the states).
+//
+// The state read-modify-write is the whole cost: per (row, head) P*N fp32
+// are read once and written once.  One CTA per (row i, head h): its warps
+// split the P state rows; a lane owns 16 bytes (4 consecutive n) of a state
+// row, so every warp access is a contiguous 512-byte run, loaded with
+// streaming hints (the pool is touched once per step).  y[p] is a warp
+// shuffle reduction over n.
+#include "internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kRowsInFlight = 4;  // state rows a warp keeps in flight
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
+{
+    extern __shared__ float sm[];  // x [P] | B [N] | C [N]
+    const int h = blockIdx.x, i = blockIdx.y;
+    const int H = p.H, P = p.P, N = p.N, G = p.G;
+    const int g = h / (H / G);
+    const int Cdim = H * P + 2 * G * N;
+    const int CH = P + 2 * N;
+    const int s = p.slots[i];
+    if (s < 0 || s >= p.num_slots) {
+        if (threadIdx.x == 0 && h == 0) atomicOr(p.err, kErrBadSlot);
+        return;
+    }
+    const T* xbc = static_cast<const T*>(p.xbc);
+    const T* cpool = static_cast<const T*>(p.conv_pool);
+    const int HW = p.W - 1;
+    for (int c = threadIdx.x; c < CH; c += blockDim.x) {
+        const int gc = c < P ? h * P + c
+                             : (c < P + N ? H * P + g * N + (c - P)
+                                          : H * P + G * N + g * N + (c - P - N));
+        float v;
+        if (p.conv_w) {
+            v = p.conv_b ? p.conv_b[gc] : 0.0f;
+            for (int k = 0; k < HW; ++k)
+                v = fmaf(p.conv_w[(size_t)gc * p.W + k],
+                         to_f32(cpool[((size_t)s * HW + k) * Cdim + gc]), v);
+            v = fmaf(p.conv_w[(size_t)gc * p.W + HW], to_f32(xbc[(size_t)i * Cdim + gc]), v);
+            v = v / (1.0f + expf(-v));
+        } else {
+            v = to_f32(xbc[(size_t)i * Cdim + gc]);
+        }
+        sm[c] = v;
+    }
+    float dt = p.dt[(size_t)i * H + h];
+    if (p.flags & kDtSoftplus) dt = softplus_f32(dt + (p.dt_bias ? p.dt_bias[h] : 0.0f));
+    const float dA = expf(dt * p.A[h]);
+    const float Dh = p.D ? p.D[h] : 0.0f;
+    __syncthreads();
+
+    const float* xs = sm;
+    const float4* B4 = reinterpret_cast<const float4*>(sm + P);
+    const float4* C4 = reinterpret_cast<const float4*>(sm + P + N);
+    float4* st = reinterpret_cast<float4*>(p.pool + ((size_t)s * H + h) * (size_t)P * N);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+    const int nv = N / 4;  // float4 per state row
+    const T* zz = static_cast<const T*>(p.z);
+    T* y = static_cast<T*>(p.y);
+
+    for (int p0 = warp * kRowsInFlight; p0 < P; p0 += nwarp * kRowsInFlight) {
+        float acc[kRowsInFlight];
+#pragma unroll
+        for (int r = 0; r < kRowsInFlight; ++r) acc[r] = 0.0f;
+        for (int v = lane; v < nv; v += 32) {
+            float4 hv[kRowsInFlight];
+#pragma unroll
+            for (int r = 0; r < kRowsInFlight; ++r)
+                if (p0 + r < P) hv[r] = __ldcs(st + (size_t)(p0 + r) * nv + v);
+            const float4 bv = B4[v], cv = C4[v];
+#pragma unroll
+            for (int r = 0; r < kRowsInFlight; ++r) {
+                if (p0 + r >= P) continue;
+                const float dx = dt * xs[p0 + r];
+                float4 o;
+                o.x = fmaf(dA, hv[r].x, dx * bv.x);
+                o.y = fmaf(dA, hv[r].y, dx * bv.y);
+                o.z = fmaf(dA, hv[r].z, dx * bv.z);
+                o.w = fmaf(dA, hv[r].w, dx * bv.w);
+                acc[r] = fmaf(o.x, cv.x, acc[r]);
+                acc[r] = fmaf(o.y, cv.y, acc[r]);
+                acc[r] = fmaf(o.z, cv.z, acc[r]);
+                acc[r] = fmaf(o.w, cv.w, acc[r]);
+                __stcs(st + (size_t)(p0 + r) * nv + v, o);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kRowsInFlight; ++r) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
+        }
+        if (lane < kRowsInFlight && p0 + lane < P) {
+            float a = acc[0];
+#pragma unroll
+            for (int r = 1; r < kRowsInFlight; ++r) a = lane == r ? acc[r] : a;
+            const int pp = p0 + lane;
+            float yv = fmaf(Dh, xs[pp], a);
+            if (p.flags & kHasZ) {
+                const float zv = to_f32(zz[(size_t)i * H * P + h * P + pp]);
+                yv *= zv / (1.0f + expf(-zv));
+            }
+            y[((size_t)i * H + h) * P + pp] = from_f32<T>(yv);
+        }
+    }
+}
+
+// conv_pool[s] <- [conv_pool[s][1:], raw row i]  (one thread per (row, channel);
+// it reads row k+1 before writing row k, so the shift is in place).
+template <typename T>
+__global__ void decode_conv_roll_kernel(DecodeParams p)
+{
+    const int Cdim = p.H * p.P + 2 * p.G * p.N;
+    const int i = blockIdx.y;
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= Cdim) return;
+    const int s = p.slots[i];
+    if (s < 0 || s >= p.num_slots) return;
+    const int HW = p.W - 1;
+    T* cp = static_cast<T*>(p.conv_pool) + (size_t)s * HW * Cdim;
+    for (int k = 0; k + 1 < HW; ++k) cp[(size_t)k * Cdim + c] = cp[(size_t)(k + 1) * Cdim + c];
+    cp[(size_t)(HW - 1) * Cdim + c] = static_cast<const T*>(p.xbc)[(size_t)i * Cdim + c];
+}
+
+}  // namespace
+
+cudaError_t launch_decode_step(const DecodeParams& p, bool bf16, cudaStream_t st)
+{
+    if (p.R == 0) return cudaSuccess;
+    dim3 grid(p.H, p.R);
+    const size_t smem = sizeof(float) * (size_t)(p.P + 2 * p.N);
+    if (bf16) {
+        cudaError_t e = cudaFuncSetAttribute(decode_step_kernel<__nv_bfloat16>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        decode_step_kernel<__nv_bfloat16><<<grid, kThreads, smem, st>>>(p);
+    } else {
+        cudaError_t e = cudaFuncSetAttribute(decode_step_kernel<float>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        decode_step_kernel<float><<<grid, kThreads, smem, st>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_conv_roll(const DecodeParams& p, bool bf16, cudaStream_t st)
+{
+    if (p.R == 0 || p.conv_w == nullptr || p.W <= 1) return cudaSuccess;
+    const int Cdim = p.H * p.P + 2 * p.G * p.N;
+    dim3 grid((Cdim + 255) / 256, p.R);
+    if (bf16) decode_conv_roll_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
+    else decode_conv_roll_kernel<float><<<grid, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ssd

@@ -1,0 +1,90 @@
+// internal.cuh -- launch parameters and helpers shared by the kernels of the
+// GB300 SSD library.  Not part of the public ABI (see include/ssd.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssd {
+
+// Bits of the per-device error word (first error kind wins in the report).
+enum : unsigned { kErrBadSlot = 1u, kErrTimeout = 2u };
+
+enum : unsigned { kDtSoftplus = 1u, kHasZ = 2u };
+
+struct ConvParams {
+    int B, S, C, W;
+    const void* x;        // [B,S,C] act, raw rows
+    const float* w;       // [C,W]
+    const float* bias;    // [C] or null
+    const void* st_in;    // [B,W-1,C] act or null
+    void* out;            // [B,S,C] act
+    void* st_out;         // [B,W-1,C] act or null
+};
+
+struct ScanParams {
+    int B, S, H, P, N, G, W;
+    unsigned flags;
+    const void* xbc;            // [B,S,Cdim] act
+    const float* conv_w;        // [Cdim,W] or null (xbc already post-conv)
+    const float* conv_b;        // [Cdim] or null
+    const void* conv_state_in;  // [B,W-1,Cdim] act or null
+    const float* dt;            // [B,S,H]
+    const float* dt_bias;       // [H] or null
+    const float* A;             // [H]
+    const float* D;             // [H] or null
+    const void* z;              // [B,S,H*P] act or null
+    const float* h0;            // [B,H,P,N] or null
+    void* y;                    // [B,S,H,P] act
+    float* hS;                  // [B,H,P,N]
+    unsigned* err;              // device error word
+};
+
+struct DecodeParams {
+    int R, H, P, N, G, W;
+    unsigned flags;
+    const void* xbc;        // [R,Cdim] act
+    const float* conv_w;    // [Cdim,W] or null
+    const float* conv_b;    // [Cdim] or null
+    void* conv_pool;        // [num_slots,W-1,Cdim] act or null
+    const float* dt;        // [R,H]
+    const float* dt_bias;   // [H] or null
+    const float* A;         // [H]
+    const float* D;         // [H] or null
+    const void* z;          // [R,H*P] act or null
+    const int32_t* slots;   // [R]
+    int num_slots;
+    float* pool;            // [num_slots,H,P,N]
+    void* y;                // [R,H,P] act
+    unsigned* err;
+};
+
+// ---- element conversions --------------------------------------------------
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v)
+{
+    return __float2bfloat16_rn(v);
+}
+
+// silu(v) = v * sigmoid(v), fp32, IEEE division.
+__device__ __forceinline__ float silu_f32(float v) { return v / (1.0f + __expf(-v)); }
+
+// softplus(v) = max(v,0) + log1p(exp(-|v|)), no threshold.
+__device__ __forceinline__ float softplus_f32(float v)
+{
+    return fmaxf(v, 0.0f) + log1pf(__expf(-fabsf(v)));
+}
+
+// ---- launchers (each returns the cudaError_t of its launch) ----------------
+cudaError_t launch_conv1d_rows(const ConvParams& p, bool bf16, cudaStream_t st);
+cudaError_t launch_conv_state(const ConvParams& p, bool bf16, cudaStream_t st);
+cudaError_t launch_scan_simt(const ScanParams& p, bool bf16, cudaStream_t st);
+bool scan_simt_supports(int P, int N);
+cudaError_t launch_decode_step(const DecodeParams& p, bool bf16, cudaStream_t st);
+cudaError_t launch_decode_conv_roll(const DecodeParams& p, bool bf16, cudaStream_t st);
+
+}  // namespace ssd

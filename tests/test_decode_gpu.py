@@ -1,0 +1,166 @@
+"""GPU tests of ssd_decode_step: parity with the oracle and bit-exact slot
+indexing (untouched slots unchanged, permutation invariance, in-place update
+equal to a gathered contiguous copy), plus the bad-slot error word."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ssd_inputs as si
+from tests.helpers import TOL, assert_close, f64
+
+pytestmark = pytest.mark.gpu
+
+ssd = pytest.importorskip("ssd_scan_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ssd.load_library()
+    yield
+
+
+def _setup(shape, num_slots, seed=0, act=torch.bfloat16, with_z=True):
+    prm = {k: v.cuda() for k, v in si.params(shape, seed=seed).items()}
+    pools = si.decode_pools(shape, num_slots, seed=seed, act_dtype=act, device="cuda")
+    return prm, pools
+
+
+def _step(shape, prm, pools, inp, conv=True, slots=None, pool=None, conv_pool=None,
+          with_z=True):
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    R = inp["xbc"].shape[0]
+    d = ssd.dims(R, 1, H, P, N, G, shape.conv_width)
+    y = torch.empty((R, H, P), dtype=inp["xbc"].dtype, device="cuda")
+    flags = ssd.SSD_DT_SOFTPLUS | (ssd.SSD_HAS_Z if with_z else 0)
+    pool = pools["ssm_pool"] if pool is None else pool
+    cpool = pools["conv_pool"] if conv_pool is None else conv_pool
+    slots = pools["slot_ids"] if slots is None else slots
+    ssd.ssd_decode_step(d, ssd.act_of(inp["xbc"]), flags, inp["xbc"],
+                        prm["conv_w"] if conv else None, prm["conv_b"] if conv else None,
+                        cpool if conv else None, inp["dt_raw"], prm["dt_bias"], prm["A"],
+                        prm["D"], inp["z"] if with_z else None, slots, pool.shape[0], pool, y)
+    return y
+
+
+def _inputs(shape, step, seed=0, act=torch.bfloat16):
+    return {k: (v.cuda() if v is not None else None)
+            for k, v in si.decode_inputs(shape, step, seed=seed, act_dtype=act).items()}
+
+
+@pytest.mark.parametrize("act", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("conv", [True, False])
+def test_decode_matches_oracle_over_steps(act, conv):
+    shape = si.Shape(batch=12, seqlen=1, nheads=8, headdim=64, dstate=128, ngroups=2)
+    prm, pools = _setup(shape, 40, act=act)
+    pool0 = pools["ssm_pool"].clone()
+    cpool0 = pools["conv_pool"].clone()
+    steps = 5
+    ys, ins = [], []
+    for t in range(steps):
+        inp = _inputs(shape, t, act=act)
+        ins.append(inp)
+        ys.append(_step(shape, prm, pools, inp, conv=conv))
+    slots = pools["slot_ids"].cpu().numpy()
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    # the oracle: each row continues the sequence held in its slot
+    xbc_seq = np.stack([f64(i["xbc"]) for i in ins], axis=1)      # [R, steps, C]
+    dt_seq = np.stack([f64(i["dt_raw"]) for i in ins], axis=1)    # [R, steps, H]
+    z_seq = np.stack([f64(i["z"]) for i in ins], axis=1)
+    y_o, h_o, c_o = oracle.mixer_prefill(
+        xbc_seq, f64(prm["conv_w"]) if conv else None, dt_seq, f64(prm["A"]), H=H, P=P, N=N,
+        G=G, conv_b=f64(prm["conv_b"]) if conv else None,
+        conv_state=f64(cpool0)[slots] if conv else None, dt_bias=f64(prm["dt_bias"]),
+        D=f64(prm["D"]), z=z_seq, h0=f64(pool0)[slots])
+    y_gpu = torch.stack(ys, dim=1)  # [R, steps, H, P]
+    tol = TOL[act]
+    assert_close(y_gpu, y_o, tol, count=12 * steps * H * P, what="y")
+    assert_close(pools["ssm_pool"][pools["slot_ids"].long()], h_o, tol, what="pool")
+    if conv:
+        assert np.array_equal(f64(pools["conv_pool"])[slots], c_o)
+
+
+def test_untouched_slots_and_permutation_bit_exact():
+    shape = si.Shape(batch=16, seqlen=1, nheads=8, headdim=64, dstate=128, ngroups=2)
+    prm, pools = _setup(shape, 64)
+    pool0 = pools["ssm_pool"].clone()
+    cpool0 = pools["conv_pool"].clone()
+    slots = pools["slot_ids"]
+    steps = 8
+    ins = [_inputs(shape, t) for t in range(steps)]
+    ys = [_step(shape, prm, pools, ins[t]) for t in range(steps)]
+    # (i) slots not in slot_ids are byte-identical
+    mask = torch.ones(64, dtype=torch.bool, device="cuda")
+    mask[slots.long()] = False
+    assert torch.equal(pools["ssm_pool"][mask], pool0[mask])
+    assert torch.equal(pools["conv_pool"][mask], cpool0[mask])
+    # (ii) the same sequences in permuted rows give byte-identical results
+    perm = torch.randperm(16, generator=torch.Generator().manual_seed(9)).cuda()
+    pool_b, cpool_b = pool0.clone(), cpool0.clone()
+    ys_b = []
+    for t in range(steps):
+        inp = {k: v[perm].contiguous() for k, v in ins[t].items()}
+        ys_b.append(_step(shape, prm, pools, inp, slots=slots[perm].contiguous(), pool=pool_b,
+                          conv_pool=cpool_b))
+    for t in range(steps):
+        assert torch.equal(ys_b[t], ys[t][perm])
+    assert torch.equal(pool_b, pools["ssm_pool"])
+    assert torch.equal(cpool_b, pools["conv_pool"])
+    # (iii) in place at the slots == a gathered contiguous copy, identity slots
+    g_pool = pool0[slots.long()].contiguous()
+    g_cpool = cpool0[slots.long()].contiguous()
+    ident = torch.arange(16, dtype=torch.int32, device="cuda")
+    for t in range(steps):
+        yg = _step(shape, prm, pools, ins[t], slots=ident, pool=g_pool, conv_pool=g_cpool)
+        assert torch.equal(yg, ys[t])
+    assert torch.equal(g_pool, pools["ssm_pool"][slots.long()])
+    assert torch.equal(g_cpool, pools["conv_pool"][slots.long()])
+
+
+def test_bad_slot_sets_error_word_and_writes_nothing():
+    shape = si.Shape(batch=4, seqlen=1, nheads=4, headdim=64, dstate=128, ngroups=1)
+    prm, pools = _setup(shape, 8)
+    assert ssd.ssd_read_device_error() == ssd.SSD_OK
+    slots = torch.tensor([2, 8, 5, -1], dtype=torch.int32, device="cuda")
+    pool0 = pools["ssm_pool"].clone()
+    cpool0 = pools["conv_pool"].clone()
+    inp = _inputs(shape, 0)
+    y = _step(shape, prm, pools, inp, slots=slots)
+    assert ssd.ssd_read_device_error() == ssd.SSD_ERR_BAD_SLOT
+    assert ssd.ssd_read_device_error() == ssd.SSD_OK  # read clears it
+    changed = [bool((pools["ssm_pool"][s] != pool0[s]).any()) for s in range(8)]
+    assert changed == [s in (2, 5) for s in range(8)]
+    cchanged = [bool((pools["conv_pool"][s] != cpool0[s]).any()) for s in range(8)]
+    assert cchanged == [s in (2, 5) for s in range(8)]
+    assert torch.isfinite(y[0].float()).all() and torch.isfinite(y[2].float()).all()
+
+
+def test_decode_full_size_sampled():
+    """256 rows in a 1024-slot pool [1024,128,64,128] fp32, 64 steps; the oracle
+    follows 3 rows through all steps."""
+    shape = si.DECODE
+    prm, pools = _setup(shape, si.DECODE_SLOTS)
+    rows = [0, 101, 255]
+    slots = pools["slot_ids"].cpu().numpy()
+    h0 = f64(pools["ssm_pool"][pools["slot_ids"][rows].long()])
+    c0 = f64(pools["conv_pool"][pools["slot_ids"][rows].long()])
+    xs, dts, zs, ys = [], [], [], []
+    for t in range(si.DECODE_STEPS):
+        inp = _inputs(shape, t)
+        y = _step(shape, prm, pools, inp)
+        xs.append(f64(inp["xbc"][rows]))
+        dts.append(f64(inp["dt_raw"][rows]))
+        zs.append(f64(inp["z"][rows]))
+        ys.append(y[rows].float().cpu())
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    y_o, h_o, c_o = oracle.mixer_prefill(
+        np.stack(xs, 1), f64(prm["conv_w"]), np.stack(dts, 1), f64(prm["A"]), H=H, P=P, N=N,
+        G=G, conv_b=f64(prm["conv_b"]), conv_state=c0, dt_bias=f64(prm["dt_bias"]),
+        D=f64(prm["D"]), z=np.stack(zs, 1), h0=h0)
+    assert_close(torch.stack(ys, 1), y_o, TOL[torch.bfloat16], what="y")
+    assert_close(pools["ssm_pool"][pools["slot_ids"][rows].long()], h_o, TOL[torch.bfloat16],
+                 what="pool")
+    assert np.array_equal(f64(pools["conv_pool"][pools["slot_ids"][rows].long()]), c_o)
+    assert torch.isfinite(pools["ssm_pool"][pools["slot_ids"].long()]).all()

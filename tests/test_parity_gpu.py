@@ -1,0 +1,151 @@
+"""GPU parity: the CUDA library (through the C-ABI) against the fp64 oracle.
+
+Every test here runs the library's kernels on cuda:0 and compares with the
+oracle on the same seeded inputs (tests/helpers.py states the tolerance).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ssd_inputs as si
+from tests.helpers import (TOL, assert_close, f64, gpu_prefill, make_problem,
+                           oracle_prefill)
+
+pytestmark = pytest.mark.gpu
+
+ssd = pytest.importorskip("ssd_scan_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ssd.load_library()
+    yield
+    assert ssd.ssd_read_device_error() == ssd.SSD_OK
+
+
+def _check_prefill(shape, cpu, y, h, cs, act, conv=True, dt_softplus=True, heads=None,
+                   batches=None):
+    yo, ho, co, cols = oracle_prefill(shape, cpu, conv=conv, dt_softplus=dt_softplus,
+                                      heads=heads, batches=batches)
+    hh = list(range(shape.nheads)) if heads is None else list(heads)
+    bb = list(range(shape.batch)) if batches is None else list(batches)
+    tol = TOL[act]
+    P, N = shape.headdim, shape.dstate
+    e1 = assert_close(y[bb][:, :, hh], yo, tol, count=len(bb) * shape.seqlen * len(hh) * P,
+                      what="y")
+    e2 = assert_close(h[bb][:, hh], ho, tol, count=len(bb) * len(hh) * P * N, what="ssm_state")
+    if conv and cs is not None:
+        gcs = f64(cs)[bb][:, :, cols]
+        assert np.array_equal(gcs, co), "conv state must be the raw rows, bit for bit"
+    return e1, e2
+
+
+# ---------------------------------------------------------------------------
+# tiny fp32 problem: 11 rows in one call, as 7 + 4, and one row per call
+
+@pytest.mark.parametrize("splits", [[11], [7, 4], [1] * 11, [3, 5, 3]])
+@pytest.mark.parametrize("init", [False, True])
+def test_tiny_fp32(splits, init):
+    shape = si.TINY
+    cpu, dev = make_problem(shape, act=torch.float32, initial_state=init, with_z=True)
+    y, h, cs = gpu_prefill(shape, dev, splits)
+    _check_prefill(shape, cpu, y, h, cs, torch.float32)
+
+
+def test_tiny_fp32_no_conv_no_z_no_softplus():
+    shape = si.TINY
+    cpu, dev = make_problem(shape, act=torch.float32, with_z=False)
+    y, h, _ = gpu_prefill(shape, dev, [7, 4], conv=False, dt_softplus=False)
+    dev2 = dict(dev)
+    dev2["dt_raw"] = dev["dt_raw"].abs() * 0.1
+    cpu2 = dict(cpu)
+    cpu2["dt_raw"] = cpu["dt_raw"].abs() * 0.1
+    y, h, _ = gpu_prefill(shape, dev2, [7, 4], conv=False, dt_softplus=False)
+    _check_prefill(shape, cpu2, y, h, None, torch.float32, conv=False, dt_softplus=False)
+
+
+def test_dt_zero_leaves_state_bit_unchanged():
+    shape = si.TINY
+    cpu, dev = make_problem(shape, act=torch.float32)
+    dev["dt_raw"] = torch.zeros_like(dev["dt_raw"])
+    y, h, _ = gpu_prefill(shape, dev, [7, 4], conv=False, dt_softplus=False)
+    assert torch.equal(h, dev["ssm_state"])
+
+
+# ---------------------------------------------------------------------------
+# conv alone
+
+@pytest.mark.parametrize("act", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("S", [1, 2, 5, 200])
+@pytest.mark.parametrize("inplace", [False, True])
+def test_conv1d_rows(act, S, inplace):
+    shape = si.TINY.with_(batch=3, seqlen=S)
+    cpu, dev = make_problem(shape, act=act)
+    C, W = shape.cdim, shape.conv_width
+    d = ssd.dims(3, S, shape.nheads, shape.headdim, shape.dstate, shape.ngroups, W)
+    out = torch.empty_like(dev["xbc"])
+    st_in = dev["conv_state"].clone()
+    st_out = st_in if inplace else torch.empty_like(st_in)
+    ssd.ssd_conv1d_rows(d, ssd.act_of(out), dev["xbc"], dev["conv_w"], dev["conv_b"], st_in,
+                        out, st_out)
+    ref, ref_st = oracle.conv1d(f64(cpu["xbc"]), f64(cpu["conv_w"]), f64(cpu["conv_b"]),
+                                f64(cpu["conv_state"]))
+    assert_close(out, ref, TOL[act], count=3 * S * C, what="conv out")
+    assert np.array_equal(f64(st_out), ref_st)
+
+
+# ---------------------------------------------------------------------------
+# bf16 prefill at small sizes that span several 128-row chunks + ragged tail
+
+@pytest.mark.parametrize("splits", [[300], [128, 172], [37, 91, 172], [1, 299]])
+def test_prefill_bf16_multichunk(splits):
+    shape = si.Shape(batch=2, seqlen=300, nheads=8, headdim=64, dstate=128, ngroups=2)
+    cpu, dev = make_problem(shape, act=torch.bfloat16)
+    y, h, cs = gpu_prefill(shape, dev, splits)
+    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
+
+
+def test_prefill_bf16_fresh_request_no_z():
+    shape = si.Shape(batch=1, seqlen=137, nheads=4, headdim=64, dstate=128, ngroups=1)
+    cpu, dev = make_problem(shape, act=torch.bfloat16, initial_state=False, with_z=False)
+    y, h, cs = gpu_prefill(shape, dev)
+    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
+
+
+def test_prefill_empty_rows_copies_state():
+    shape = si.Shape(batch=2, seqlen=0, nheads=4, headdim=64, dstate=128, ngroups=1)
+    cpu, dev = make_problem(shape, act=torch.bfloat16)
+    y, h, cs = gpu_prefill(shape, dev)
+    assert y.numel() == 0
+    assert torch.equal(h, dev["ssm_state"])
+    assert torch.equal(cs, dev["conv_state"])
+
+
+def test_decay_stress_small():
+    shape = si.Shape(batch=2, seqlen=260, nheads=4, headdim=64, dstate=128, ngroups=1)
+    cpu, dev = make_problem(shape, act=torch.bfloat16, stress=True)
+    splits = si.random_splits(260, seed=3)
+    y, h, cs = gpu_prefill(shape, dev, splits)
+    assert torch.isfinite(y.float()).all() and torch.isfinite(h).all()
+    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------
+# Nemotron-H-8B-shaped prefill at full size: B=1, S=2048, H=128 (sampled heads)
+
+def test_prefill_full_size_sampled_heads():
+    shape = si.PREFILL
+    cpu, dev = make_problem(shape, act=torch.bfloat16)
+    y, h, cs = gpu_prefill(shape, dev)
+    assert torch.isfinite(y.float()).all() and torch.isfinite(h).all()
+    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16, heads=[0, 17, 63, 64, 127])
+
+
+def test_prefill_137_rows_full_heads_sampled():
+    shape = si.PREFILL.with_(seqlen=137)
+    cpu, dev = make_problem(shape, act=torch.bfloat16, seed=5, initial_state=False)
+    y, h, cs = gpu_prefill(shape, dev)
+    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16, heads=[1, 30, 99, 126])
