@@ -57,6 +57,23 @@ ssd_status check_dims(const ssd_dims* d, ssd_dtype act, long long* cdim)
 
 ssd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
 
+// The tensor-core chunk scan serves bf16 with P = 64, N = 128, W <= 4 and
+// 128-row chunks; everything else runs on the row-exact fp32-pipe kernel.
+bool use_tensor_cores(const ssd_dims* d, ssd_dtype act)
+{
+    const int chunk = d->chunk == 0 ? 128 : d->chunk;
+    return act == SSD_BF16 && chunk == 128 && scan_tc_supports(d->headdim, d->dstate) &&
+           d->conv_width <= 4 && d->seqlen > 0;
+}
+
+// Scratch of the tensor-core path with the conv fused: the post-conv B|C
+// columns of every row, [B, S, 2*G*N] bf16.
+size_t tc_workspace_bytes(const ssd_dims* d)
+{
+    const size_t n = (size_t)d->batch * d->seqlen * 2 * d->ngroups * d->dstate * 2;
+    return (n + 255) & ~(size_t)255;
+}
+
 std::atomic<uint64_t> g_launches[SSD_KERNEL_KINDS];
 
 // Records one launch of `kind` when it succeeded (kernels that a launcher
@@ -141,8 +158,7 @@ ssd_status ssd_chunk_scan_workspace_size(const ssd_dims* dims, ssd_dtype act, un
     ssd_status s = check_dims(dims, act, &cdim);
     if (s != SSD_OK) return s;
     if (flags & ~(unsigned)(SSD_DT_SOFTPLUS | SSD_HAS_Z)) return SSD_ERR_INVALID_ARG;
-    (void)conv_fused;
-    *bytes = 0;
+    *bytes = (conv_fused && use_tensor_cores(dims, act)) ? tc_workspace_bytes(dims) : 0;
     return SSD_OK;
 }
 
@@ -181,17 +197,37 @@ ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned flags, c
         return SSD_ERR_INVALID_ARG;
     const int chunk = dims->chunk == 0 ? 128 : dims->chunk;
     if (act == SSD_BF16 && chunk != 128) return SSD_ERR_UNSUPPORTED;
-    if (!scan_simt_supports(dims->headdim, dims->dstate)) return SSD_ERR_UNSUPPORTED;
+    const bool tc = use_tensor_cores(dims, act);
+    if (!tc && !scan_simt_supports(dims->headdim, dims->dstate)) return SSD_ERR_UNSUPPORTED;
     if (dims->batch == 0) return SSD_OK;
 
     unsigned* err = nullptr;
     s = error_word_address(&err);
     if (s != SSD_OK) return s;
     const bool bf16 = act == SSD_BF16;
-    ScanParams p{dims->batch, dims->seqlen, dims->nheads, dims->headdim, dims->dstate,
-                 dims->ngroups, dims->conv_width, flags, xbc, conv_w, conv_b, conv_state_in,
-                 dt, dt_bias, A, D, has_z ? z : nullptr, ssm_state_in, y, ssm_state_out, err};
-    s = counted(launch_scan_simt(p, bf16, stream), SSD_KERNEL_SCAN_SIMT);
+    if (tc) {
+        const int H = dims->nheads, P = dims->headdim, N = dims->dstate, G = dims->ngroups;
+        TcScanParams tp{dims->batch, dims->seqlen, H, G, dims->conv_width, flags,
+                        conv_w != nullptr, xbc, xbc, (int)cdim, H * P, conv_w, conv_b,
+                        conv_state_in, dt, dt_bias, A, D, has_z ? z : nullptr, ssm_state_in, y,
+                        ssm_state_out, err};
+        if (conv_w != nullptr) {
+            // B|C columns: conv + SiLU once per group into the workspace
+            ConvParams bp{dims->batch, dims->seqlen, (int)cdim, dims->conv_width, xbc, conv_w,
+                          conv_b, conv_state_in, workspace, nullptr, H * P, 2 * G * N, 2 * G * N};
+            s = counted(launch_conv1d_rows(bp, true, stream), SSD_KERNEL_BC_CONV);
+            if (s != SSD_OK) return s;
+            tp.bc = workspace;
+            tp.bc_stride = 2 * G * N;
+            tp.bc_col0 = 0;
+        }
+        s = counted(launch_scan_tc(tp, stream), SSD_KERNEL_SCAN_TC);
+    } else {
+        ScanParams p{dims->batch, dims->seqlen, dims->nheads, dims->headdim, dims->dstate,
+                     dims->ngroups, dims->conv_width, flags, xbc, conv_w, conv_b, conv_state_in,
+                     dt, dt_bias, A, D, has_z ? z : nullptr, ssm_state_in, y, ssm_state_out, err};
+        s = counted(launch_scan_simt(p, bf16, stream), SSD_KERNEL_SCAN_SIMT);
+    }
     if (s != SSD_OK) return s;
     if (conv_w != nullptr && conv_state_out != nullptr) {
         ConvParams cp{dims->batch, dims->seqlen, (int)cdim, dims->conv_width,

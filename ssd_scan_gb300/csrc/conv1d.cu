@@ -56,13 +56,14 @@ template <typename T, int W>
 __global__ void __launch_bounds__(128) conv1d_rows_kernel(ConvParams p)
 {
     constexpr int V = Vec16<T>::n;
-    const int nvec = p.C / V;
+    const int nvec = p.ncols / V;
     const int cv = blockIdx.x * blockDim.x + threadIdx.x;
     if (cv >= nvec) return;
     const int b = blockIdx.z;
     const int t0 = blockIdx.y * kRowsPerThread;
     const int t1 = min(t0 + kRowsPerThread, p.S);
-    const int c0 = cv * V;
+    const int c0 = p.col0 + cv * V;        // absolute channel
+    const int o0 = cv * V;                 // column in the output rows
     const T* x = static_cast<const T*>(p.x);
     const T* st = static_cast<const T*>(p.st_in);
     T* out = static_cast<T*>(p.out);
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(128) conv1d_rows_kernel(ConvParams p)
             v = fmaf(w[W - 1][j], cur[j], v);
             o[j] = silu_f32(v);
         }
-        Vec16<T>::store(out + ((size_t)b * p.S + t) * p.C + c0, o);
+        Vec16<T>::store(out + ((size_t)b * p.S + t) * p.out_stride + o0, o);
 #pragma unroll
         for (int k = 0; k + 1 < W - 1; ++k)
 #pragma unroll
@@ -134,10 +135,13 @@ __global__ void conv_state_kernel(ConvParams p)
 }
 
 template <typename T>
-cudaError_t launch_rows_t(const ConvParams& p, cudaStream_t st)
+cudaError_t launch_rows_t(ConvParams p, cudaStream_t st)
 {
     constexpr int V = Vec16<T>::n;
-    const int nvec = p.C / V;
+    if (p.ncols < 0) p.ncols = p.C;
+    if (p.out_stride < 0) p.out_stride = p.ncols;
+    if (p.ncols % V != 0 || p.col0 % V != 0 || p.out_stride % V != 0) return cudaErrorInvalidValue;
+    const int nvec = p.ncols / V;
     dim3 block(128);
     dim3 grid((nvec + 127) / 128, (p.S + kRowsPerThread - 1) / kRowsPerThread, p.B);
     switch (p.W) {

@@ -19,8 +19,11 @@ struct ConvParams {
     const float* w;       // [C,W]
     const float* bias;    // [C] or null
     const void* st_in;    // [B,W-1,C] act or null
-    void* out;            // [B,S,C] act
+    void* out;            // [B,S,out_stride] act: channels [col0, col0+ncols) of the conv
     void* st_out;         // [B,W-1,C] act or null
+    int col0 = 0;         // first channel the rows kernel computes
+    int ncols = -1;       // channels it computes (-1: all C)
+    int out_stride = -1;  // output row length in elements (-1: C)
 };
 
 struct ScanParams {
@@ -84,6 +87,30 @@ cudaError_t launch_conv1d_rows(const ConvParams& p, bool bf16, cudaStream_t st);
 cudaError_t launch_conv_state(const ConvParams& p, bool bf16, cudaStream_t st);
 cudaError_t launch_scan_simt(const ScanParams& p, bool bf16, cudaStream_t st);
 bool scan_simt_supports(int P, int N);
+// Tensor-core chunk scan (bf16, P = 64, N = 128, 128-row chunks).
+struct TcScanParams {
+    int B, S, H, G, W;
+    unsigned flags;
+    bool conv;                   // x columns are raw: conv + SiLU in the kernel
+    const void* xbc;             // [B,S,Cdim] bf16 (raw x when conv)
+    const void* bc;              // post-conv B|C columns: rows of bc_stride elements
+    int bc_stride, bc_col0;      // row length and first B column of `bc`
+    const float* conv_w;         // [Cdim,W] (when conv)
+    const float* conv_b;         // [Cdim] or null
+    const void* conv_state_in;   // [B,W-1,Cdim] bf16 or null
+    const float* dt;             // [B,S,H]
+    const float* dt_bias;        // [H] or null
+    const float* A;              // [H]
+    const float* D;              // [H] or null
+    const void* z;               // [B,S,H*64] bf16 or null
+    const float* h0;             // [B,H,64,128] or null
+    void* y;                     // [B,S,H,64] bf16
+    float* hS;                   // [B,H,64,128]
+    unsigned* err;
+};
+bool scan_tc_supports(int P, int N);
+cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st);
+
 cudaError_t launch_decode_step(const DecodeParams& p, bool bf16, cudaStream_t st);
 cudaError_t launch_decode_conv_roll(const DecodeParams& p, bool bf16, cudaStream_t st);
 

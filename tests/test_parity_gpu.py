@@ -149,3 +149,54 @@ def test_prefill_137_rows_full_heads_sampled():
     cpu, dev = make_problem(shape, act=torch.bfloat16, seed=5, initial_state=False)
     y, h, cs = gpu_prefill(shape, dev)
     _check_prefill(shape, cpu, y, h, cs, torch.bfloat16, heads=[1, 30, 99, 126])
+
+
+# ---------------------------------------------------------------------------
+# which kernels ran (launch counters), and the paths around the tensor cores
+
+def _counts():
+    return ssd.ssd_launch_counts()
+
+
+def test_bf16_runs_on_tensor_cores():
+    shape = si.Shape(batch=1, seqlen=256, nheads=8, headdim=64, dstate=128, ngroups=2)
+    cpu, dev = make_problem(shape, act=torch.bfloat16)
+    c0 = _counts()
+    y, h, cs = gpu_prefill(shape, dev)
+    torch.cuda.synchronize()
+    c1 = _counts()
+    assert c1["scan_tc"] - c0["scan_tc"] == 1
+    assert c1["bc_conv"] - c0["bc_conv"] == 1
+    assert c1["scan_simt"] == c0["scan_simt"]
+    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
+
+
+def test_bf16_tensor_cores_without_conv():
+    shape = si.Shape(batch=2, seqlen=200, nheads=4, headdim=64, dstate=128, ngroups=2)
+    cpu, dev = make_problem(shape, act=torch.bfloat16)
+    c0 = _counts()
+    y, h, _ = gpu_prefill(shape, dev, [77, 123], conv=False)
+    torch.cuda.synchronize()
+    c1 = _counts()
+    assert c1["scan_tc"] - c0["scan_tc"] == 2 and c1["bc_conv"] == c0["bc_conv"]
+    _check_prefill(shape, cpu, y, h, None, torch.bfloat16, conv=False)
+
+
+def test_bf16_other_head_dims_run_row_exact_kernel():
+    shape = si.Shape(batch=1, seqlen=150, nheads=4, headdim=32, dstate=64, ngroups=1)
+    cpu, dev = make_problem(shape, act=torch.bfloat16)
+    c0 = _counts()
+    y, h, cs = gpu_prefill(shape, dev, [100, 50])
+    torch.cuda.synchronize()
+    c1 = _counts()
+    assert c1["scan_simt"] - c0["scan_simt"] == 2 and c1["scan_tc"] == c0["scan_tc"]
+    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
+
+
+@pytest.mark.parametrize("W", [2, 3])
+def test_bf16_short_conv_widths(W):
+    shape = si.Shape(batch=1, seqlen=260, nheads=4, headdim=64, dstate=128, ngroups=1,
+                     conv_width=W)
+    cpu, dev = make_problem(shape, act=torch.bfloat16)
+    y, h, cs = gpu_prefill(shape, dev, [130, 130])
+    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
