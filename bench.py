@@ -263,11 +263,13 @@ def bench_ours(args):
                 "peak_source": hbm_src,
                 "kernel": "ssd_chunk_scan call (all its kernels, events around the call)",
                 "algorithmic_bytes_per_launch": pb["per_launch"]}
-    # ---- end to end through the C-ABI from pinned host buffers
-    e2e = bench_e2e(ssd, shape, d, flags, prm, sets[0], stream, args)
-
-    # ---- decode step (config: 256 rows, 1024-slot pool, 64 steps)
-    dec = bench_decode(ssd, dev, stream, world, args)
+    if args.only == "prefill":  # profiling runs: the timed prefill steps alone
+        e2e = dec = None
+    else:
+        # ---- end to end through the C-ABI from pinned host buffers
+        e2e = bench_e2e(ssd, shape, d, flags, prm, sets[0], stream, args)
+        # ---- decode step (256 rows, 1024-slot pool, 64 steps)
+        dec = bench_decode(ssd, dev, stream, world, args)
 
     out = None
     if rank == 0:
@@ -438,6 +440,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "prefill"], default="all",
+                    help="prefill: time the prefill steps only (for profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -449,7 +453,7 @@ def main():
     res = bench_ours(args)
     rank, world, _ = _dist()
     if rank == 0 and res is not None:
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and args.only == "all":
             res["cpu_baseline"] = cpu_baseline()
         print(json.dumps(res), flush=True)
     if world > 1:
