@@ -14,7 +14,7 @@
 namespace ssd {
 namespace {
 
-constexpr int kRowsPerThread = 64;
+constexpr int kRowsPerThread = 16;
 
 template <typename T> struct Vec16;
 template <> struct Vec16<__nv_bfloat16> {

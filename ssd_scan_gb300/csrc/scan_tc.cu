@@ -16,16 +16,20 @@
 // 128 x {128,64} x 128, bf16 operands in shared memory, fp32 accumulators in
 // TMEM:
 //   G1  CB[t,s] = C_t . B_s                 A = C  (TMA tile)   B = B (TMA)
-//   G3  Yo[t,p] = C_t . h[p,:]              A = C               B = bf16(h)
-//   G4  dH[n,p] = sum_s B[s,n] w_s x[s,p]   A = B^T (MN-major)  B = (w x)^T
-//   G2  Yd[t,p] = sum_s M[t,s] x[s,p]       A = M (masked, decayed CB)  B = x^T
-// The 128 threads (one warpgroup) own one TMEM lane each: row t of the
-// chunk for CB / Yd / Yo, state row n for dH.  They compute dt and the
-// cumulative sum (a double-float warp-shuffle scan), the x conv + SiLU from
-// the raw TMA tile, the causal mask with its decays, the state update and the
-// epilogue y = Yd + exp(gamma_t) Yo + D x, times silu(z).  Thread 0 issues
-// the TMA loads and the MMAs.  B and C of a group are read by each of its
-// heads' CTAs; they come from L2 after the first.
+//   G3  Yo[t,p] = C_t . h[p,:]              A = C               B = bf16(h) rows [n][p]
+//   G4  dH[n,p] = sum_s B[s,n] w_s x[s,p]   A = B^T (MN-major)  B = (w x) rows [s][p]
+//   G2  Yd[t,p] = sum_s M[t,s] x[s,p]       A = M (masked, decayed CB)  B = x rows [s][p]
+// Every operand the threads write is row-major with 16-byte stores; the
+// operands whose K index runs along rows are read MN-major by the MMA.
+// Two warpgroups (256 threads): the warps of each read one 32-lane quarter of
+// TMEM (row t of the chunk for CB / Yd / Yo, state row n for dH) and the two
+// warpgroups split the columns.  The threads compute dt and the cumulative
+// sum (a double-float warp-shuffle scan), the x conv + SiLU from the raw TMA
+// tile (4 rows x 8 channels per thread), the causal mask with its decays
+// (blocks above the diagonal are written as zeros without a TMEM read), the
+// state update and the epilogue y = Yd + exp(gamma_t) Yo + D x, times
+// silu(z).  Thread 0 issues the TMA loads and the MMAs.  B and C of a group
+// are read by each of its heads' CTAs; they come from L2 after the first.
 #include "internal.cuh"
 #include "sm100.cuh"
 
@@ -41,27 +45,29 @@ using namespace sm100;
 constexpr int Q = 128;   // rows per chunk
 constexpr int P = 64;    // head dim
 constexpr int N = 128;   // state dim
-constexpr int kThreads = 128;
-constexpr int kMaxW = 4;  // conv taps handled in the kernel (W-1 carried rows)
+constexpr int kThreads = 256;  // two warpgroups; each owns one half of the columns
+constexpr int kMaxW = 4;       // conv taps handled in the kernel (W-1 carried rows)
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound on any single wait: 2 s
 
+// G1: A, B K-major.  G2, G3: A K-major, B MN-major (row tiles [k][p]).
+// G4: A = B^T read MN-major from the B tile, B MN-major.
 constexpr uint32_t kIdCB = idesc_bf16_f32(128, 128, false, false);
-constexpr uint32_t kIdY = idesc_bf16_f32(128, 64, false, false);
-constexpr uint32_t kIdState = idesc_bf16_f32(128, 64, true, false);
+constexpr uint32_t kIdY = idesc_bf16_f32(128, 64, false, true);
+constexpr uint32_t kIdState = idesc_bf16_f32(128, 64, true, true);
 
 struct __align__(1024) TcSmem {
     __nv_bfloat16 C[2][Q * 64];    // C tile [t][n]: 2 panels of 64 n (TMA, SW128)
     __nv_bfloat16 B[2][Q * 64];    // B tile [s][n]
     __nv_bfloat16 Xr[Q * 64];      // x tile [t][p] (raw rows when the conv is fused)
     __nv_bfloat16 Z[Q * 64];       // z tile [t][p]
-    __nv_bfloat16 XT[2][P * 64];   // x^T [p][s], 2 panels of 64 s (K-major SW128)
-    __nv_bfloat16 XW[2][P * 64];   // (w o x)^T [p][s]
-    __nv_bfloat16 M[2][Q * 64];    // masked decayed CB [t][s]
-    __nv_bfloat16 Hs[2][P * 64];   // bf16 state [p][n], 2 panels of 64 n
-    float carry[2][kMaxW - 1][P];  // raw x rows before the chunk, by chunk parity
-    float wconv[P][kMaxW];
+    __nv_bfloat16 XR[Q * 64];      // post-conv x rows [s][p] (SW128): G2's B, the D x term
+    __nv_bfloat16 XW[Q * 64];      // (w o x) rows [s][p]: G4's B
+    __nv_bfloat16 M[2][Q * 64];    // masked decayed CB [t][s]: G2's A (K-major)
+    __nv_bfloat16 Hs[N * 64];      // bf16 state rows [n][p]: G3's B
+    __nv_bfloat16 carry[2][kMaxW - 1][P];  // raw x rows before the chunk, by parity
+    float4 wconv[P];               // 4 taps per x channel (front-padded with zeros)
     float bconv[P];
-    float gam_hi[Q], gam_lo[Q], dts[Q];
+    float g2h[Q], g2l[Q], dts[Q], wrow[Q];  // gamma*log2(e) (hi, lo), dt, w_s
     float wsum_hi[4], wsum_lo[4];
     uint64_t bar_ld, bar_z, bar_g1, bar_g34, bar_g2;
     uint32_t tmem_base;
@@ -69,14 +75,25 @@ struct __align__(1024) TcSmem {
 
 constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;
 
-__device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float tanh_fast(float v)
+{
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(v));
+    return t;
+}
 
 // silu via one MUFU op: v * sigmoid(v) = 0.5 v (1 + tanh(v / 2)).
 __device__ __forceinline__ float silu_fast(float v)
 {
-    float t;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * v));
-    return 0.5f * v * (1.0f + t);
+    const float hv = 0.5f * v;
+    return fmaf(hv, tanh_fast(hv), hv);
+}
+
+__device__ __forceinline__ float ex2_fast(float v)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
 }
 
 // (hi, lo) += (bhi, blo), double-float (TwoSum then renormalise).
@@ -101,28 +118,21 @@ __device__ __forceinline__ void unpack8(uint4 r, float* f)
     }
 }
 
+__device__ __forceinline__ uint32_t pack2(float a, float b)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
 __device__ __forceinline__ uint4 pack8(const float* f)
 {
-    uint4 r;
-    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&r);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-    return r;
+    return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
 }
 
-// 16-byte chunk j (8 elements) of row r of a SW128 tile of 64-element rows.
-__device__ __forceinline__ const uint4* tile_chunk(const __nv_bfloat16* tile, int r, int j)
+// byte offset of 16-byte chunk j of row r in a SW128 tile of 64-element rows.
+__device__ __forceinline__ uint32_t chunk_off(int r, int j)
 {
-    return reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(tile) + r * 128 +
-                                          (((j ^ r) & 7) << 4));
-}
-
-// element (row, k) of a K-major operand stored as panels of 64 k.
-__device__ __forceinline__ __nv_bfloat16* kmajor_elem(__nv_bfloat16 (*panels)[P * 64], int row,
-                                                      int k)
-{
-    return reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(panels[k >> 6]) +
-                                            sw128_offset(row, k & 63));
+    return (uint32_t)(r * 128 + (((j ^ r) & 7) << 4));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -134,6 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     TcSmem& s = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3;      // TMEM lane quarter of this warp
+    const int half = warp >> 2;        // column half of this warpgroup
+    const int row = 32 * quarter + lane;  // chunk row t (or state column n) of this thread
     const int h = blockIdx.x, b = blockIdx.y;
     const int H = p.H, G = p.G, W = p.W;
     const int g = h / (H / G);
@@ -158,46 +171,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     if (p.conv) {
-        for (int i = tid; i < P * kMaxW; i += kThreads) {
-            const int pp = i / kMaxW, k = i % kMaxW;
-            s.wconv[pp][k] = k < W ? p.conv_w[(size_t)(h * P + pp) * W + k] : 0.0f;
+        for (int i = tid; i < P; i += kThreads) {
+            float w4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int k = 0; k < W; ++k) w4[kMaxW - W + k] = p.conv_w[(size_t)(h * P + i) * W + k];
+            s.wconv[i] = make_float4(w4[0], w4[1], w4[2], w4[3]);
+            s.bconv[i] = p.conv_b ? p.conv_b[h * P + i] : 0.0f;
         }
-        for (int i = tid; i < P; i += kThreads) s.bconv[i] = p.conv_b ? p.conv_b[h * P + i] : 0.0f;
-        // carry rows -3..-1 before chunk 0 come from the conv state (its last rows)
+        // raw rows -3..-1 before chunk 0: the last rows of the conv state (or zeros)
         const __nv_bfloat16* cs = static_cast<const __nv_bfloat16*>(p.conv_state_in);
         for (int i = tid; i < (kMaxW - 1) * P; i += kThreads) {
             const int j = i / P, pp = i % P;
-            const int sr = (W - 1) + (j - (kMaxW - 1));  // state row holding raw row j-3
-            float v = 0.0f;
-            if (cs && sr >= 0) v = bf2f(cs[((size_t)b * (W - 1) + sr) * Cdim + h * P + pp]);
+            const int sr = (W - 1) + (j - (kMaxW - 1));
+            __nv_bfloat16 v = __float2bfloat16_rn(0.0f);
+            if (cs && sr >= 0) v = cs[((size_t)b * (W - 1) + sr) * Cdim + h * P + pp];
             s.carry[0][j][pp] = v;
         }
     }
 
-    // the fp32 state, thread n owns h[:, n]
-    const int n = tid;
+    // The fp32 state: thread (n = row, half) owns h[32*half .. 32*half+31][n].
+    const int n = row;
+    const int p0 = 32 * half;
     const size_t sbase = ((size_t)b * H + h) * P * N;
-    float hreg[P];
+    float hreg[32];
 #pragma unroll
-    for (int pp = 0; pp < P; ++pp) hreg[pp] = p.h0 ? p.h0[sbase + (size_t)pp * N + n] : 0.0f;
+    for (int i = 0; i < 32; ++i) hreg[i] = p.h0 ? p.h0[sbase + (size_t)(p0 + i) * N + n] : 0.0f;
+    // Hs row n holds bf16 h[0..63][n]; this thread writes its 4 chunks of 8 p
+    auto store_h = [&]() {
 #pragma unroll
-    for (int pp = 0; pp < P; ++pp) *kmajor_elem(s.Hs, pp, n) = __float2bfloat16_rn(hreg[pp]);
+        for (int q4 = 0; q4 < 4; ++q4)
+            *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(s.Hs) + chunk_off(n, 4 * half + q4)) =
+                pack8(&hreg[8 * q4]);
+    };
+    store_h();
+
+    // conv work split: thread (j = channel group of 8, rb = block of 4 rows)
+    const int cj = tid & 7, rb = tid >> 3;
+    float4 wq[8];
+    float bq[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) wq[e] = make_float4(0.f, 0.f, 0.f, 0.f), bq[e] = 0.0f;
 
     const float Ah = p.A[h];
     const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
     const float Dh = p.D ? p.D[h] : 0.0f;
-    float dt_next = tid < p.S ? p.dt[((size_t)b * p.S + tid) * H + h] : 0.0f;
+    const int trow = tid & (Q - 1);  // row for the dt scan (both warpgroups scan the same rows)
+    float dt_next = trow < p.S ? p.dt[((size_t)b * p.S + trow) * H + h] : 0.0f;
 
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (p.conv) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            wq[e] = s.wconv[8 * cj + e];
+            bq[e] = s.bconv[8 * cj + e];
+        }
+    }
     const uint32_t tbase = s.tmem_base;
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
     const uint32_t t_cb = tbase, t_yd = tbase + 128, t_yo = tbase + 192, t_st = tbase + 256;
 
-    const int xB = p.bc_col0 + g * N;            // first B column in the bc source
-    const int xC = p.bc_col0 + G * N + g * N;    // first C column
+    const int xB = p.bc_col0 + g * N;          // first B column in the bc source
+    const int xC = p.bc_col0 + G * N + g * N;  // first C column
     auto issue_main = [&](int c) {
         mbar_arrive_expect_tx(&s.bar_ld, 5 * Q * 64 * 2);
         tma_load_3d(s.C[0], &map_bc, &s.bar_ld, xC, c * Q, b);
@@ -215,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (has_z) issue_z(0);
     }
 
-    const uint32_t aC = smem_u32(s.C), aB = smem_u32(s.B), aXT = smem_u32(s.XT);
+    const uint32_t aC = smem_u32(s.C), aB = smem_u32(s.B), aXR = smem_u32(s.XR);
     const uint32_t aXW = smem_u32(s.XW), aM = smem_u32(s.M), aH = smem_u32(s.Hs);
     constexpr float kLog2e = 1.4426950408889634f;
 
@@ -227,9 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- dt and the cumulative sum of a = dt A (double-float) --------------
         float dt = 0.0f;
-        if (tid < rows) dt = softplus ? softplus_f32(dt_next + bias) : dt_next;
+        if (trow < rows) dt = softplus ? softplus_f32(dt_next + bias) : dt_next;
         if (c + 1 < nchunks)
-            dt_next = r0 + Q + tid < p.S ? p.dt[((size_t)b * p.S + r0 + Q + tid) * H + h] : 0.0f;
+            dt_next = r0 + Q + trow < p.S ? p.dt[((size_t)b * p.S + r0 + Q + trow) * H + h] : 0.0f;
         float ghi = dt * Ah, glo = 0.0f;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -237,15 +273,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float olo = __shfl_up_sync(0xffffffffu, glo, d);
             if (lane >= d) df_add(ghi, glo, ohi, olo);
         }
-        if (lane == 31) {
-            s.wsum_hi[warp] = ghi;
-            s.wsum_lo[warp] = glo;
+        if (half == 0 && lane == 31) {
+            s.wsum_hi[quarter] = ghi;
+            s.wsum_lo[quarter] = glo;
         }
-        s.dts[tid] = dt;
         __syncthreads();
-        for (int w2 = 0; w2 < warp; ++w2) df_add(ghi, glo, s.wsum_hi[w2], s.wsum_lo[w2]);
-        s.gam_hi[tid] = ghi;
-        s.gam_lo[tid] = glo;
+        for (int w2 = 0; w2 < quarter; ++w2) df_add(ghi, glo, s.wsum_hi[w2], s.wsum_lo[w2]);
+        // ghi/glo: gamma of row trow (== row for every thread)
+        if (half == 0) {
+            s.g2h[trow] = ghi * kLog2e;
+            s.g2l[trow] = glo * kLog2e;
+            s.dts[trow] = dt;
+        }
+        float gLh, gLl;  // gamma (log2 units) of the chunk's last row, from shared memory
 
         // ---- this chunk's tiles; G1 = C B^T ---------------------------------------
         ok = ok && mbar_wait_ns(&s.bar_ld, par, kWaitNs);
@@ -260,52 +300,69 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&s.bar_g1);
         }
         __syncthreads();
-        const float gShi = s.gam_hi[rows - 1], gSlo = s.gam_lo[rows - 1];
-        const float decay_t = __expf(fminf(ghi + glo, 0.0f));
-        const float w_t = tid < rows ? __expf(fminf((gShi - ghi) + (gSlo - glo), 0.0f)) * dt : 0.0f;
-        const float decay_S = __expf(fminf(gShi + gSlo, 0.0f));
+        gLh = s.g2h[rows - 1];
+        gLl = s.g2l[rows - 1];
+        const float g2h_t = ghi * kLog2e, g2l_t = glo * kLog2e;
+        // exp(min(gamma_t,0)), w_t = exp(min(gamma_Q - gamma_t, 0)) dt_t, exp(min(gamma_Q,0))
+        const float decay_t = ex2_fast(fminf(g2h_t + g2l_t, 0.0f));
+        const float decay_S = ex2_fast(fminf(gLh + gLl, 0.0f));
+        if (half == 0) {
+            const float w_t = trow < rows ? ex2_fast(fminf((gLh - g2h_t) + (gLl - g2l_t), 0.0f)) * dt
+                                          : 0.0f;
+            s.wrow[trow] = w_t;
+        }
+        __syncthreads();
 
-        // ---- x: conv + SiLU of the raw rows (or the post-conv tile) -> x^T, (w x)^T
+        // ---- x: conv + SiLU of 4 rows x 8 channels per thread -> x, w x rows ------
         {
-            const int t = tid;
-#pragma unroll 2
-            for (int j = 0; j < 8; ++j) {
-                float xv[8];
-                if (p.conv) {
-                    float acc[8];
+            const int t0 = 4 * rb;
+            float xo[4][8];
+            if (p.conv) {
+                float win[7][8];  // raw rows t0-3 .. t0+3
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = s.bconv[8 * j + e];
-                    for (int k = 0; k < W; ++k) {
-                        const int r = t - (W - 1) + k;
-                        float raw[8];
-                        if (r >= 0) {
-                            unpack8(*tile_chunk(s.Xr, r, j), raw);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) raw[e] = s.carry[par][kMaxW - 1 + r][8 * j + e];
-                        }
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[e] = fmaf(s.wconv[8 * j + e][k], raw[e], acc[e]);
-                    }
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) xv[e] = t < rows ? silu_fast(acc[e]) : 0.0f;
-                } else {
-                    unpack8(*tile_chunk(s.Xr, t, j), xv);
+                for (int k = 0; k < 7; ++k) {
+                    const int r = t0 - 3 + k;
+                    uint4 raw;
+                    if (r >= 0)
+                        raw = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(s.Xr) +
+                                                              chunk_off(r, cj));
+                    else
+                        raw = *reinterpret_cast<const uint4*>(&s.carry[par][r + 3][8 * cj]);
+                    unpack8(raw, win[k]);
+                    if (r >= Q - (kMaxW - 1))  // rows Q-3..Q-1 carry into the next chunk
+                        *reinterpret_cast<uint4*>(&s.carry[par ^ 1][r - (Q - 3)][8 * cj]) = raw;
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    *kmajor_elem(s.XT, 8 * j + e, t) = __float2bfloat16_rn(xv[e]);
-                    *kmajor_elem(s.XW, 8 * j + e, t) = __float2bfloat16_rn(w_t * xv[e]);
+                for (int i = 0; i < 4; ++i) {
+                    const bool valid = t0 + i < rows;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        float v = bq[e];
+                        v = fmaf(wq[e].x, win[i][e], v);
+                        v = fmaf(wq[e].y, win[i + 1][e], v);
+                        v = fmaf(wq[e].z, win[i + 2][e], v);
+                        v = fmaf(wq[e].w, win[i + 3][e], v);
+                        xo[i][e] = valid ? silu_fast(v) : 0.0f;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 raw = *reinterpret_cast<const uint4*>(
+                        reinterpret_cast<const uint8_t*>(s.Xr) + chunk_off(t0 + i, cj));
+                    unpack8(raw, xo[i]);
                 }
             }
-            if (p.conv && t >= Q - (kMaxW - 1)) {
-                // raw rows Q-3..Q-1 carry into the next chunk
-                for (int j = 0; j < 8; ++j) {
-                    float raw[8];
-                    unpack8(*tile_chunk(s.Xr, t, j), raw);
+            const float4 w4 = *reinterpret_cast<const float4*>(&s.wrow[t0]);
+            const float wr[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) s.carry[par ^ 1][t - (Q - (kMaxW - 1))][8 * j + e] = raw[e];
-                }
+            for (int i = 0; i < 4; ++i) {
+                float xw[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xw[e] = wr[i] * xo[i][e];
+                const uint32_t off = chunk_off(t0 + i, cj);
+                *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(s.XR) + off) = pack8(xo[i]);
+                *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(s.XW) + off) = pack8(xw);
             }
         }
         fence_proxy_async_smem();
@@ -313,47 +370,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0 && ok) {
             tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {  // G3: Yo = C h^T
+            for (int k = 0; k < 8; ++k) {  // G3: Yo = C h^T  (K = n, 16 rows of Hs per step)
                 const uint32_t offc = (k >> 2) * (Q * 128) + (k & 3) * 32;
-                const uint32_t offh = (k >> 2) * (P * 128) + (k & 3) * 32;
                 mma_bf16_ss(t_yo, sdesc_sw128(aC + offc, 16, 1024),
-                            sdesc_sw128(aH + offh, 16, 1024), kIdY, k > 0);
+                            sdesc_sw128(aH + k * 2048, 8192, 1024), kIdY, k > 0);
             }
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {  // G4: dH = B^T (w x)
-                const uint32_t offx = (k >> 2) * (P * 128) + (k & 3) * 32;
+            for (int k = 0; k < 8; ++k) {  // G4: dH = B^T (w x)  (K = s)
                 mma_bf16_ss(t_st, sdesc_sw128(aB + k * 2048, Q * 128, 1024),
-                            sdesc_sw128(aXW + offx, 16, 1024), kIdState, k > 0);
+                            sdesc_sw128(aXW + k * 2048, 8192, 1024), kIdState, k > 0);
             }
             mma_commit(&s.bar_g34);
         }
 
-        // ---- causal mask with decays: M[t,s] = CB[t,s] exp(gamma_t - gamma_s) dt_s
+        // ---- causal mask with decays: M[t,s] = CB[t,s] 2^(g2_t - g2_s) dt_s ------
         ok = ok && mbar_wait_ns(&s.bar_g1, par, kWaitNs);
         tc_fence_after();
         {
-            const int t = tid;
-#pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
+            const int t = row;
+#pragma unroll
+            for (int cb2 = 0; cb2 < 2; ++cb2) {
+                const int cc = 2 * half + cb2;  // 32-column block of this thread
+                uint8_t* mrow = reinterpret_cast<uint8_t*>(s.M[cc >> 1]);
+                if (cc > quarter) {  // strictly above the diagonal for the whole warp
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int k = (cc & 1) * 32 + q4 * 8;
+                        *reinterpret_cast<uint4*>(mrow + chunk_off(t, k >> 3)) = make_uint4(0, 0, 0, 0);
+                    }
+                    continue;
+                }
                 float v[32];
                 tmem_ld32(t_cb + lane_off + cc * 32, v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
+                    const int sb = cc * 32 + q4 * 8;
+                    const float4 h0 = *reinterpret_cast<const float4*>(&s.g2h[sb]);
+                    const float4 h1 = *reinterpret_cast<const float4*>(&s.g2h[sb + 4]);
+                    const float4 l0 = *reinterpret_cast<const float4*>(&s.g2l[sb]);
+                    const float4 l1 = *reinterpret_cast<const float4*>(&s.g2l[sb + 4]);
+                    const float4 d0 = *reinterpret_cast<const float4*>(&s.dts[sb]);
+                    const float4 d1 = *reinterpret_cast<const float4*>(&s.dts[sb + 4]);
+                    const float gh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+                    const float gl[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+                    const float ds[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
                     float m[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const int sidx = cc * 32 + q4 * 8 + e;
-                        float val = 0.0f;
-                        if (sidx <= t) {
-                            const float ex = (ghi - s.gam_hi[sidx]) + (glo - s.gam_lo[sidx]);
-                            val = v[q4 * 8 + e] * exp2f(fminf(ex, 0.0f) * kLog2e) * s.dts[sidx];
-                        }
-                        m[e] = val;
+                        const float ex = (g2h_t - gh[e]) + (g2l_t - gl[e]);
+                        const float val = v[q4 * 8 + e] * ds[e] * ex2_fast(fminf(ex, 0.0f));
+                        m[e] = (sb + e <= t) ? val : 0.0f;
                     }
-                    const int k = cc * 32 + q4 * 8;  // first s of this 16-byte chunk
-                    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(s.M[k >> 6]) +
-                                              sw128_offset(t, k & 63)) = pack8(m);
+                    const int k = (cc & 1) * 32 + q4 * 8;
+                    *reinterpret_cast<uint4*>(mrow + chunk_off(t, k >> 3)) = pack8(m);
                 }
             }
         }
@@ -363,11 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0 && ok) {
             tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {  // G2: Yd = M x
+            for (int k = 0; k < 8; ++k) {  // G2: Yd = M x  (K = s)
                 const uint32_t offm = (k >> 2) * (Q * 128) + (k & 3) * 32;
-                const uint32_t offx = (k >> 2) * (P * 128) + (k & 3) * 32;
                 mma_bf16_ss(t_yd, sdesc_sw128(aM + offm, 16, 1024),
-                            sdesc_sw128(aXT + offx, 16, 1024), kIdY, k > 0);
+                            sdesc_sw128(aXR + k * 2048, 8192, 1024), kIdY, k > 0);
             }
             mma_commit(&s.bar_g2);
         }
@@ -376,17 +445,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = ok && mbar_wait_ns(&s.bar_g34, par, kWaitNs);
         tc_fence_after();
         if (tid == 0 && ok && c + 1 < nchunks) issue_main(c + 1);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        {
             float v[32];
-            tmem_ld32(t_st + lane_off + half * 32, v);
+            tmem_ld32(t_st + lane_off + p0, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int pp = half * 32 + e;
-                hreg[pp] = fmaf(decay_S, hreg[pp], v[e]);
-                *kmajor_elem(s.Hs, pp, n) = __float2bfloat16_rn(hreg[pp]);
-            }
+            for (int i = 0; i < 32; ++i) hreg[i] = fmaf(decay_S, hreg[i], v[i]);
+            store_h();
         }
 
         // ---- epilogue: y = Yd + exp(gamma_t) Yo + D x, gated ------------------------
@@ -394,31 +459,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (has_z) ok = ok && mbar_wait_ns(&s.bar_z, par, kWaitNs);
         tc_fence_after();
         {
-            const int t = tid;
-            __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(p.y) +
-                                  (((size_t)b * p.S + r0 + t) * H + h) * P;
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                float yd[32], yo[32];
-                tmem_ld32(t_yd + lane_off + half * 32, yd);
-                tmem_ld32(t_yo + lane_off + half * 32, yo);
-                tmem_ld_wait();
+            const int t = row;
+            float yd[32], yo[32];
+            tmem_ld32(t_yd + lane_off + p0, yd);
+            tmem_ld32(t_yo + lane_off + p0, yo);
+            tmem_ld_wait();
+            uint4* yrow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) +
+                                                   (((size_t)b * p.S + r0 + t) * H + h) * P + p0);
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int j = half * 4 + q4;
-                    float out[8], zv[8];
-                    if (has_z) unpack8(*tile_chunk(s.Z, t, j), zv);
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const int j = 4 * half + q4;
+                float xv[8], zv[8], out[8];
+                unpack8(*reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(s.XR) +
+                                                        chunk_off(t, j)), xv);
+                if (has_z)
+                    unpack8(*reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(s.Z) +
+                                                            chunk_off(t, j)), zv);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int pp = 8 * j + e;
-                        const float xv = bf2f(*kmajor_elem(s.XT, pp, t));
-                        float yv = fmaf(decay_t, yo[q4 * 8 + e], yd[q4 * 8 + e]);
-                        yv = fmaf(Dh, xv, yv);
-                        if (has_z) yv *= silu_fast(zv[e]);
-                        out[e] = yv;
-                    }
-                    if (t < rows) reinterpret_cast<uint4*>(yrow)[j] = pack8(out);
+                for (int e = 0; e < 8; ++e) {
+                    float yv = fmaf(decay_t, yo[q4 * 8 + e], yd[q4 * 8 + e]);
+                    yv = fmaf(Dh, xv[e], yv);
+                    if (has_z) yv *= silu_fast(zv[e]);
+                    out[e] = yv;
                 }
+                if (t < rows) yrow[q4] = pack8(out);
             }
         }
         fence_proxy_async_smem();
@@ -430,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (ok) {
 #pragma unroll
-        for (int pp = 0; pp < P; ++pp) p.hS[sbase + (size_t)pp * N + n] = hreg[pp];
+        for (int i = 0; i < 32; ++i) p.hS[sbase + (size_t)(p0 + i) * N + n] = hreg[i];
     } else if (tid == 0) {
         atomicOr(p.err, kErrTimeout);
     }
