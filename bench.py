@@ -179,13 +179,23 @@ def _barrier(world):
         dist.barrier()
 
 
-def _max_over_ranks(v: float, world: int) -> float:
+def _max_over_ranks(v: float, world: int, device="cuda") -> float:
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank draws its own independent sequences (weak scaling)."""
+    return 1000 * rank
+
+
+def whole_job_tokens_per_s(world: int, shape: si.Shape, ms_max: float) -> float:
+    """Tokens all ranks processed in one step over the slowest rank's time."""
+    return world * shape.batch * shape.seqlen / (ms_max / 1e3)
 
 
 def make_prefill_sets(shape, nsets, seed_base, device):
@@ -230,7 +240,7 @@ def bench_ours(args):
     pb = prefill_bytes(shape)
     set_bytes = pb["per_launch"]
     nsets = max(3, -(-2 * L2_BYTES // set_bytes))  # rotate over > 2x L2 of inputs+outputs
-    prm, sets, d, flags = make_prefill_sets(shape, nsets, 1000 * rank, dev)
+    prm, sets, d, flags = make_prefill_sets(shape, nsets, rank_seed(rank), dev)
 
     # ---- warm-up, then K timed steps (one ssd_chunk_scan call each)
     for i in range(args.warmup):
@@ -253,8 +263,7 @@ def bench_ours(args):
     ms = ev0.elapsed_time(ev1) / args.steps
     ms = _max_over_ranks(ms, world)
     gpu_launches = sum(launches1[k] - launches0[k] for k in launches0)
-    tokens_per_step = world * shape.batch * shape.seqlen
-    value = tokens_per_step / (ms / 1e3)
+    value = whole_job_tokens_per_s(world, shape, ms)
 
     hbm, hbm_src = measured_peaks()
     achieved = pb["per_launch"] / (ms / 1e3) / 1e9
