@@ -14,7 +14,7 @@
 namespace ssd {
 namespace {
 
-constexpr int kRowsPerThread = 16;
+constexpr int kRowsPerThread = 8;
 
 template <typename T> struct Vec16;
 template <> struct Vec16<__nv_bfloat16> {
@@ -56,18 +56,42 @@ template <typename T, int W>
 __global__ void __launch_bounds__(128) conv1d_rows_kernel(ConvParams p)
 {
     constexpr int V = Vec16<T>::n;
+    constexpr int R = kRowsPerThread;
     const int nvec = p.ncols / V;
     const int cv = blockIdx.x * blockDim.x + threadIdx.x;
     if (cv >= nvec) return;
     const int b = blockIdx.z;
-    const int t0 = blockIdx.y * kRowsPerThread;
-    const int t1 = min(t0 + kRowsPerThread, p.S);
+    const int t0 = blockIdx.y * R;
+    const int nrows = min(R, p.S - t0);
     const int c0 = p.col0 + cv * V;        // absolute channel
     const int o0 = cv * V;                 // column in the output rows
-    const T* x = static_cast<const T*>(p.x);
-    const T* st = static_cast<const T*>(p.st_in);
-    T* out = static_cast<T*>(p.out);
+    const T* __restrict__ x = static_cast<const T*>(p.x);
+    const T* __restrict__ st = static_cast<const T*>(p.st_in);
+    T* __restrict__ out = static_cast<T*>(p.out);
 
+    // raw rows t0-(W-1) .. t0+R-1 of these channels, all loads issued up front
+    float u[R + W - 1][V];
+#pragma unroll
+    for (int k = 0; k < W - 1; ++k) {
+        const int r = t0 - (W - 1) + k;
+        if (r >= 0) {
+            Vec16<T>::load(x + ((size_t)b * p.S + r) * p.C + c0, u[k]);
+        } else if (st) {
+            Vec16<T>::load(st + ((size_t)b * (W - 1) + (r + W - 1)) * p.C + c0, u[k]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < V; ++j) u[k][j] = 0.0f;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        if (i < nrows) {
+            Vec16<T>::load(x + ((size_t)b * p.S + t0 + i) * p.C + c0, u[W - 1 + i]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < V; ++j) u[W - 1 + i][j] = 0.0f;
+        }
+    }
     float w[W][V], bias[V];
 #pragma unroll
     for (int j = 0; j < V; ++j) {
@@ -75,40 +99,18 @@ __global__ void __launch_bounds__(128) conv1d_rows_kernel(ConvParams p)
 #pragma unroll
         for (int k = 0; k < W; ++k) w[k][j] = __ldg(p.w + (size_t)(c0 + j) * W + k);
     }
-    // hist[k] = raw row t0-(W-1)+k of these channels (from the state when < 0)
-    float hist[W > 1 ? W - 1 : 1][V];
 #pragma unroll
-    for (int k = 0; k < W - 1; ++k) {
-        const int r = t0 - (W - 1) + k;
-        if (r >= 0) {
-            Vec16<T>::load(x + ((size_t)b * p.S + r) * p.C + c0, hist[k]);
-        } else if (st) {
-            Vec16<T>::load(st + ((size_t)b * (W - 1) + (r + W - 1)) * p.C + c0, hist[k]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < V; ++j) hist[k][j] = 0.0f;
-        }
-    }
-    for (int t = t0; t < t1; ++t) {
-        float cur[V], o[V];
-        Vec16<T>::load(x + ((size_t)b * p.S + t) * p.C + c0, cur);
+    for (int i = 0; i < R; ++i) {
+        if (i >= nrows) break;
+        float o[V];
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             float v = bias[j];
 #pragma unroll
-            for (int k = 0; k < W - 1; ++k) v = fmaf(w[k][j], hist[k][j], v);
-            v = fmaf(w[W - 1][j], cur[j], v);
+            for (int k = 0; k < W; ++k) v = fmaf(w[k][j], u[i + k][j], v);
             o[j] = silu_f32(v);
         }
-        Vec16<T>::store(out + ((size_t)b * p.S + t) * p.out_stride + o0, o);
-#pragma unroll
-        for (int k = 0; k + 1 < W - 1; ++k)
-#pragma unroll
-            for (int j = 0; j < V; ++j) hist[k][j] = hist[k + 1][j];
-        if (W > 1) {
-#pragma unroll
-            for (int j = 0; j < V; ++j) hist[W > 1 ? W - 2 : 0][j] = cur[j];
-        }
+        Vec16<T>::store(out + ((size_t)b * p.S + t0 + i) * p.out_stride + o0, o);
     }
 }
 

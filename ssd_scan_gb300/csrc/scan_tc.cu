@@ -26,10 +26,13 @@
 // warpgroups split the columns.  The threads compute dt and the cumulative
 // sum (a double-float warp-shuffle scan), the x conv + SiLU from the raw TMA
 // tile (4 rows x 8 channels per thread), the causal mask with its decays
-// (blocks above the diagonal are written as zeros without a TMEM read), the
-// state update and the epilogue y = Yd + exp(gamma_t) Yo + D x, times
-// silu(z).  Thread 0 issues the TMA loads and the MMAs.  B and C of a group
-// are read by each of its heads' CTAs; they come from L2 after the first.
+// (blocks above the diagonal are written as zeros without a TMEM read; when
+// the chunk's total decay is moderate the decay factors into exp(gamma_t) and
+// exp(-gamma_s) dt_s, otherwise each entry takes its own clamped exponent),
+// the state update and the epilogue y = Yd + exp(gamma_t) Yo, times silu(z);
+// D x enters G2 through D on the diagonal of M.  Thread 0 issues the TMA
+// loads and the MMAs.  B and C of a group are read by each of its heads'
+// CTAs; they come from L2 after the first.
 #include "internal.cuh"
 #include "sm100.cuh"
 
@@ -60,20 +63,27 @@ struct __align__(1024) TcSmem {
     __nv_bfloat16 B[2][Q * 64];    // B tile [s][n]
     __nv_bfloat16 Xr[Q * 64];      // x tile [t][p] (raw rows when the conv is fused)
     __nv_bfloat16 Z[Q * 64];       // z tile [t][p]
-    __nv_bfloat16 XR[Q * 64];      // post-conv x rows [s][p] (SW128): G2's B, the D x term
+    __nv_bfloat16 XR[Q * 64];      // post-conv x rows [s][p] (SW128): G2's B
     __nv_bfloat16 XW[Q * 64];      // (w o x) rows [s][p]: G4's B
     __nv_bfloat16 M[2][Q * 64];    // masked decayed CB [t][s]: G2's A (K-major)
     __nv_bfloat16 Hs[N * 64];      // bf16 state rows [n][p]: G3's B
     __nv_bfloat16 carry[2][kMaxW - 1][P];  // raw x rows before the chunk, by parity
-    float4 wconv[P];               // 4 taps per x channel (front-padded with zeros)
-    float bconv[P];
-    float g2h[Q], g2l[Q], dts[Q], wrow[Q];  // gamma*log2(e) (hi, lo), dt, w_s
+    float2 wconv[P / 2][kMaxW];    // taps of channel pairs (front-padded with zeros)
+    float2 bconv[P / 2];
+    float g2h[Q], g2l[Q];          // gamma * log2(e), double-float (hi, lo)
+    float dts[Q];                  // dt_s
+    float vfac[Q];                 // exp(-gamma_s) dt_s (factored mask only)
+    float wrow[Q];                 // w_s = exp(min(gamma_Q - gamma_s, 0)) dt_s
     float wsum_hi[4], wsum_lo[4];
     uint64_t bar_ld, bar_z, bar_g1, bar_g34, bar_g2;
     uint32_t tmem_base;
 };
 
 constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;
+
+// Below this total chunk decay (log2 units) the mask factors as
+// exp(gamma_t) * exp(-gamma_s): every factor stays within fp32 (2^90 < 2^127).
+constexpr float kFactorMinLog2 = -90.0f;
 
 __device__ __forceinline__ float tanh_fast(float v)
 {
@@ -82,11 +92,11 @@ __device__ __forceinline__ float tanh_fast(float v)
     return t;
 }
 
-// silu via one MUFU op: v * sigmoid(v) = 0.5 v (1 + tanh(v / 2)).
-__device__ __forceinline__ float silu_fast(float v)
+// silu(v) = v sigmoid(v) = 0.5 v (1 + tanh(v / 2)), two lanes at a time.
+__device__ __forceinline__ float2 silu2(float2 v)
 {
-    const float hv = 0.5f * v;
-    return fmaf(hv, tanh_fast(hv), hv);
+    const float2 hv = __fmul2_rn(v, make_float2(0.5f, 0.5f));
+    return __ffma2_rn(hv, make_float2(tanh_fast(hv.x), tanh_fast(hv.y)), hv);
 }
 
 __device__ __forceinline__ float ex2_fast(float v)
@@ -107,32 +117,34 @@ __device__ __forceinline__ void df_add(float& hi, float& lo, float bhi, float bl
     lo = e - (hi - s);
 }
 
-__device__ __forceinline__ void unpack8(uint4 r, float* f)
+__device__ __forceinline__ void unpack4x2(uint4 r, float2* f)
 {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 t = __bfloat1622float2(h[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
-    }
+    for (int i = 0; i < 4; ++i) f[i] = __bfloat1622float2(h[i]);
 }
 
-__device__ __forceinline__ uint32_t pack2(float a, float b)
+__device__ __forceinline__ uint32_t pack2(float2 a)
 {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    __nv_bfloat162 h = __float22bfloat162_rn(a);
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ uint4 pack8(const float* f)
+__device__ __forceinline__ uint4 pack4x2(const float2* f)
 {
-    return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+    return make_uint4(pack2(f[0]), pack2(f[1]), pack2(f[2]), pack2(f[3]));
 }
 
 // byte offset of 16-byte chunk j of row r in a SW128 tile of 64-element rows.
 __device__ __forceinline__ uint32_t chunk_off(int r, int j)
 {
     return (uint32_t)(r * 128 + (((j ^ r) & 7) << 4));
+}
+
+template <typename T>
+__device__ __forceinline__ T& at(void* base, uint32_t off)
+{
+    return *reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(base) + off);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -144,8 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     TcSmem& s = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3;      // TMEM lane quarter of this warp
-    const int half = warp >> 2;        // column half of this warpgroup
+    const int quarter = warp & 3;         // TMEM lane quarter of this warp
+    const int half = warp >> 2;           // column half of this warpgroup
     const int row = 32 * quarter + lane;  // chunk row t (or state column n) of this thread
     const int h = blockIdx.x, b = blockIdx.y;
     const int H = p.H, G = p.G, W = p.W;
@@ -171,11 +183,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     if (p.conv) {
-        for (int i = tid; i < P; i += kThreads) {
-            float w4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            for (int k = 0; k < W; ++k) w4[kMaxW - W + k] = p.conv_w[(size_t)(h * P + i) * W + k];
-            s.wconv[i] = make_float4(w4[0], w4[1], w4[2], w4[3]);
-            s.bconv[i] = p.conv_b ? p.conv_b[h * P + i] : 0.0f;
+        for (int i = tid; i < P / 2; i += kThreads) {
+            float w4[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            for (int e = 0; e < 2; ++e)
+                for (int k = 0; k < W; ++k)
+                    w4[e][kMaxW - W + k] = p.conv_w[(size_t)(h * P + 2 * i + e) * W + k];
+            for (int k = 0; k < kMaxW; ++k) s.wconv[i][k] = make_float2(w4[0][k], w4[1][k]);
+            s.bconv[i] = p.conv_b ? make_float2(p.conv_b[h * P + 2 * i], p.conv_b[h * P + 2 * i + 1])
+                                  : make_float2(0.f, 0.f);
         }
         // raw rows -3..-1 before chunk 0: the last rows of the conv state (or zeros)
         const __nv_bfloat16* cs = static_cast<const __nv_bfloat16*>(p.conv_state_in);
@@ -188,44 +203,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // The fp32 state: thread (n = row, half) owns h[32*half .. 32*half+31][n].
+    // The fp32 state: thread (n = row, half) owns h[32*half .. 32*half+31][n],
+    // as 16 pairs of consecutive p.
     const int n = row;
     const int p0 = 32 * half;
     const size_t sbase = ((size_t)b * H + h) * P * N;
-    float hreg[32];
+    float2 hreg[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) hreg[i] = p.h0 ? p.h0[sbase + (size_t)(p0 + i) * N + n] : 0.0f;
+    for (int i = 0; i < 16; ++i)
+        hreg[i] = p.h0 ? make_float2(p.h0[sbase + (size_t)(p0 + 2 * i) * N + n],
+                                     p.h0[sbase + (size_t)(p0 + 2 * i + 1) * N + n])
+                       : make_float2(0.f, 0.f);
     // Hs row n holds bf16 h[0..63][n]; this thread writes its 4 chunks of 8 p
     auto store_h = [&]() {
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
-            *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(s.Hs) + chunk_off(n, 4 * half + q4)) =
-                pack8(&hreg[8 * q4]);
+            at<uint4>(s.Hs, chunk_off(n, 4 * half + q4)) = pack4x2(&hreg[4 * q4]);
     };
     store_h();
 
-    // conv work split: thread (j = channel group of 8, rb = block of 4 rows)
+    // conv work split: thread (cj = channel group of 8, rb = block of 4 rows)
     const int cj = tid & 7, rb = tid >> 3;
-    float4 wq[8];
-    float bq[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) wq[e] = make_float4(0.f, 0.f, 0.f, 0.f), bq[e] = 0.0f;
 
     const float Ah = p.A[h];
     const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
     const float Dh = p.D ? p.D[h] : 0.0f;
-    const int trow = tid & (Q - 1);  // row for the dt scan (both warpgroups scan the same rows)
-    float dt_next = trow < p.S ? p.dt[((size_t)b * p.S + trow) * H + h] : 0.0f;
+    float dt_next = (half == 0 && row < p.S) ? p.dt[((size_t)b * p.S + row) * H + h] : 0.0f;
 
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    float2 wq[4][kMaxW], bq[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        bq[e] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < kMaxW; ++k) wq[e][k] = make_float2(0.f, 0.f);
+    }
     if (p.conv) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            wq[e] = s.wconv[8 * cj + e];
-            bq[e] = s.bconv[8 * cj + e];
+        for (int e = 0; e < 4; ++e) {
+            bq[e] = s.bconv[4 * cj + e];
+#pragma unroll
+            for (int k = 0; k < kMaxW; ++k) wq[e][k] = s.wconv[4 * cj + e][k];
         }
     }
     const uint32_t tbase = s.tmem_base;
@@ -261,31 +282,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r0 = c * Q;
         const int rows = min(Q, p.S - r0);
 
-        // ---- dt and the cumulative sum of a = dt A (double-float) --------------
-        float dt = 0.0f;
-        if (trow < rows) dt = softplus ? softplus_f32(dt_next + bias) : dt_next;
-        if (c + 1 < nchunks)
-            dt_next = r0 + Q + trow < p.S ? p.dt[((size_t)b * p.S + r0 + Q + trow) * H + h] : 0.0f;
-        float ghi = dt * Ah, glo = 0.0f;
+        // ---- dt and the cumulative sum of a = dt A (double-float), warpgroup 0 ----
+        float ghi = 0.0f, glo = 0.0f, dt = 0.0f;
+        if (half == 0) {
+            if (row < rows) dt = softplus ? softplus_f32(dt_next + bias) : dt_next;
+            if (c + 1 < nchunks)
+                dt_next = r0 + Q + row < p.S ? p.dt[((size_t)b * p.S + r0 + Q + row) * H + h] : 0.0f;
+            ghi = dt * Ah;
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const float ohi = __shfl_up_sync(0xffffffffu, ghi, d);
-            const float olo = __shfl_up_sync(0xffffffffu, glo, d);
-            if (lane >= d) df_add(ghi, glo, ohi, olo);
-        }
-        if (half == 0 && lane == 31) {
-            s.wsum_hi[quarter] = ghi;
-            s.wsum_lo[quarter] = glo;
+            for (int d = 1; d < 32; d <<= 1) {
+                const float ohi = __shfl_up_sync(0xffffffffu, ghi, d);
+                const float olo = __shfl_up_sync(0xffffffffu, glo, d);
+                if (lane >= d) df_add(ghi, glo, ohi, olo);
+            }
+            if (lane == 31) {
+                s.wsum_hi[quarter] = ghi;
+                s.wsum_lo[quarter] = glo;
+            }
         }
         __syncthreads();
-        for (int w2 = 0; w2 < quarter; ++w2) df_add(ghi, glo, s.wsum_hi[w2], s.wsum_lo[w2]);
-        // ghi/glo: gamma of row trow (== row for every thread)
         if (half == 0) {
-            s.g2h[trow] = ghi * kLog2e;
-            s.g2l[trow] = glo * kLog2e;
-            s.dts[trow] = dt;
+            for (int w2 = 0; w2 < quarter; ++w2) df_add(ghi, glo, s.wsum_hi[w2], s.wsum_lo[w2]);
+            s.g2h[row] = ghi * kLog2e;
+            s.g2l[row] = glo * kLog2e;
+            s.dts[row] = dt;
         }
-        float gLh, gLl;  // gamma (log2 units) of the chunk's last row, from shared memory
 
         // ---- this chunk's tiles; G1 = C B^T ---------------------------------------
         ok = ok && mbar_wait_ns(&s.bar_ld, par, kWaitNs);
@@ -300,35 +321,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&s.bar_g1);
         }
         __syncthreads();
-        gLh = s.g2h[rows - 1];
-        gLl = s.g2l[rows - 1];
-        const float g2h_t = ghi * kLog2e, g2l_t = glo * kLog2e;
-        // exp(min(gamma_t,0)), w_t = exp(min(gamma_Q - gamma_t, 0)) dt_t, exp(min(gamma_Q,0))
-        const float decay_t = ex2_fast(fminf(g2h_t + g2l_t, 0.0f));
-        const float decay_S = ex2_fast(fminf(gLh + gLl, 0.0f));
+        // gamma of this thread's row t and of the chunk's last row (log2 units)
+        const float g2h_t = s.g2h[row], g2l_t = s.g2l[row];
+        const float gLh = s.g2h[rows - 1], gLl = s.g2l[rows - 1];
+        const float decay_t = ex2_fast(fminf(g2h_t + g2l_t, 0.0f));  // exp(min(gamma_t, 0))
+        const float decay_S = ex2_fast(fminf(gLh + gLl, 0.0f));      // exp(min(gamma_Q, 0))
+        // factored mask: a <= 0 everywhere (A <= 0) and gamma_Q not too negative
+        const bool factored = Ah <= 0.0f && gLh + gLl >= kFactorMinLog2;
         if (half == 0) {
-            const float w_t = trow < rows ? ex2_fast(fminf((gLh - g2h_t) + (gLl - g2l_t), 0.0f)) * dt
-                                          : 0.0f;
-            s.wrow[trow] = w_t;
+            const float dtt = s.dts[row];
+            s.wrow[row] = row < rows ? ex2_fast(fminf((gLh - g2h_t) + (gLl - g2l_t), 0.0f)) * dtt
+                                     : 0.0f;
+            if (factored) s.vfac[row] = ex2_fast(-(g2h_t + g2l_t)) * dtt;
         }
         __syncthreads();
 
         // ---- x: conv + SiLU of 4 rows x 8 channels per thread -> x, w x rows ------
         {
             const int t0 = 4 * rb;
-            float xo[4][8];
+            float2 xo[4][4];  // [row][channel pair]
             if (p.conv) {
-                float win[7][8];  // raw rows t0-3 .. t0+3
+                float2 win[7][4];  // raw rows t0-3 .. t0+3
 #pragma unroll
                 for (int k = 0; k < 7; ++k) {
                     const int r = t0 - 3 + k;
-                    uint4 raw;
-                    if (r >= 0)
-                        raw = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(s.Xr) +
-                                                              chunk_off(r, cj));
-                    else
-                        raw = *reinterpret_cast<const uint4*>(&s.carry[par][r + 3][8 * cj]);
-                    unpack8(raw, win[k]);
+                    const uint4 raw = r >= 0 ? at<const uint4>(s.Xr, chunk_off(r, cj))
+                                             : *reinterpret_cast<const uint4*>(&s.carry[par][r + 3][8 * cj]);
+                    unpack4x2(raw, win[k]);
                     if (r >= Q - (kMaxW - 1))  // rows Q-3..Q-1 carry into the next chunk
                         *reinterpret_cast<uint4*>(&s.carry[par ^ 1][r - (Q - 3)][8 * cj]) = raw;
                 }
@@ -336,33 +355,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 4; ++i) {
                     const bool valid = t0 + i < rows;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        float v = bq[e];
-                        v = fmaf(wq[e].x, win[i][e], v);
-                        v = fmaf(wq[e].y, win[i + 1][e], v);
-                        v = fmaf(wq[e].z, win[i + 2][e], v);
-                        v = fmaf(wq[e].w, win[i + 3][e], v);
-                        xo[i][e] = valid ? silu_fast(v) : 0.0f;
+                    for (int e = 0; e < 4; ++e) {
+                        float2 v = bq[e];
+#pragma unroll
+                        for (int k = 0; k < kMaxW; ++k) v = __ffma2_rn(wq[e][k], win[i + k][e], v);
+                        xo[i][e] = valid ? silu2(v) : make_float2(0.f, 0.f);
                     }
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint4 raw = *reinterpret_cast<const uint4*>(
-                        reinterpret_cast<const uint8_t*>(s.Xr) + chunk_off(t0 + i, cj));
-                    unpack8(raw, xo[i]);
-                }
+                for (int i = 0; i < 4; ++i) unpack4x2(at<const uint4>(s.Xr, chunk_off(t0 + i, cj)), xo[i]);
             }
             const float4 w4 = *reinterpret_cast<const float4*>(&s.wrow[t0]);
             const float wr[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                float xw[8];
+                float2 xw[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) xw[e] = wr[i] * xo[i][e];
+                for (int e = 0; e < 4; ++e) xw[e] = __fmul2_rn(make_float2(wr[i], wr[i]), xo[i][e]);
                 const uint32_t off = chunk_off(t0 + i, cj);
-                *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(s.XR) + off) = pack8(xo[i]);
-                *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(s.XW) + off) = pack8(xw);
+                at<uint4>(s.XR, off) = pack4x2(xo[i]);
+                at<uint4>(s.XW, off) = pack4x2(xw);
             }
         }
         fence_proxy_async_smem();
@@ -383,7 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&s.bar_g34);
         }
 
-        // ---- causal mask with decays: M[t,s] = CB[t,s] 2^(g2_t - g2_s) dt_s ------
+        // ---- causal mask with decays: M[t,s] = CB[t,s] exp(gamma_t - gamma_s) dt_s,
+        //      plus D on the diagonal (so G2 also adds D x_t) -------------------------
         ok = ok && mbar_wait_ns(&s.bar_g1, par, kWaitNs);
         tc_fence_after();
         {
@@ -391,39 +405,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int cb2 = 0; cb2 < 2; ++cb2) {
                 const int cc = 2 * half + cb2;  // 32-column block of this thread
-                uint8_t* mrow = reinterpret_cast<uint8_t*>(s.M[cc >> 1]);
+                __nv_bfloat16* mpanel = s.M[cc >> 1];
                 if (cc > quarter) {  // strictly above the diagonal for the whole warp
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const int k = (cc & 1) * 32 + q4 * 8;
-                        *reinterpret_cast<uint4*>(mrow + chunk_off(t, k >> 3)) = make_uint4(0, 0, 0, 0);
-                    }
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        at<uint4>(mpanel, chunk_off(t, (cc & 1) * 4 + q4)) = make_uint4(0, 0, 0, 0);
                     continue;
                 }
                 float v[32];
                 tmem_ld32(t_cb + lane_off + cc * 32, v);
                 tmem_ld_wait();
+                const bool diag = cc == quarter;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     const int sb = cc * 32 + q4 * 8;
-                    const float4 h0 = *reinterpret_cast<const float4*>(&s.g2h[sb]);
-                    const float4 h1 = *reinterpret_cast<const float4*>(&s.g2h[sb + 4]);
-                    const float4 l0 = *reinterpret_cast<const float4*>(&s.g2l[sb]);
-                    const float4 l1 = *reinterpret_cast<const float4*>(&s.g2l[sb + 4]);
-                    const float4 d0 = *reinterpret_cast<const float4*>(&s.dts[sb]);
-                    const float4 d1 = *reinterpret_cast<const float4*>(&s.dts[sb + 4]);
-                    const float gh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-                    const float gl[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-                    const float ds[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-                    float m[8];
+                    float2 m[4];
+                    if (factored) {
+                        const float4 f0 = *reinterpret_cast<const float4*>(&s.vfac[sb]);
+                        const float4 f1 = *reinterpret_cast<const float4*>(&s.vfac[sb + 4]);
+                        const float2 uu = make_float2(decay_t, decay_t);
+                        m[0] = __fmul2_rn(__fmul2_rn(make_float2(v[q4 * 8 + 0], v[q4 * 8 + 1]), make_float2(f0.x, f0.y)), uu);
+                        m[1] = __fmul2_rn(__fmul2_rn(make_float2(v[q4 * 8 + 2], v[q4 * 8 + 3]), make_float2(f0.z, f0.w)), uu);
+                        m[2] = __fmul2_rn(__fmul2_rn(make_float2(v[q4 * 8 + 4], v[q4 * 8 + 5]), make_float2(f1.x, f1.y)), uu);
+                        m[3] = __fmul2_rn(__fmul2_rn(make_float2(v[q4 * 8 + 6], v[q4 * 8 + 7]), make_float2(f1.z, f1.w)), uu);
+                    } else {
+                        const float4 h0 = *reinterpret_cast<const float4*>(&s.g2h[sb]);
+                        const float4 h1 = *reinterpret_cast<const float4*>(&s.g2h[sb + 4]);
+                        const float4 l0 = *reinterpret_cast<const float4*>(&s.g2l[sb]);
+                        const float4 l1 = *reinterpret_cast<const float4*>(&s.g2l[sb + 4]);
+                        const float4 d0 = *reinterpret_cast<const float4*>(&s.dts[sb]);
+                        const float4 d1 = *reinterpret_cast<const float4*>(&s.dts[sb + 4]);
+                        const float gh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+                        const float gl[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+                        const float ds[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+                        float mm[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float ex = (g2h_t - gh[e]) + (g2l_t - gl[e]);
-                        const float val = v[q4 * 8 + e] * ds[e] * ex2_fast(fminf(ex, 0.0f));
-                        m[e] = (sb + e <= t) ? val : 0.0f;
+                        for (int e = 0; e < 8; ++e) {
+                            const float ex = (g2h_t - gh[e]) + (g2l_t - gl[e]);
+                            mm[e] = v[q4 * 8 + e] * ds[e] * ex2_fast(fminf(ex, 0.0f));
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) m[e] = make_float2(mm[2 * e], mm[2 * e + 1]);
                     }
-                    const int k = (cc & 1) * 32 + q4 * 8;
-                    *reinterpret_cast<uint4*>(mrow + chunk_off(t, k >> 3)) = pack8(m);
+                    if (diag) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int s0 = sb + 2 * e;
+                            m[e].x = s0 < t ? m[e].x : (s0 == t ? m[e].x + Dh : 0.0f);
+                            m[e].y = s0 + 1 < t ? m[e].y : (s0 + 1 == t ? m[e].y + Dh : 0.0f);
+                        }
+                    }
+                    at<uint4>(mpanel, chunk_off(t, (cc & 1) * 4 + q4)) = pack4x2(m);
                 }
             }
         }
@@ -449,12 +481,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v[32];
             tmem_ld32(t_st + lane_off + p0, v);
             tmem_ld_wait();
+            const float2 dd = make_float2(decay_S, decay_S);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) hreg[i] = fmaf(decay_S, hreg[i], v[i]);
+            for (int i = 0; i < 16; ++i)
+                hreg[i] = __ffma2_rn(dd, hreg[i], make_float2(v[2 * i], v[2 * i + 1]));
             store_h();
         }
 
-        // ---- epilogue: y = Yd + exp(gamma_t) Yo + D x, gated ------------------------
+        // ---- epilogue: y = Yd + exp(gamma_t) Yo (Yd holds D x), gated -------------
         ok = ok && mbar_wait_ns(&s.bar_g2, par, kWaitNs);
         if (has_z) ok = ok && mbar_wait_ns(&s.bar_z, par, kWaitNs);
         tc_fence_after();
@@ -466,23 +500,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
             uint4* yrow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) +
                                                    (((size_t)b * p.S + r0 + t) * H + h) * P + p0);
+            const float2 dec = make_float2(decay_t, decay_t);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-                const int j = 4 * half + q4;
-                float xv[8], zv[8], out[8];
-                unpack8(*reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(s.XR) +
-                                                        chunk_off(t, j)), xv);
-                if (has_z)
-                    unpack8(*reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(s.Z) +
-                                                            chunk_off(t, j)), zv);
+                float2 out[4], zv[4];
+                if (has_z) unpack4x2(at<const uint4>(s.Z, chunk_off(t, 4 * half + q4)), zv);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float yv = fmaf(decay_t, yo[q4 * 8 + e], yd[q4 * 8 + e]);
-                    yv = fmaf(Dh, xv[e], yv);
-                    if (has_z) yv *= silu_fast(zv[e]);
+                for (int e = 0; e < 4; ++e) {
+                    const int k = q4 * 8 + 2 * e;
+                    float2 yv = __ffma2_rn(dec, make_float2(yo[k], yo[k + 1]),
+                                           make_float2(yd[k], yd[k + 1]));
+                    if (has_z) yv = __fmul2_rn(yv, silu2(zv[e]));
                     out[e] = yv;
                 }
-                if (t < rows) yrow[q4] = pack8(out);
+                if (t < rows) yrow[q4] = pack4x2(out);
             }
         }
         fence_proxy_async_smem();
@@ -494,7 +525,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (ok) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) p.hS[sbase + (size_t)(p0 + i) * N + n] = hreg[i];
+        for (int i = 0; i < 16; ++i) {
+            p.hS[sbase + (size_t)(p0 + 2 * i) * N + n] = hreg[i].x;
+            p.hS[sbase + (size_t)(p0 + 2 * i + 1) * N + n] = hreg[i].y;
+        }
     } else if (tid == 0) {
         atomicOr(p.err, kErrTimeout);
     }
