@@ -200,3 +200,31 @@ def test_bf16_short_conv_widths(W):
     cpu, dev = make_problem(shape, act=torch.bfloat16)
     y, h, cs = gpu_prefill(shape, dev, [130, 130])
     _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
+
+
+def test_mixed_magnitude_decay_in_one_chunk():
+    """One row with a decay of ~e^-1000 followed by rows of small decay in the
+    same chunk: gamma differences of small rows after the big one must keep
+    their precision (double-float cumulative sum)."""
+    shape = si.Shape(batch=1, seqlen=256, nheads=4, headdim=64, dstate=128, ngroups=1)
+    cpu, dev = make_problem(shape, act=torch.bfloat16)
+    dt_raw = cpu["dt_raw"].clone()
+    dt_raw[0, 40, :] = 300.0     # dt ~ 300 at row 40 -> dt*A ~ -300..-4800
+    dt_raw[0, 170, :] = 120.0    # and one in the second chunk
+    cpu["dt_raw"] = dt_raw
+    dev["dt_raw"] = dt_raw.cuda()
+    y, h, cs = gpu_prefill(shape, dev)
+    assert torch.isfinite(y.float()).all() and torch.isfinite(h).all()
+    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
+
+
+@pytest.mark.parametrize("scale", [0.25, 1.0, 4.0, 16.0])
+def test_decay_range_across_factored_threshold(scale):
+    """Chunks whose total decay falls on either side of the range where the
+    mask factors into exp(gamma_t) exp(-gamma_s) give the same answer."""
+    shape = si.Shape(batch=1, seqlen=384, nheads=8, headdim=64, dstate=128, ngroups=2)
+    cpu, dev = make_problem(shape, act=torch.bfloat16, seed=7)
+    cpu["A"] = cpu["A"] * scale
+    dev["A"] = cpu["A"].cuda()
+    y, h, cs = gpu_prefill(shape, dev)
+    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
