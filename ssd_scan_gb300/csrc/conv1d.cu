@@ -16,16 +16,20 @@ namespace {
 
 constexpr int kRowsPerThread = 8;
 
+// 16 bytes of channels: 8 bf16 or 4 fp32, kept packed in registers.
 template <typename T> struct Vec16;
 template <> struct Vec16<__nv_bfloat16> {
     static constexpr int n = 8;
-    __device__ static void load(const __nv_bfloat16* p, float* v)
+    __device__ static uint4 load(const __nv_bfloat16* p)
     {
-        uint4 r = __ldg(reinterpret_cast<const uint4*>(p));
+        return __ldg(reinterpret_cast<const uint4*>(p));
+    }
+    __device__ static void unpack(uint4 r, float* v)
+    {
         const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            float2 f = __bfloat1622float2(h[i]);
+            const float2 f = __bfloat1622float2(h[i]);
             v[2 * i] = f.x;
             v[2 * i + 1] = f.y;
         }
@@ -38,18 +42,33 @@ template <> struct Vec16<__nv_bfloat16> {
         for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
         *reinterpret_cast<uint4*>(p) = r;
     }
+    // bf16 outputs: silu through one tanh.approx (relative error ~2^-11,
+    // below the bf16 rounding of the result)
+    __device__ static float silu(float v)
+    {
+        float t;
+        const float hv = 0.5f * v;
+        asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(hv));
+        return fmaf(hv, t, hv);
+    }
 };
 template <> struct Vec16<float> {
     static constexpr int n = 4;
-    __device__ static void load(const float* p, float* v)
+    __device__ static uint4 load(const float* p)
     {
-        float4 r = __ldg(reinterpret_cast<const float4*>(p));
-        v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
+        return __ldg(reinterpret_cast<const uint4*>(p));
+    }
+    __device__ static void unpack(uint4 r, float* v)
+    {
+        v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
+        v[2] = __uint_as_float(r.z); v[3] = __uint_as_float(r.w);
     }
     __device__ static void store(float* p, const float* v)
     {
         *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
     }
+    // fp32 outputs: exp + fast reciprocal division (a few ulp)
+    __device__ static float silu(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 };
 
 template <typename T, int W>
@@ -69,29 +88,19 @@ __global__ void __launch_bounds__(128) conv1d_rows_kernel(ConvParams p)
     const T* __restrict__ st = static_cast<const T*>(p.st_in);
     T* __restrict__ out = static_cast<T*>(p.out);
 
-    // raw rows t0-(W-1) .. t0+R-1 of these channels, all loads issued up front
-    float u[R + W - 1][V];
+    // raw rows t0-(W-1) .. t0+R-1 of these channels, packed, all loads up front
+    uint4 u[R + W - 1];
 #pragma unroll
     for (int k = 0; k < W - 1; ++k) {
         const int r = t0 - (W - 1) + k;
-        if (r >= 0) {
-            Vec16<T>::load(x + ((size_t)b * p.S + r) * p.C + c0, u[k]);
-        } else if (st) {
-            Vec16<T>::load(st + ((size_t)b * (W - 1) + (r + W - 1)) * p.C + c0, u[k]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < V; ++j) u[k][j] = 0.0f;
-        }
+        if (r >= 0) u[k] = Vec16<T>::load(x + ((size_t)b * p.S + r) * p.C + c0);
+        else if (st) u[k] = Vec16<T>::load(st + ((size_t)b * (W - 1) + (r + W - 1)) * p.C + c0);
+        else u[k] = make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-        if (i < nrows) {
-            Vec16<T>::load(x + ((size_t)b * p.S + t0 + i) * p.C + c0, u[W - 1 + i]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < V; ++j) u[W - 1 + i][j] = 0.0f;
-        }
-    }
+    for (int i = 0; i < R; ++i)
+        u[W - 1 + i] = i < nrows ? Vec16<T>::load(x + ((size_t)b * p.S + t0 + i) * p.C + c0)
+                                 : make_uint4(0, 0, 0, 0);
     float w[W][V], bias[V];
 #pragma unroll
     for (int j = 0; j < V; ++j) {
@@ -104,12 +113,16 @@ __global__ void __launch_bounds__(128) conv1d_rows_kernel(ConvParams p)
         if (i >= nrows) break;
         float o[V];
 #pragma unroll
-        for (int j = 0; j < V; ++j) {
-            float v = bias[j];
+        for (int j = 0; j < V; ++j) o[j] = bias[j];
 #pragma unroll
-            for (int k = 0; k < W; ++k) v = fmaf(w[k][j], u[i + k][j], v);
-            o[j] = silu_f32(v);
+        for (int k = 0; k < W; ++k) {
+            float f[V];
+            Vec16<T>::unpack(u[i + k], f);
+#pragma unroll
+            for (int j = 0; j < V; ++j) o[j] = fmaf(w[k][j], f[j], o[j]);
         }
+#pragma unroll
+        for (int j = 0; j < V; ++j) o[j] = Vec16<T>::silu(o[j]);
         Vec16<T>::store(out + ((size_t)b * p.S + t0 + i) * p.out_stride + o0, o);
     }
 }
