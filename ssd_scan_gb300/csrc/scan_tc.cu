@@ -40,6 +40,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <cstddef>
 #include <mutex>
 
 namespace ssd {
@@ -69,7 +70,7 @@ constexpr uint32_t kColCB = 0, kColYd = 128, kColYo = 256, kColDH = 384;
 // exp(gamma_t) * exp(-gamma_s): every factor stays within fp32 (2^90 < 2^127).
 constexpr float kFactorMinLog2 = -90.0f;
 
-struct ChunkVals {             // per-chunk row values, written by the front
+struct __align__(16) ChunkVals {  // per-chunk row values, written by the front
     float g2h[Q], g2l[Q];      // gamma * log2(e), double-float (hi, lo)
     float dts[Q];              // dt_s
     float vfac[Q];             // exp(-gamma_s) dt_s (factored mask only)
@@ -87,8 +88,8 @@ struct __align__(1024) TcSmem {
     __nv_bfloat16 M[2][Q * 64];     // masked decayed CB [t][s]: G2's A (K-major)
     __nv_bfloat16 Hs[N * 64];       // bf16 state rows [n][p]: G3's B
     ChunkVals cv[2];
-    __nv_bfloat16 carry[2][kMaxW - 1][P];  // raw x rows before the chunk, by parity
-    float2 wconv[P / 2][kMaxW];     // taps of channel pairs (front-padded with zeros)
+    alignas(16) __nv_bfloat16 carry[2][kMaxW - 1][P];  // raw x rows before the chunk, by parity
+    alignas(16) float2 wconv[P / 2][kMaxW];     // taps of channel pairs (front-padded with zeros)
     float2 bconv[P / 2];
     float wsum_hi[4], wsum_lo[4];
     uint64_t tma_bc, tma_x[2], g1, g2[2], g3[2], g4[2];
@@ -98,6 +99,19 @@ struct __align__(1024) TcSmem {
 };
 
 constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;
+
+// operand tiles start on 1024-byte swizzle atoms; vector-accessed members on
+// their vector size
+static_assert(offsetof(TcSmem, C) % 1024 == 0 && offsetof(TcSmem, B) % 1024 == 0, "tile");
+static_assert(offsetof(TcSmem, Xr) % 1024 == 0 && offsetof(TcSmem, XR) % 1024 == 0, "tile");
+static_assert(offsetof(TcSmem, XW) % 1024 == 0 && offsetof(TcSmem, M) % 1024 == 0, "tile");
+static_assert(offsetof(TcSmem, Hs) % 1024 == 0, "tile");
+static_assert(sizeof(ChunkVals) % 16 == 0 && offsetof(TcSmem, cv) % 16 == 0, "float4 rows");
+static_assert(offsetof(ChunkVals, vfac) % 16 == 0 && offsetof(ChunkVals, wrow) % 16 == 0, "float4");
+static_assert(offsetof(TcSmem, carry) % 16 == 0 && (P * 2) % 16 == 0, "uint4 carry rows");
+static_assert(offsetof(TcSmem, wconv) % 8 == 0 && offsetof(TcSmem, bconv) % 8 == 0, "float2");
+static_assert(offsetof(TcSmem, tma_bc) % 8 == 0, "mbarriers");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ float tanh_fast(float v)
 {
