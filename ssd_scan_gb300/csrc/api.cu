@@ -262,8 +262,7 @@ ssd_status ssd_decode_step(const ssd_dims* dims, ssd_dtype act, unsigned flags, 
     if (conv_w == nullptr && (conv_pool || conv_b)) return SSD_ERR_INVALID_ARG;
     if (conv_w && (!aligned4(conv_w) || conv_pool == nullptr || !aligned16(conv_pool)))
         return SSD_ERR_INVALID_ARG;
-    if (dims->dstate % 4 != 0 || dims->headdim % 4 != 0) return SSD_ERR_UNSUPPORTED;
-    if (sizeof(float) * (size_t)(dims->headdim + 2 * dims->dstate) > 200 * 1024)
+    if (!decode_supports(dims->nheads, dims->headdim, dims->dstate, dims->ngroups))
         return SSD_ERR_UNSUPPORTED;
     if (!rows) return SSD_OK;
 

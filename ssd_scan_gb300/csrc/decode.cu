@@ -6,40 +6,49 @@
 // in place, with no gather/scatter copies of the states).
 //
 // The state read-modify-write is the whole cost: per (row, head) P*N fp32
-// are read once and written once.  One CTA per (row i, head h): its warps
-// split the P state rows; a lane owns 16 bytes (4 consecutive n) of a state
-// row, so every warp access is a contiguous 512-byte run, loaded with
-// streaming hints (the pool is touched once per step).  y[p] is a warp
-// shuffle reduction over n.
+// are read once and written once.  One CTA per (row i, group g): it conv's
+// the x columns of the group's heads and the group's B and C columns once
+// (the B|C conv is shared by the heads of the group), then its warps stream
+// the state rows of those heads.  A lane owns 16 bytes (4 consecutive n) of
+// a state row, so every warp access is a contiguous 512-byte run, loaded
+// with streaming hints (the pool is touched once per step); each warp keeps
+// several rows in flight.  y[p] is a warp shuffle reduction over n.
 #include "internal.cuh"
 
 namespace ssd {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kRowsInFlight = 4;  // state rows a warp keeps in flight
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
 {
-    extern __shared__ float sm[];  // x [P] | B [N] | C [N]
-    const int h = blockIdx.x, i = blockIdx.y;
+    extern __shared__ float sm[];  // x [hpg*P] | B [N] | C [N] | dt, dA [hpg]
+    const int g = blockIdx.x, i = blockIdx.y;
     const int H = p.H, P = p.P, N = p.N, G = p.G;
-    const int g = h / (H / G);
+    const int hpg = H / G;
+    const int h0 = g * hpg;
     const int Cdim = H * P + 2 * G * N;
-    const int CH = P + 2 * N;
+    const int XW = hpg * P;        // x columns of this group
+    const int CH = XW + 2 * N;
     const int s = p.slots[i];
     if (s < 0 || s >= p.num_slots) {
-        if (threadIdx.x == 0 && h == 0) atomicOr(p.err, kErrBadSlot);
+        if (threadIdx.x == 0 && g == 0) atomicOr(p.err, kErrBadSlot);
         return;
     }
     const T* xbc = static_cast<const T*>(p.xbc);
     const T* cpool = static_cast<const T*>(p.conv_pool);
     const int HW = p.W - 1;
+    float* xs = sm;
+    float* Bs = sm + XW;
+    float* Cs = Bs + N;
+    float* dts = Cs + N;
+    float* dAs = dts + hpg;
     for (int c = threadIdx.x; c < CH; c += blockDim.x) {
-        const int gc = c < P ? h * P + c
-                             : (c < P + N ? H * P + g * N + (c - P)
-                                          : H * P + G * N + g * N + (c - P - N));
+        const int gc = c < XW ? h0 * P + c
+                              : (c < XW + N ? H * P + g * N + (c - XW)
+                                            : H * P + G * N + g * N + (c - XW - N));
         float v;
         if (p.conv_w) {
             v = p.conv_b ? p.conv_b[gc] : 0.0f;
@@ -53,22 +62,25 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
         }
         sm[c] = v;
     }
-    float dt = p.dt[(size_t)i * H + h];
-    if (p.flags & kDtSoftplus) dt = softplus_f32(dt + (p.dt_bias ? p.dt_bias[h] : 0.0f));
-    const float dA = expf(dt * p.A[h]);
-    const float Dh = p.D ? p.D[h] : 0.0f;
+    for (int j = threadIdx.x; j < hpg; j += blockDim.x) {
+        const int h = h0 + j;
+        float dt = p.dt[(size_t)i * H + h];
+        if (p.flags & kDtSoftplus) dt = softplus_f32(dt + (p.dt_bias ? p.dt_bias[h] : 0.0f));
+        dts[j] = dt;
+        dAs[j] = expf(dt * p.A[h]);
+    }
     __syncthreads();
 
-    const float* xs = sm;
-    const float4* B4 = reinterpret_cast<const float4*>(sm + P);
-    const float4* C4 = reinterpret_cast<const float4*>(sm + P + N);
-    float4* st = reinterpret_cast<float4*>(p.pool + ((size_t)s * H + h) * (size_t)P * N);
+    const float4* B4 = reinterpret_cast<const float4*>(Bs);
+    const float4* C4 = reinterpret_cast<const float4*>(Cs);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
     const int nv = N / 4;  // float4 per state row
     const T* zz = static_cast<const T*>(p.z);
     T* y = static_cast<T*>(p.y);
+    const int nrows = hpg * P;  // state rows of this group, head-major
+    float4* st0 = reinterpret_cast<float4*>(p.pool + ((size_t)s * H + h0) * (size_t)P * N);
 
-    for (int p0 = warp * kRowsInFlight; p0 < P; p0 += nwarp * kRowsInFlight) {
+    for (int r0 = warp * kRowsInFlight; r0 < nrows; r0 += nwarp * kRowsInFlight) {
         float acc[kRowsInFlight];
 #pragma unroll
         for (int r = 0; r < kRowsInFlight; ++r) acc[r] = 0.0f;
@@ -76,12 +88,14 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
             float4 hv[kRowsInFlight];
 #pragma unroll
             for (int r = 0; r < kRowsInFlight; ++r)
-                if (p0 + r < P) hv[r] = __ldcs(st + (size_t)(p0 + r) * nv + v);
+                if (r0 + r < nrows) hv[r] = __ldcs(st0 + (size_t)(r0 + r) * nv + v);
             const float4 bv = B4[v], cv = C4[v];
 #pragma unroll
             for (int r = 0; r < kRowsInFlight; ++r) {
-                if (p0 + r >= P) continue;
-                const float dx = dt * xs[p0 + r];
+                if (r0 + r >= nrows) continue;
+                const int j = (r0 + r) / P;  // head within the group
+                const float dt = dts[j], dA = dAs[j];
+                const float dx = dt * xs[r0 + r];
                 float4 o;
                 o.x = fmaf(dA, hv[r].x, dx * bv.x);
                 o.y = fmaf(dA, hv[r].y, dx * bv.y);
@@ -91,7 +105,7 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
                 acc[r] = fmaf(o.y, cv.y, acc[r]);
                 acc[r] = fmaf(o.z, cv.z, acc[r]);
                 acc[r] = fmaf(o.w, cv.w, acc[r]);
-                __stcs(st + (size_t)(p0 + r) * nv + v, o);
+                __stcs(st0 + (size_t)(r0 + r) * nv + v, o);
             }
         }
 #pragma unroll
@@ -99,12 +113,13 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
         }
-        if (lane < kRowsInFlight && p0 + lane < P) {
+        if (lane < kRowsInFlight && r0 + lane < nrows) {
             float a = acc[0];
 #pragma unroll
             for (int r = 1; r < kRowsInFlight; ++r) a = lane == r ? acc[r] : a;
-            const int pp = p0 + lane;
-            float yv = fmaf(Dh, xs[pp], a);
+            const int row = r0 + lane;       // j * P + pp
+            const int h = h0 + row / P, pp = row % P;
+            float yv = fmaf(p.D ? p.D[h] : 0.0f, xs[row], a);
             if (p.flags & kHasZ) {
                 const float zv = to_f32(zz[(size_t)i * H * P + h * P + pp]);
                 yv *= zv / (1.0f + expf(-zv));
@@ -131,13 +146,25 @@ __global__ void decode_conv_roll_kernel(DecodeParams p)
     cp[(size_t)(HW - 1) * Cdim + c] = static_cast<const T*>(p.xbc)[(size_t)i * Cdim + c];
 }
 
+size_t decode_smem_bytes(const DecodeParams& p)
+{
+    const int hpg = p.H / p.G;
+    return sizeof(float) * ((size_t)hpg * p.P + 2 * (size_t)p.N + 2 * (size_t)hpg);
+}
+
 }  // namespace
+
+bool decode_supports(int H, int P, int N, int G)
+{
+    const size_t smem = sizeof(float) * ((size_t)(H / G) * P + 2 * (size_t)N + 2 * (size_t)(H / G));
+    return N % 4 == 0 && P % 4 == 0 && smem <= 200 * 1024;
+}
 
 cudaError_t launch_decode_step(const DecodeParams& p, bool bf16, cudaStream_t st)
 {
     if (p.R == 0) return cudaSuccess;
-    dim3 grid(p.H, p.R);
-    const size_t smem = sizeof(float) * (size_t)(p.P + 2 * p.N);
+    dim3 grid(p.G, p.R);
+    const size_t smem = decode_smem_bytes(p);
     if (bf16) {
         cudaError_t e = cudaFuncSetAttribute(decode_step_kernel<__nv_bfloat16>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

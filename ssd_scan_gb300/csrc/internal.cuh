@@ -111,6 +111,7 @@ struct TcScanParams {
 bool scan_tc_supports(int P, int N);
 cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st);
 
+bool decode_supports(int H, int P, int N, int G);
 cudaError_t launch_decode_step(const DecodeParams& p, bool bf16, cudaStream_t st);
 cudaError_t launch_decode_conv_roll(const DecodeParams& p, bool bf16, cudaStream_t st);
 
