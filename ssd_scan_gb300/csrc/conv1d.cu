@@ -101,12 +101,19 @@ __global__ void __launch_bounds__(128) conv1d_rows_kernel(ConvParams p)
     for (int i = 0; i < R; ++i)
         u[W - 1 + i] = i < nrows ? Vec16<T>::load(x + ((size_t)b * p.S + t0 + i) * p.C + c0)
                                  : make_uint4(0, 0, 0, 0);
+    // taps: the W floats of one channel are contiguous ([C, W] layout)
     float w[W][V], bias[V];
 #pragma unroll
     for (int j = 0; j < V; ++j) {
         bias[j] = p.bias ? __ldg(p.bias + c0 + j) : 0.0f;
+        const float* wc = p.w + (size_t)(c0 + j) * W;
+        if (W == 4 && (reinterpret_cast<uintptr_t>(p.w) & 15) == 0) {
+            const float4 q = __ldg(reinterpret_cast<const float4*>(wc));
+            w[0][j] = q.x; w[1 % W][j] = q.y; w[2 % W][j] = q.z; w[3 % W][j] = q.w;
+        } else {
 #pragma unroll
-        for (int k = 0; k < W; ++k) w[k][j] = __ldg(p.w + (size_t)(c0 + j) * W + k);
+            for (int k = 0; k < W; ++k) w[k][j] = __ldg(wc + k);
+        }
     }
 #pragma unroll
     for (int i = 0; i < R; ++i) {

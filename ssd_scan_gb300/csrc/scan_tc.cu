@@ -175,14 +175,20 @@ __device__ __forceinline__ T& at(void* base, uint32_t off)
     return *reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(base) + off);
 }
 
-// Bounded wait that also gives up as soon as another role has aborted.
+// Bounded wait that also gives up as soon as another role has aborted.  After
+// a few immediate polls it backs off with nanosleep so that waiting warps do
+// not take issue slots from the warps doing the work.
 __device__ __forceinline__ bool wait_or_abort(TcSmem& s, uint64_t* bar, uint32_t parity)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 4; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    uint32_t ns = 32;
     while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        __nanosleep(ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        ns = ns < 256 ? ns * 2 : 256;
         if (*reinterpret_cast<volatile int*>(&s.abort)) return false;
         if (globaltimer_ns() - t0 > kWaitNs) {
             *reinterpret_cast<volatile int*>(&s.abort) = 1;
