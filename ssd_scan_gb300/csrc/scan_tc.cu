@@ -16,17 +16,22 @@
 // memory, fp32 accumulators in TMEM):
 //   G1  CB[t,s] = C_t . B_s                 A = C  (TMA tile)   B = B (TMA)
 //   G3  Yo[t,p] = C_t . h[p,:]              A = C               B = bf16(h) rows [n][p]
-//   G4  dH[n,p] = sum_s B[s,n] w_s x[s,p]   A = B^T (MN-major)  B = (w x) rows [s][p]
-//   G2  Yd[t,p] = sum_s M[t,s] x[s,p]       A = M (masked, decayed CB, D on the diagonal)
-//                                           B = x rows [s][p]
+//   G4  dH[n,p] = sum_s B[s,n] xw[s,p]      A = B^T (MN-major)  B = xw rows [s][p]
+//   G2  Yd[t,p] = sum_s M[t,s] xv[s,p]      A = M (causal mask of CB)  B = xv rows [s][p]
+// Two forms of the decay, chosen per chunk:
+//   factored (a <= 0 and the chunk's total decay is moderate): with
+//     u_t = exp(gamma_t) and v_s = exp(-gamma_s) dt_s,
+//     M = mask(CB), xv = xw = v o x, y = u_t (Yd + Yo) + D x,
+//     h <- exp(gamma_Q) (h + dH);  the mask is a plain select and convert.
+//   exact (otherwise): M = mask(CB o exp(min(gamma_t - gamma_s, 0)) dt_s),
+//     xv = x, xw = w o x with w_s = exp(min(gamma_Q - gamma_s, 0)) dt_s,
+//     y = Yd + u_t Yo + D x,  h <- exp(gamma_Q) h + dH.
 //
 // The CTA is warp-specialised and software-pipelined over chunks:
 //   warps 0-3  "front": dt and the double-float cumulative sum of a, the x
-//              conv + SiLU (4 rows x 8 channels per task), then the causal
-//              mask M from CB (blocks above the diagonal are zero-filled
-//              without a TMEM read; when the chunk's total decay is moderate
-//              the decay factors into exp(gamma_t) exp(-gamma_s) dt_s,
-//              otherwise each entry takes its own clamped exponent).
+//              conv + SiLU (4 rows x 8 channels per task) into the x tiles,
+//              then the causal mask M from CB (blocks above the diagonal are
+//              zero-filled without a TMEM read).
 //   warps 4-7  "back": the state update h <- exp(gamma_Q) h + dH and the
 //              epilogue y = Yd + exp(gamma_t) Yo, times silu(z).
 //   warp 8     one thread issues every TMA load and every MMA as soon as its
@@ -77,14 +82,15 @@ struct __align__(16) ChunkVals {  // per-chunk row values, written by the front
     float wrow[Q];             // w_s = exp(min(gamma_Q - gamma_s, 0)) dt_s
     float dec[Q];              // exp(min(gamma_t, 0))
     float decS;                // exp(min(gamma_Q, 0))
+    int factored;              // which form of the decay this chunk uses
 };
 
 struct __align__(1024) TcSmem {
     __nv_bfloat16 C[2][Q * 64];     // C tile [t][n]: 2 panels of 64 n (TMA, SW128)
     __nv_bfloat16 B[2][Q * 64];     // B tile [s][n]
     __nv_bfloat16 Xr[2][Q * 64];    // x tiles [t][p] by chunk parity (raw rows with the conv)
-    __nv_bfloat16 XR[2][Q * 64];    // post-conv x rows [s][p] (SW128): G2's B, by parity
-    __nv_bfloat16 XW[Q * 64];       // (w o x) rows [s][p]: G4's B
+    __nv_bfloat16 XA[2][Q * 64];    // xv rows [s][p] (SW128): G2's B (and G4's when factored)
+    __nv_bfloat16 X2[2][Q * 64];    // factored: x rows (for D x); exact: xw rows (G4's B)
     __nv_bfloat16 M[2][Q * 64];     // masked decayed CB [t][s]: G2's A (K-major)
     __nv_bfloat16 Hs[N * 64];       // bf16 state rows [n][p]: G3's B
     ChunkVals cv[2];
@@ -103,11 +109,12 @@ constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;
 // operand tiles start on 1024-byte swizzle atoms; vector-accessed members on
 // their vector size
 static_assert(offsetof(TcSmem, C) % 1024 == 0 && offsetof(TcSmem, B) % 1024 == 0, "tile");
-static_assert(offsetof(TcSmem, Xr) % 1024 == 0 && offsetof(TcSmem, XR) % 1024 == 0, "tile");
-static_assert(offsetof(TcSmem, XW) % 1024 == 0 && offsetof(TcSmem, M) % 1024 == 0, "tile");
+static_assert(offsetof(TcSmem, Xr) % 1024 == 0 && offsetof(TcSmem, XA) % 1024 == 0, "tile");
+static_assert(offsetof(TcSmem, X2) % 1024 == 0 && offsetof(TcSmem, M) % 1024 == 0, "tile");
 static_assert(offsetof(TcSmem, Hs) % 1024 == 0, "tile");
 static_assert(sizeof(ChunkVals) % 16 == 0 && offsetof(TcSmem, cv) % 16 == 0, "float4 rows");
 static_assert(offsetof(ChunkVals, vfac) % 16 == 0 && offsetof(ChunkVals, wrow) % 16 == 0, "float4");
+static_assert(offsetof(ChunkVals, g2l) % 16 == 0 && offsetof(ChunkVals, dts) % 16 == 0, "float4");
 static_assert(offsetof(TcSmem, carry) % 16 == 0 && (P * 2) % 16 == 0, "uint4 carry rows");
 static_assert(offsetof(TcSmem, wconv) % 8 == 0 && offsetof(TcSmem, bconv) % 8 == 0, "float2");
 static_assert(offsetof(TcSmem, tma_bc) % 8 == 0, "mbarriers");
@@ -201,9 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     scan_tc_kernel(const __grid_constant__ CUtensorMap map_x,
                    const __grid_constant__ CUtensorMap map_bc, const TcScanParams p)
 {
-    extern __shared__ uint8_t smem_raw[];
-    TcSmem& s = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~uintptr_t(1023));
+    // Align to the 1024-byte swizzle atom with pointer arithmetic on the
+    // shared array itself, so the compiler keeps every access in the shared
+    // address space (LDS/STS rather than generic loads and stores).
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    TcSmem& s = *reinterpret_cast<TcSmem*>(smem_raw + ((1024u - (sm100::smem_u32(smem_raw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.x, b = blockIdx.y;
     const int H = p.H, G = p.G, W = p.W;
@@ -268,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&map_bc);
             const int xB = p.bc_col0 + g * N;          // first B column in the bc source
             const int xC = p.bc_col0 + G * N + g * N;  // first C column
-            const uint32_t aC = smem_u32(s.C), aB = smem_u32(s.B), aXW = smem_u32(s.XW);
+            const uint32_t aC = smem_u32(s.C), aB = smem_u32(s.B);
             const uint32_t aM = smem_u32(s.M), aH = smem_u32(s.Hs);
             auto load_bc = [&](int c) {
                 mbar_arrive_expect_tx(&s.tma_bc, 4 * Q * 64 * 2);
@@ -305,6 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok && c >= 2) ok = wait_or_abort(s, &s.epidone[buf], bpar ^ 1);
                 if (!ok) break;
                 tc_fence_after();
+                // the front wrote cv[buf] (and the form of the decay) before xready
+                const uint32_t aXW = smem_u32(s.cv[buf].factored ? s.XA[buf] : s.X2[buf]);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     mma_bf16_ss(tbase + kColDH + 64 * buf, sdesc_sw128(aB + k * 2048, Q * 128, 1024),
@@ -332,12 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = wait_or_abort(s, &s.mready, par);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t aXR = smem_u32(s.XR[buf]);
+                const uint32_t aXV = smem_u32(s.XA[buf]);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t offm = (k >> 2) * (Q * 128) + (k & 3) * 32;
                     mma_bf16_ss(tbase + kColYd + 64 * buf, sdesc_sw128(aM + offm, 16, 1024),
-                                sdesc_sw128(aXR + k * 2048, 8192, 1024), kIdY, k > 0);
+                                sdesc_sw128(aXV + k * 2048, 8192, 1024), kIdY, k > 0);
                 }
                 mma_commit(&s.g2[buf]);
             }
@@ -349,17 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp;          // TMEM lane quarter
         const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
         const int cj = tid & 7;            // conv: channel group (8 channels)
-        float2 wq[4][kMaxW], bq[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            bq[e] = p.conv ? s.bconv[4 * cj + e] : make_float2(0.f, 0.f);
-#pragma unroll
-            for (int k = 0; k < kMaxW; ++k)
-                wq[e][k] = p.conv ? s.wconv[4 * cj + e][k] : make_float2(0.f, 0.f);
-        }
         const float Ah = p.A[h];
         const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
-        const float Dh = p.D ? p.D[h] : 0.0f;
         constexpr float kLog2e = 1.4426950408889634f;
         float dt_next = t < p.S ? p.dt[((size_t)b * p.S + t) * H + h] : 0.0f;
         bool ok = true;
@@ -400,19 +402,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool factored = Ah <= 0.0f && gLh + gLl >= kFactorMinLog2;
             const float decay_t = ex2_fast(fminf(g2h_t + g2l_t, 0.0f));
             cv.dec[t] = decay_t;
-            cv.wrow[t] = t < rows ? ex2_fast(fminf((gLh - g2h_t) + (gLl - g2l_t), 0.0f)) * dt : 0.0f;
             if (factored) cv.vfac[t] = ex2_fast(-(g2h_t + g2l_t)) * dt;
-            if (t == 0) cv.decS = ex2_fast(fminf(gLh + gLl, 0.0f));
+            else cv.wrow[t] = t < rows ? ex2_fast(fminf((gLh - g2h_t) + (gLl - g2l_t), 0.0f)) * dt : 0.0f;
+            if (t == 0) {
+                cv.decS = ex2_fast(fminf(gLh + gLl, 0.0f));
+                cv.factored = factored;
+            }
             mbar_arrive(&s.cvready[buf]);  // cv[buf] of chunk c is complete
-            // XW is free once G4(c-1) is done; XR[buf] once G2(c-2) is done
-            if (ok && c >= 1) ok = wait_or_abort(s, &s.g4[buf ^ 1], ((c - 1) >> 1) & 1);
-            if (ok && c >= 2) ok = wait_or_abort(s, &s.g2[buf], bpar ^ 1);
+            // XA[buf], X2[buf] are free: the back finished chunk c-2 (waited above),
+            // after G2(c-2) and G4(c-2) had read them
             if (ok) ok = wait_or_abort(s, &s.tma_x[buf], bpar);
             // wrow visible; carry of the last chunk written; a common decision
             ok = !named_bar_or(kBarFront, kFrontThreads, !ok);
             if (!ok) break;
 
-            // ---- x: conv + SiLU, 2 tasks of 4 rows x 8 channels -> x, w x rows ----
+            // ---- x: conv + SiLU, 2 tasks of 4 rows x 8 channels -> x tiles ----
+            // factored: XA = v o x, X2 = x;  exact: XA = x, X2 = w o x
 #pragma unroll 1
             for (int task = 0; task < 2; ++task) {
                 const int t0 = 4 * ((tid >> 3) + 16 * task);
@@ -429,14 +434,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<uint4*>(&s.carry[buf ^ 1][r - (Q - 3)][8 * cj]) = raw;
                     }
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const bool valid = t0 + i < rows;
+                    for (int e = 0; e < 4; ++e) {  // channel pair: taps from shared memory
+                        const float2 bq = s.bconv[4 * cj + e];
+                        float2 wq[kMaxW];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float2 v = bq[e];
+                        for (int k = 0; k < kMaxW; ++k) wq[k] = s.wconv[4 * cj + e][k];
 #pragma unroll
-                            for (int k = 0; k < kMaxW; ++k) v = __ffma2_rn(wq[e][k], win[i + k][e], v);
-                            xo[i][e] = valid ? silu2(v) : make_float2(0.f, 0.f);
+                        for (int i = 0; i < 4; ++i) {
+                            float2 v = bq;
+#pragma unroll
+                            for (int k = 0; k < kMaxW; ++k) v = __ffma2_rn(wq[k], win[i + k][e], v);
+                            xo[i][e] = t0 + i < rows ? silu2(v) : make_float2(0.f, 0.f);
                         }
                     }
                 } else {
@@ -444,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 4; ++i)
                         unpack4x2(at<const uint4>(s.Xr[buf], chunk_off(t0 + i, cj)), xo[i]);
                 }
-                const float4 w4 = *reinterpret_cast<const float4*>(&cv.wrow[t0]);
+                const float4 w4 = *reinterpret_cast<const float4*>(factored ? &cv.vfac[t0] : &cv.wrow[t0]);
                 const float wr[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -452,14 +460,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) xw[e] = __fmul2_rn(make_float2(wr[i], wr[i]), xo[i][e]);
                     const uint32_t off = chunk_off(t0 + i, cj);
-                    at<uint4>(s.XR[buf], off) = pack4x2(xo[i]);
-                    at<uint4>(s.XW, off) = pack4x2(xw);
+                    const uint4 px = pack4x2(xo[i]), pw = pack4x2(xw);
+                    at<uint4>(s.XA[buf], off) = factored ? pw : px;
+                    at<uint4>(s.X2[buf], off) = factored ? px : pw;
                 }
             }
             fence_proxy_async_smem();
             mbar_arrive(&s.xready);
 
-            // ---- causal mask with decays, D on the diagonal ----
+            // ---- causal mask (with the decays in the exact form) ----
             // M is free once G2(c-1) is done; CB(c) is ready once G1(c) is done
             if (c >= 1) ok = wait_or_abort(s, &s.g2[buf ^ 1], ((c - 1) >> 1) & 1);
             if (ok) ok = wait_or_abort(s, &s.g1, par);
@@ -474,41 +483,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                         at<uint4>(mpanel, chunk_off(t, (cc & 1) * 4 + q4)) = make_uint4(0, 0, 0, 0);
                     continue;
                 }
-                float v[32];
-                tmem_ld32(tbase + kColCB + lane_off + cc * 32, v);
-                tmem_ld_wait();
-                const bool diag = cc == quarter;
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {  // 16 columns at a time
+                    const int c0 = cc * 32 + 16 * hh;
+                    float v[16];
+                    tmem_ld16(tbase + kColCB + lane_off + c0, v);
+                    tmem_ld_wait();
+                    if (!factored) {
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int sb = cc * 32 + q4 * 8;
-                    float2 m[4];
-                    if (factored) {
-                        const float4 f0 = *reinterpret_cast<const float4*>(&cv.vfac[sb]);
-                        const float4 f1 = *reinterpret_cast<const float4*>(&cv.vfac[sb + 4]);
-                        const float2 uu = make_float2(decay_t, decay_t);
-                        m[0] = __fmul2_rn(__fmul2_rn(make_float2(v[q4 * 8 + 0], v[q4 * 8 + 1]), make_float2(f0.x, f0.y)), uu);
-                        m[1] = __fmul2_rn(__fmul2_rn(make_float2(v[q4 * 8 + 2], v[q4 * 8 + 3]), make_float2(f0.z, f0.w)), uu);
-                        m[2] = __fmul2_rn(__fmul2_rn(make_float2(v[q4 * 8 + 4], v[q4 * 8 + 5]), make_float2(f1.x, f1.y)), uu);
-                        m[3] = __fmul2_rn(__fmul2_rn(make_float2(v[q4 * 8 + 6], v[q4 * 8 + 7]), make_float2(f1.z, f1.w)), uu);
-                    } else {
-                        float mm[8];
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const int sb = c0 + 4 * q4;
+                            const float4 gh = *reinterpret_cast<const float4*>(&cv.g2h[sb]);
+                            const float4 gl = *reinterpret_cast<const float4*>(&cv.g2l[sb]);
+                            const float4 ds = *reinterpret_cast<const float4*>(&cv.dts[sb]);
+                            const float ghs[4] = {gh.x, gh.y, gh.z, gh.w}, gls[4] = {gl.x, gl.y, gl.z, gl.w};
+                            const float dss[4] = {ds.x, ds.y, ds.z, ds.w};
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float ex = (g2h_t - cv.g2h[sb + e]) + (g2l_t - cv.g2l[sb + e]);
-                            mm[e] = v[q4 * 8 + e] * cv.dts[sb + e] * ex2_fast(fminf(ex, 0.0f));
-                        }
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) m[e] = make_float2(mm[2 * e], mm[2 * e + 1]);
-                    }
-                    if (diag) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int s0 = sb + 2 * e;
-                            m[e].x = s0 < t ? m[e].x : (s0 == t ? m[e].x + Dh : 0.0f);
-                            m[e].y = s0 + 1 < t ? m[e].y : (s0 + 1 == t ? m[e].y + Dh : 0.0f);
+                            for (int e = 0; e < 4; ++e) {
+                                const float ex = (g2h_t - ghs[e]) + (g2l_t - gls[e]);
+                                v[4 * q4 + e] = v[4 * q4 + e] * dss[e] * ex2_fast(fminf(ex, 0.0f));
+                            }
                         }
                     }
-                    at<uint4>(mpanel, chunk_off(t, (cc & 1) * 4 + q4)) = pack4x2(m);
+                    if (cc == quarter) {  // the diagonal block: keep s <= t
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[e] = (c0 + e <= t) ? v[e] : 0.0f;
+                    }
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        const float2 m[4] = {make_float2(v[8 * q2 + 0], v[8 * q2 + 1]),
+                                             make_float2(v[8 * q2 + 2], v[8 * q2 + 3]),
+                                             make_float2(v[8 * q2 + 4], v[8 * q2 + 5]),
+                                             make_float2(v[8 * q2 + 6], v[8 * q2 + 7])};
+                        at<uint4>(mpanel, chunk_off(t, (cc & 1) * 4 + 2 * hh + q2)) = pack4x2(m);
+                    }
                 }
             }
             fence_proxy_async_smem();
@@ -536,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(&s.hsready);
         const __nv_bfloat16* zbase = static_cast<const __nv_bfloat16*>(p.z);
+        const float Dh = p.D ? p.D[h] : 0.0f;
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             const uint32_t bpar = (c >> 1) & 1;
@@ -543,13 +552,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r0 = c * Q;
             const int rows = min(Q, p.S - r0);
             const ChunkVals& cv = s.cv[buf];
-            // z of this row, early (used at the end)
+            // z of this row: the first half early, the second half before the epilogue
+            const uint4* zr = reinterpret_cast<const uint4*>(
+                zbase + ((size_t)b * p.S + r0 + min(t, rows - 1)) * (H * P) + h * P);
             uint4 zq[8];
-            if (has_z && t < rows) {
-                const uint4* zr = reinterpret_cast<const uint4*>(
-                    zbase + ((size_t)b * p.S + r0 + t) * (H * P) + h * P);
+            if (has_z) {
 #pragma unroll
-                for (int q8 = 0; q8 < 8; ++q8) zq[q8] = __ldg(zr + q8);
+                for (int q8 = 0; q8 < 2; ++q8) zq[q8] = __ldg(zr + q8);
             }
             // ---- state ----
             ok = wait_or_abort(s, &s.cvready[buf], bpar);     // cv of chunk c written
@@ -558,7 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);  // warp-uniform: tcgen05.ld is .sync.aligned
             if (!ok) break;
             tc_fence_after();
+            // h <- decS h + b dH, b = decS (factored: dH carries exp(-gamma_s)) or 1
+            const bool factored = cv.factored != 0;
             const float2 dS = make_float2(cv.decS, cv.decS);
+            const float2 bS = factored ? dS : make_float2(1.0f, 1.0f);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 float v[32];
@@ -566,8 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    hreg[16 * half + i] =
-                        __ffma2_rn(dS, hreg[16 * half + i], make_float2(v[2 * i], v[2 * i + 1]));
+                    hreg[16 * half + i] = __ffma2_rn(dS, hreg[16 * half + i],
+                                                     __fmul2_rn(bS, make_float2(v[2 * i], v[2 * i + 1])));
             }
             store_h();
             fence_proxy_async_smem();
@@ -577,9 +589,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_or_abort(s, &s.g2[buf], bpar);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
+            if (has_z) {
+#pragma unroll
+                for (int q8 = 2; q8 < 8; ++q8) zq[q8] = __ldg(zr + q8);
+            }
             tc_fence_after();
+            // y = a Yd + u Yo + D x, a = u (factored) or 1; x from the tile holding x
             const float dec = cv.dec[t];
             const float2 dd = make_float2(dec, dec);
+            const float2 aa = factored ? dd : make_float2(1.0f, 1.0f);
+            const float2 D2 = make_float2(Dh, Dh);
+            const __nv_bfloat16* xt = factored ? s.X2[buf] : s.XA[buf];
             uint4* yrow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) +
                                                    (((size_t)b * p.S + r0 + t) * H + h) * P);
 #pragma unroll
@@ -590,13 +610,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
 #pragma unroll
                 for (int j2 = 0; j2 < 2; ++j2) {
-                    float2 out[4], zv[4];
+                    float2 out[4], zv[4], xv[4];
                     if (has_z) unpack4x2(zq[2 * q4 + j2], zv);
+                    unpack4x2(at<const uint4>(const_cast<__nv_bfloat16*>(xt), chunk_off(t, 2 * q4 + j2)), xv);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int k = j2 * 8 + 2 * e;
                         float2 yv = __ffma2_rn(dd, make_float2(yo[k], yo[k + 1]),
-                                               make_float2(yd[k], yd[k + 1]));
+                                               __fmul2_rn(aa, make_float2(yd[k], yd[k + 1])));
+                        yv = __ffma2_rn(D2, xv[e], yv);
                         if (has_z) yv = __fmul2_rn(yv, silu2(zv[e]));
                         out[e] = yv;
                     }
