@@ -57,7 +57,13 @@ constexpr int Q = 128;  // rows per chunk
 constexpr int P = 64;   // head dim
 constexpr int N = 128;  // state dim
 constexpr int kFrontThreads = 128, kBackThreads = 128;
-constexpr int kThreads = kFrontThreads + kBackThreads + 32;  // + the issuing warp
+// three warpgroups: front, back, and the issuer (one thread of it works)
+constexpr int kThreads = kFrontThreads + kBackThreads + 128;
+// Registers: launched at kLaunchRegs per thread (384 x 168 = 64,512, the
+// whole pool); the issuing warpgroup gives back down to kIssuerRegs and the
+// front and back warpgroups take kWorkRegs each: 2*200 + 104 = 3*168.
+constexpr uint32_t kLaunchRegs = 168, kWorkRegs = 200, kIssuerRegs = 104;
+static_assert(2 * kWorkRegs + kIssuerRegs == 3 * kLaunchRegs, "register split");
 constexpr int kMaxW = 4;  // conv taps handled in the kernel (W-1 carried rows)
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound on any single wait: 2 s
 constexpr uint32_t kBarFront = 1;             // named barrier of the front warps
@@ -269,10 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tbase = s.tmem_base;
     const size_t sbase = ((size_t)b * H + h) * P * N;
-
     if (role == 2) {
         // ===================== issuer: TMA + MMA (one thread) =====================
-        if (lane == 0 && nchunks > 0) {
+        regs_dec<kIssuerRegs>();
+        if (warp == 8 && lane == 0 && nchunks > 0) {
             prefetch_tmap(&map_x);
             prefetch_tmap(&map_bc);
             const int xB = p.bc_col0 + g * N;          // first B column in the bc source
@@ -356,10 +362,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (role == 0) {
         // ===================== front: gamma, conv, mask =====================
+        regs_inc<kWorkRegs>();
         const int t = tid;                 // chunk row of this thread
         const int quarter = warp;          // TMEM lane quarter
         const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
         const int cj = tid & 7;            // conv: channel group (8 channels)
+        float2 wq[4][kMaxW], bq[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            bq[e] = p.conv ? s.bconv[4 * cj + e] : make_float2(0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kMaxW; ++k)
+                wq[e][k] = p.conv ? s.wconv[4 * cj + e][k] : make_float2(0.f, 0.f);
+        }
         const float Ah = p.A[h];
         const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
         constexpr float kLog2e = 1.4426950408889634f;
@@ -434,16 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<uint4*>(&s.carry[buf ^ 1][r - (Q - 3)][8 * cj]) = raw;
                     }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {  // channel pair: taps from shared memory
-                        const float2 bq = s.bconv[4 * cj + e];
-                        float2 wq[kMaxW];
+                    for (int i = 0; i < 4; ++i) {
 #pragma unroll
-                        for (int k = 0; k < kMaxW; ++k) wq[k] = s.wconv[4 * cj + e][k];
+                        for (int e = 0; e < 4; ++e) {
+                            float2 v = bq[e];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            float2 v = bq;
-#pragma unroll
-                            for (int k = 0; k < kMaxW; ++k) v = __ffma2_rn(wq[k], win[i + k][e], v);
+                            for (int k = 0; k < kMaxW; ++k) v = __ffma2_rn(wq[e][k], win[i + k][e], v);
                             xo[i][e] = t0 + i < rows ? silu2(v) : make_float2(0.f, 0.f);
                         }
                     }
@@ -526,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) *reinterpret_cast<volatile int*>(&s.abort) = 1;
     } else {
         // ===================== back: state update, epilogue =====================
+        regs_inc<kWorkRegs>();
         const int t = tid - kFrontThreads;  // chunk row / state column of this thread
         const int n = t;
         const int quarter = warp - 4;
@@ -558,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4 zq[8];
             if (has_z) {
 #pragma unroll
-                for (int q8 = 0; q8 < 2; ++q8) zq[q8] = __ldg(zr + q8);
+                for (int q8 = 0; q8 < 8; ++q8) zq[q8] = __ldg(zr + q8);
             }
             // ---- state ----
             ok = wait_or_abort(s, &s.cvready[buf], bpar);     // cv of chunk c written
@@ -589,10 +601,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_or_abort(s, &s.g2[buf], bpar);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
-            if (has_z) {
-#pragma unroll
-                for (int q8 = 2; q8 < 8; ++q8) zq[q8] = __ldg(zr + q8);
-            }
             tc_fence_after();
             // y = a Yd + u Yo + D x, a = u (factored) or 1; x from the tile holding x
             const float dec = cv.dec[t];
@@ -691,9 +699,15 @@ cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st)
     CUtensorMap mx, mbc;
     if (!make_map(&mx, p.xbc, Cdim, p.S, p.B)) return cudaErrorInvalidValue;
     if (!make_map(&mbc, p.bc, p.bc_stride, p.S, p.B)) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    // The warpgroups' register split assumes the kernel was compiled to
+    // exactly kLaunchRegs per thread; anything else is refused (a split that
+    // does not add up would leave setmaxnreg waiting).
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, scan_tc_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != (int)kLaunchRegs) return cudaErrorNotSupported;
+    e = cudaFuncSetAttribute(scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(p.H, p.B);
     scan_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mx, mbc, p);

@@ -108,6 +108,16 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool p
     return r != 0;
 }
 
+// Move registers between warpgroups (all warps of a warpgroup execute it).
+template <uint32_t kRegs> __device__ __forceinline__ void regs_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs> __device__ __forceinline__ void regs_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ---- TMA -----------------------------------------------------------------
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int x, int y, int z)
