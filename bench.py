@@ -236,6 +236,9 @@ def bench_ours(args):
     ssd.load_library()
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
+    if args.only == "decode":
+        dec = bench_decode(ssd, dev, stream, world, args)
+        return {"metric": "decode-step state GB/s", "decode": dec} if rank == 0 else None
     shape = si.PREFILL
     pb = prefill_bytes(shape)
     set_bytes = pb["per_launch"]
@@ -335,7 +338,7 @@ def bench_e2e(ssd, shape, d, flags, prm, dset, stream, args):
 
 def bench_decode(ssd, dev, stream, world, args):
     shape = si.DECODE
-    R, nslots = si.DECODE_ROWS, si.DECODE_SLOTS
+    R, nslots = si.DECODE_ROWS, max(si.DECODE_ROWS, args.decode_slots)
     prm = {k: v.to(dev) for k, v in si.params(shape).items()}
     pools = {k: v.to(dev) for k, v in si.decode_pools(shape, nslots, device=dev).items()}
     nin = 8
@@ -449,8 +452,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill"], default="all",
-                    help="prefill: time the prefill steps only (for profiler runs)")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="time only the prefill or only the decode steps (profiler runs)")
+    ap.add_argument("--decode-slots", type=int, default=si.DECODE_SLOTS,
+                    help="slots in the decode pool (the 256 rows touch the same bytes "
+                         "whatever the pool size; a smaller pool keeps profiler captures small)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
