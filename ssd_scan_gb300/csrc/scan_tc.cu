@@ -27,18 +27,21 @@
 //     xv = x, xw = w o x with w_s = exp(min(gamma_Q - gamma_s, 0)) dt_s,
 //     y = Yd + u_t Yo + D x,  h <- exp(gamma_Q) h + dH.
 //
-// The CTA is warp-specialised and software-pipelined over chunks:
-//   warps 0-3  "front": dt and the double-float cumulative sum of a, the x
-//              conv + SiLU (4 rows x 8 channels per task) into the x tiles,
-//              then the causal mask M from CB (blocks above the diagonal are
-//              zero-filled without a TMEM read).
-//   warps 4-7  "back": the state update h <- exp(gamma_Q) h + dH and the
-//              epilogue y = Yd + exp(gamma_t) Yo, times silu(z).
-//   warp 8     one thread issues every TMA load and every MMA as soon as its
-//              operands are ready.
-// The front works on chunk c+1 while the back finishes chunk c; the
-// accumulators the back reads (Yd, Yo, dH) are double-buffered in TMEM, and
-// mbarriers carry every hand-off.  Every wait is bounded in time; a wait
+// The CTA is warp-specialised and software-pipelined over chunks, four
+// warpgroups of 128 threads:
+//   conv   x conv + SiLU of the raw TMA tile (4 rows x 8 channels per task)
+//          into the x rows tile XR;
+//   front  dt and the double-float cumulative sum of a; the scaled x tile XS
+//          (v o x or w o x); the causal mask M from CB (blocks above the
+//          diagonal are zero-filled without a TMEM read);
+//   back   the state update and the epilogue y = a Yd + u Yo + D x, times
+//          silu(z);
+//   issuer one thread issues every TMA load and every MMA as soon as its
+//          operands are ready.
+// The conv and front run ahead on chunk c+1 while the back finishes chunk c;
+// the accumulators the back reads (Yd, Yo, dH) are double-buffered in TMEM,
+// and mbarriers carry every hand-off.  setmaxnreg moves registers from the
+// issuing warpgroup to the others.  Every wait is bounded in time; a wait
 // that runs out aborts the CTA and sets the device error word.
 #include "internal.cuh"
 #include "sm100.cuh"
@@ -56,17 +59,18 @@ using namespace sm100;
 constexpr int Q = 128;  // rows per chunk
 constexpr int P = 64;   // head dim
 constexpr int N = 128;  // state dim
-constexpr int kFrontThreads = 128, kBackThreads = 128;
-// three warpgroups: front, back, and the issuer (one thread of it works)
-constexpr int kThreads = kFrontThreads + kBackThreads + 128;
-// Registers: launched at kLaunchRegs per thread (384 x 168 = 64,512, the
-// whole pool); the issuing warpgroup gives back down to kIssuerRegs and the
-// front and back warpgroups take kWorkRegs each: 2*200 + 104 = 3*168.
-constexpr uint32_t kLaunchRegs = 168, kWorkRegs = 200, kIssuerRegs = 104;
-static_assert(2 * kWorkRegs + kIssuerRegs == 3 * kLaunchRegs, "register split");
+constexpr int kWG = 128;                 // threads per warpgroup
+constexpr int kThreads = 4 * kWG;        // conv, front, back, issuer
+// Registers: launched at kLaunchRegs per thread (512 x 128 = 65,536, the
+// whole pool); setmaxnreg then gives each warpgroup its share, adding up to
+// the pool: 136 + 112 + 192 + 72 = 4 x 128.
+constexpr uint32_t kLaunchRegs = 128;
+constexpr uint32_t kConvRegs = 136, kFrontRegs = 112, kBackRegs = 192, kIssuerRegs = 72;
+static_assert(kConvRegs + kFrontRegs + kBackRegs + kIssuerRegs == 4 * kLaunchRegs,
+              "register split");
 constexpr int kMaxW = 4;  // conv taps handled in the kernel (W-1 carried rows)
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound on any single wait: 2 s
-constexpr uint32_t kBarFront = 1;             // named barrier of the front warps
+constexpr uint32_t kBarConv = 1, kBarFront = 2;  // named barriers of two warpgroups
 
 // G1: A, B K-major.  G2, G3: A K-major, B MN-major (row tiles [k][p]).
 // G4: A = B^T read MN-major from the B tile, B MN-major.
@@ -94,18 +98,18 @@ struct __align__(16) ChunkVals {  // per-chunk row values, written by the front
 struct __align__(1024) TcSmem {
     __nv_bfloat16 C[2][Q * 64];     // C tile [t][n]: 2 panels of 64 n (TMA, SW128)
     __nv_bfloat16 B[2][Q * 64];     // B tile [s][n]
-    __nv_bfloat16 Xr[2][Q * 64];    // x tiles [t][p] by chunk parity (raw rows with the conv)
-    __nv_bfloat16 XA[2][Q * 64];    // xv rows [s][p] (SW128): G2's B (and G4's when factored)
-    __nv_bfloat16 X2[2][Q * 64];    // factored: x rows (for D x); exact: xw rows (G4's B)
-    __nv_bfloat16 M[2][Q * 64];     // masked decayed CB [t][s]: G2's A (K-major)
+    __nv_bfloat16 Xr[2][Q * 64];    // raw (or post-conv) x tiles [t][p] by chunk parity
+    __nv_bfloat16 XR[2][Q * 64];    // post-conv x rows [s][p] (SW128), by parity
+    __nv_bfloat16 XS[2][Q * 64];    // scaled x rows: v o x (factored) or w o x (exact)
+    __nv_bfloat16 M[2][Q * 64];     // masked CB [t][s]: G2's A (K-major)
     __nv_bfloat16 Hs[N * 64];       // bf16 state rows [n][p]: G3's B
     ChunkVals cv[2];
     alignas(16) __nv_bfloat16 carry[2][kMaxW - 1][P];  // raw x rows before the chunk, by parity
-    alignas(16) float2 wconv[P / 2][kMaxW];     // taps of channel pairs (front-padded with zeros)
+    alignas(16) float2 wconv[P / 2][kMaxW];  // taps of channel pairs (front-padded with zeros)
     float2 bconv[P / 2];
     float wsum_hi[4], wsum_lo[4];
     uint64_t tma_bc, tma_x[2], g1, g2[2], g3[2], g4[2];
-    uint64_t xready, mready, hsready, epidone[2], cvready[2];
+    uint64_t xconv[2], xready[2], cvready[2], mready, hsready, epidone[2];
     uint32_t tmem_base;
     int abort;
 };
@@ -115,8 +119,8 @@ constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;
 // operand tiles start on 1024-byte swizzle atoms; vector-accessed members on
 // their vector size
 static_assert(offsetof(TcSmem, C) % 1024 == 0 && offsetof(TcSmem, B) % 1024 == 0, "tile");
-static_assert(offsetof(TcSmem, Xr) % 1024 == 0 && offsetof(TcSmem, XA) % 1024 == 0, "tile");
-static_assert(offsetof(TcSmem, X2) % 1024 == 0 && offsetof(TcSmem, M) % 1024 == 0, "tile");
+static_assert(offsetof(TcSmem, Xr) % 1024 == 0 && offsetof(TcSmem, XR) % 1024 == 0, "tile");
+static_assert(offsetof(TcSmem, XS) % 1024 == 0 && offsetof(TcSmem, M) % 1024 == 0, "tile");
 static_assert(offsetof(TcSmem, Hs) % 1024 == 0, "tile");
 static_assert(sizeof(ChunkVals) % 16 == 0 && offsetof(TcSmem, cv) % 16 == 0, "float4 rows");
 static_assert(offsetof(ChunkVals, vfac) % 16 == 0 && offsetof(ChunkVals, wrow) % 16 == 0, "float4");
@@ -220,6 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     TcSmem& s = *reinterpret_cast<TcSmem*>(smem_raw + ((1024u - (sm100::smem_u32(smem_raw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wg = warp >> 2;             // 0 conv, 1 front, 2 back, 3 issuer
+    const int quarter = warp & 3;         // TMEM lane quarter of this warp
     const int h = blockIdx.x, b = blockIdx.y;
     const int H = p.H, G = p.G, W = p.W;
     const int g = h / (H / G);
@@ -227,7 +233,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nchunks = (p.S + Q - 1) / Q;
     const bool has_z = (p.flags & kHasZ) != 0;
     const bool softplus = (p.flags & kDtSoftplus) != 0;
-    const int role = warp < 4 ? 0 : (warp < 8 ? 1 : 2);  // front, back, issuer
 
     if (tid == 0) {
         mbar_init(&s.tma_bc, 1);
@@ -237,12 +242,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&s.g2[i], 1);
             mbar_init(&s.g3[i], 1);
             mbar_init(&s.g4[i], 1);
-            mbar_init(&s.epidone[i], kBackThreads);
-            mbar_init(&s.cvready[i], kFrontThreads);
+            mbar_init(&s.xconv[i], kWG);
+            mbar_init(&s.xready[i], kWG);
+            mbar_init(&s.cvready[i], kWG);
+            mbar_init(&s.epidone[i], kWG);
         }
-        mbar_init(&s.xready, kFrontThreads);
-        mbar_init(&s.mready, kFrontThreads);
-        mbar_init(&s.hsready, kBackThreads);
+        mbar_init(&s.mready, kWG);
+        mbar_init(&s.hsready, kWG);
         s.abort = 0;
         fence_mbar_init();
     }
@@ -274,11 +280,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = s.tmem_base;
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
     const size_t sbase = ((size_t)b * H + h) * P * N;
-    if (role == 2) {
+
+    if (wg == 3) {
         // ===================== issuer: TMA + MMA (one thread) =====================
         regs_dec<kIssuerRegs>();
-        if (warp == 8 && lane == 0 && nchunks > 0) {
+        if (warp == 12 && lane == 0 && nchunks > 0) {
             prefetch_tmap(&map_x);
             prefetch_tmap(&map_bc);
             const int xB = p.bc_col0 + g * N;          // first B column in the bc source
@@ -315,19 +323,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 sdesc_sw128(aB + off, 16, 1024), kIdCB, k > 0);
                 }
                 mma_commit(&s.g1);
-                // G4(c): x rows written; dH[buf] free (the back finished chunk c-2)
-                ok = wait_or_abort(s, &s.xready, par);
+                // G4(c): scaled x written; dH[buf] free (the back finished chunk c-2)
+                ok = wait_or_abort(s, &s.xready[buf], bpar);
                 if (ok && c >= 2) ok = wait_or_abort(s, &s.epidone[buf], bpar ^ 1);
                 if (!ok) break;
                 tc_fence_after();
-                // the front wrote cv[buf] (and the form of the decay) before xready
-                const uint32_t aXW = smem_u32(s.cv[buf].factored ? s.XA[buf] : s.X2[buf]);
+                const uint32_t aXS = smem_u32(s.XS[buf]);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     mma_bf16_ss(tbase + kColDH + 64 * buf, sdesc_sw128(aB + k * 2048, Q * 128, 1024),
-                                sdesc_sw128(aXW + k * 2048, 8192, 1024), kIdState, k > 0);
+                                sdesc_sw128(aXS + k * 2048, 8192, 1024), kIdState, k > 0);
                 mma_commit(&s.g4[buf]);
-                if (c + 2 < nchunks) load_x(c + 2);  // the front has read Xr[buf]
+                // raw x of chunk c+2 into Xr[buf] once the conv has read it
+                if (c + 2 < nchunks) {
+                    ok = wait_or_abort(s, &s.xconv[buf], bpar);
+                    if (!ok) break;
+                    load_x(c + 2);
+                }
                 // G3(c): the back wrote bf16 h of chunk c-1
                 ok = wait_or_abort(s, &s.hsready, par);
                 if (!ok) break;
@@ -345,11 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     load_bc(c + 1);
                 }
-                // G2(c): the front wrote M(c)
+                // G2(c): the front wrote M(c); x is XS (factored) or XR (exact)
                 ok = wait_or_abort(s, &s.mready, par);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t aXV = smem_u32(s.XA[buf]);
+                const uint32_t aXV = smem_u32(s.cv[buf].factored ? s.XS[buf] : s.XR[buf]);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t offm = (k >> 2) * (Q * 128) + (k & 3) * 32;
@@ -360,13 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) *reinterpret_cast<volatile int*>(&s.abort) = 1;
         }
-    } else if (role == 0) {
-        // ===================== front: gamma, conv, mask =====================
-        regs_inc<kWorkRegs>();
-        const int t = tid;                 // chunk row of this thread
-        const int quarter = warp;          // TMEM lane quarter
-        const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-        const int cj = tid & 7;            // conv: channel group (8 channels)
+    } else if (wg == 0) {
+        // ===================== conv: x rows of each chunk =====================
+        regs_inc<kConvRegs>();
+        const int cj = tid & 7;  // channel group (8 channels)
         float2 wq[4][kMaxW], bq[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -375,64 +384,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < kMaxW; ++k)
                 wq[e][k] = p.conv ? s.wconv[4 * cj + e][k] : make_float2(0.f, 0.f);
         }
-        const float Ah = p.A[h];
-        const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
-        constexpr float kLog2e = 1.4426950408889634f;
-        float dt_next = t < p.S ? p.dt[((size_t)b * p.S + t) * H + h] : 0.0f;
         bool ok = true;
-        for (int c = 0; c < nchunks && ok; ++c) {
-            const uint32_t par = c & 1, bpar = (c >> 1) & 1;
+        for (int c = 0; c < nchunks; ++c) {
+            const uint32_t bpar = (c >> 1) & 1;
             const int buf = c & 1;
-            const int r0 = c * Q;
-            const int rows = min(Q, p.S - r0);
-            ChunkVals& cv = s.cv[buf];
-            // ---- dt and the cumulative sum of a = dt A (double-float) ----
-            float dt = 0.0f;
-            if (t < rows) dt = softplus ? softplus_f32(dt_next + bias) : dt_next;
-            if (c + 1 < nchunks)
-                dt_next = r0 + Q + t < p.S ? p.dt[((size_t)b * p.S + r0 + Q + t) * H + h] : 0.0f;
-            float ghi = dt * Ah, glo = 0.0f;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const float ohi = __shfl_up_sync(0xffffffffu, ghi, d);
-                const float olo = __shfl_up_sync(0xffffffffu, glo, d);
-                if (lane >= d) df_add(ghi, glo, ohi, olo);
-            }
-            if (lane == 31) {
-                s.wsum_hi[quarter] = ghi;
-                s.wsum_lo[quarter] = glo;
-            }
-            // the back has finished chunk c-2, which used cv[buf]
+            const int rows = min(Q, p.S - c * Q);
+            // XR[buf] is free once the back finished chunk c-2
             if (c >= 2) ok = ok && wait_or_abort(s, &s.epidone[buf], bpar ^ 1);
-            // the front decides together (a wait that failed anywhere stops all)
-            ok = !named_bar_or(kBarFront, kFrontThreads, !ok);
-            if (!ok) break;
-            for (int w2 = 0; w2 < quarter; ++w2) df_add(ghi, glo, s.wsum_hi[w2], s.wsum_lo[w2]);
-            const float g2h_t = ghi * kLog2e, g2l_t = glo * kLog2e;
-            cv.g2h[t] = g2h_t;
-            cv.g2l[t] = g2l_t;
-            cv.dts[t] = dt;
-            named_bar_sync(kBarFront, kFrontThreads);
-            const float gLh = cv.g2h[rows - 1], gLl = cv.g2l[rows - 1];
-            const bool factored = Ah <= 0.0f && gLh + gLl >= kFactorMinLog2;
-            const float decay_t = ex2_fast(fminf(g2h_t + g2l_t, 0.0f));
-            cv.dec[t] = decay_t;
-            if (factored) cv.vfac[t] = ex2_fast(-(g2h_t + g2l_t)) * dt;
-            else cv.wrow[t] = t < rows ? ex2_fast(fminf((gLh - g2h_t) + (gLl - g2l_t), 0.0f)) * dt : 0.0f;
-            if (t == 0) {
-                cv.decS = ex2_fast(fminf(gLh + gLl, 0.0f));
-                cv.factored = factored;
-            }
-            mbar_arrive(&s.cvready[buf]);  // cv[buf] of chunk c is complete
-            // XA[buf], X2[buf] are free: the back finished chunk c-2 (waited above),
-            // after G2(c-2) and G4(c-2) had read them
             if (ok) ok = wait_or_abort(s, &s.tma_x[buf], bpar);
-            // wrow visible; carry of the last chunk written; a common decision
-            ok = !named_bar_or(kBarFront, kFrontThreads, !ok);
+            // together: the carry rows of chunk c-1 are written; a common decision
+            ok = !named_bar_or(kBarConv, kWG, !ok);
             if (!ok) break;
-
-            // ---- x: conv + SiLU, 2 tasks of 4 rows x 8 channels -> x tiles ----
-            // factored: XA = v o x, X2 = x;  exact: XA = x, X2 = w o x
 #pragma unroll 1
             for (int task = 0; task < 2; ++task) {
                 const int t0 = 4 * ((tid >> 3) + 16 * task);
@@ -463,25 +425,82 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 4; ++i)
                         unpack4x2(at<const uint4>(s.Xr[buf], chunk_off(t0 + i, cj)), xo[i]);
                 }
-                const float4 w4 = *reinterpret_cast<const float4*>(factored ? &cv.vfac[t0] : &cv.wrow[t0]);
-                const float wr[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float2 xw[4];
+                for (int i = 0; i < 4; ++i)
+                    at<uint4>(s.XR[buf], chunk_off(t0 + i, cj)) = pack4x2(xo[i]);
+            }
+            fence_proxy_async_smem();  // XR is read by G2 in the exact form
+            mbar_arrive(&s.xconv[buf]);
+        }
+        if (!ok) *reinterpret_cast<volatile int*>(&s.abort) = 1;
+    } else if (wg == 1) {
+        // ===================== front: gamma, scaled x, mask =====================
+        regs_inc<kFrontRegs>();
+        const int t = tid - kWG;  // chunk row of this thread
+        const float Ah = p.A[h];
+        const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
+        constexpr float kLog2e = 1.4426950408889634f;
+        float dt_next = t < p.S ? p.dt[((size_t)b * p.S + t) * H + h] : 0.0f;
+        bool ok = true;
+        for (int c = 0; c < nchunks; ++c) {
+            const uint32_t par = c & 1, bpar = (c >> 1) & 1;
+            const int buf = c & 1;
+            const int r0 = c * Q;
+            const int rows = min(Q, p.S - r0);
+            ChunkVals& cv = s.cv[buf];
+            // ---- dt and the cumulative sum of a = dt A (double-float) ----
+            float dt = 0.0f;
+            if (t < rows) dt = softplus ? softplus_f32(dt_next + bias) : dt_next;
+            if (c + 1 < nchunks)
+                dt_next = r0 + Q + t < p.S ? p.dt[((size_t)b * p.S + r0 + Q + t) * H + h] : 0.0f;
+            float ghi = dt * Ah, glo = 0.0f;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) xw[e] = __fmul2_rn(make_float2(wr[i], wr[i]), xo[i][e]);
-                    const uint32_t off = chunk_off(t0 + i, cj);
-                    const uint4 px = pack4x2(xo[i]), pw = pack4x2(xw);
-                    at<uint4>(s.XA[buf], off) = factored ? pw : px;
-                    at<uint4>(s.X2[buf], off) = factored ? px : pw;
-                }
+            for (int d = 1; d < 32; d <<= 1) {
+                const float ohi = __shfl_up_sync(0xffffffffu, ghi, d);
+                const float olo = __shfl_up_sync(0xffffffffu, glo, d);
+                if (lane >= d) df_add(ghi, glo, ohi, olo);
+            }
+            if (lane == 31) {
+                s.wsum_hi[quarter] = ghi;
+                s.wsum_lo[quarter] = glo;
+            }
+            // cv[buf] and XS[buf] are free once the back finished chunk c-2
+            if (c >= 2) ok = ok && wait_or_abort(s, &s.epidone[buf], bpar ^ 1);
+            ok = !named_bar_or(kBarFront, kWG, !ok);  // a common decision
+            if (!ok) break;
+            for (int w2 = 0; w2 < quarter; ++w2) df_add(ghi, glo, s.wsum_hi[w2], s.wsum_lo[w2]);
+            const float g2h_t = ghi * kLog2e, g2l_t = glo * kLog2e;
+            cv.g2h[t] = g2h_t;
+            cv.g2l[t] = g2l_t;
+            cv.dts[t] = dt;
+            named_bar_sync(kBarFront, kWG);
+            const float gLh = cv.g2h[rows - 1], gLl = cv.g2l[rows - 1];
+            const bool factored = Ah <= 0.0f && gLh + gLl >= kFactorMinLog2;
+            cv.dec[t] = ex2_fast(fminf(g2h_t + g2l_t, 0.0f));
+            // the row's x scale: v_t = exp(-gamma_t) dt_t or w_t = exp(min(gamma_Q-gamma_t,0)) dt_t
+            const float sc = factored ? ex2_fast(-(g2h_t + g2l_t)) * dt
+                                      : (t < rows ? ex2_fast(fminf((gLh - g2h_t) + (gLl - g2l_t), 0.0f)) * dt : 0.0f);
+            if (t == 0) {
+                cv.decS = ex2_fast(fminf(gLh + gLl, 0.0f));
+                cv.factored = factored;
+            }
+            mbar_arrive(&s.cvready[buf]);  // cv[buf] of chunk c is complete
+            // ---- XS row t = sc * XR row t ----
+            ok = wait_or_abort(s, &s.xconv[buf], bpar);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float2 xv[4];
+                unpack4x2(at<const uint4>(s.XR[buf], chunk_off(t, j)), xv);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) xv[e] = __fmul2_rn(make_float2(sc, sc), xv[e]);
+                at<uint4>(s.XS[buf], chunk_off(t, j)) = pack4x2(xv);
             }
             fence_proxy_async_smem();
-            mbar_arrive(&s.xready);
+            mbar_arrive(&s.xready[buf]);
 
             // ---- causal mask (with the decays in the exact form) ----
             // M is free once G2(c-1) is done; CB(c) is ready once G1(c) is done
-            if (c >= 1) ok = wait_or_abort(s, &s.g2[buf ^ 1], ((c - 1) >> 1) & 1);
+            if (ok && c >= 1) ok = wait_or_abort(s, &s.g2[buf ^ 1], ((c - 1) >> 1) & 1);
             if (ok) ok = wait_or_abort(s, &s.g1, par);
             ok = __all_sync(0xffffffffu, ok);  // warp-uniform: tcgen05.ld is .sync.aligned
             tc_fence_after();
@@ -537,11 +556,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) *reinterpret_cast<volatile int*>(&s.abort) = 1;
     } else {
         // ===================== back: state update, epilogue =====================
-        regs_inc<kWorkRegs>();
-        const int t = tid - kFrontThreads;  // chunk row / state column of this thread
+        regs_inc<kBackRegs>();
+        const int t = tid - 2 * kWG;  // chunk row / state column of this thread
         const int n = t;
-        const int quarter = warp - 4;
-        const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
         float2 hreg[32];  // h[2i .. 2i+1][n]
 #pragma unroll
         for (int i = 0; i < 32; ++i)
@@ -564,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r0 = c * Q;
             const int rows = min(Q, p.S - r0);
             const ChunkVals& cv = s.cv[buf];
-            // z of this row: the first half early, the second half before the epilogue
+            // z of this row, early (used at the end)
             const uint4* zr = reinterpret_cast<const uint4*>(
                 zbase + ((size_t)b * p.S + r0 + min(t, rows - 1)) * (H * P) + h * P);
             uint4 zq[8];
@@ -602,12 +619,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            // y = a Yd + u Yo + D x, a = u (factored) or 1; x from the tile holding x
+            // y = a Yd + u Yo + D x, a = u (factored) or 1
             const float dec = cv.dec[t];
             const float2 dd = make_float2(dec, dec);
             const float2 aa = factored ? dd : make_float2(1.0f, 1.0f);
             const float2 D2 = make_float2(Dh, Dh);
-            const __nv_bfloat16* xt = factored ? s.X2[buf] : s.XA[buf];
             uint4* yrow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) +
                                                    (((size_t)b * p.S + r0 + t) * H + h) * P);
 #pragma unroll
@@ -620,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j2 = 0; j2 < 2; ++j2) {
                     float2 out[4], zv[4], xv[4];
                     if (has_z) unpack4x2(zq[2 * q4 + j2], zv);
-                    unpack4x2(at<const uint4>(const_cast<__nv_bfloat16*>(xt), chunk_off(t, 2 * q4 + j2)), xv);
+                    unpack4x2(at<const uint4>(s.XR[buf], chunk_off(t, 2 * q4 + j2)), xv);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int k = j2 * 8 + 2 * e;
