@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (wg == 3) {
         // ===================== issuer: TMA + MMA (one thread) =====================
-        regs_dec<kIssuerRegs>();
+        regs_set<kIssuerRegs, kLaunchRegs>();
         if (warp == 12 && lane == 0 && nchunks > 0) {
             prefetch_tmap(&map_x);
             prefetch_tmap(&map_bc);
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (wg == 0) {
         // ===================== conv: x rows of each chunk =====================
-        regs_inc<kConvRegs>();
+        regs_set<kConvRegs, kLaunchRegs>();
         const int cj = tid & 7;  // channel group (8 channels)
         float2 wq[4][kMaxW], bq[4];
 #pragma unroll
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) *reinterpret_cast<volatile int*>(&s.abort) = 1;
     } else if (wg == 1) {
         // ===================== front: gamma, scaled x, mask =====================
-        regs_inc<kFrontRegs>();
+        regs_set<kFrontRegs, kLaunchRegs>();
         const int t = tid - kWG;  // chunk row of this thread
         const float Ah = p.A[h];
         const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
@@ -556,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) *reinterpret_cast<volatile int*>(&s.abort) = 1;
     } else {
         // ===================== back: state update, epilogue =====================
-        regs_inc<kBackRegs>();
+        regs_set<kBackRegs, kLaunchRegs>();
         const int t = tid - 2 * kWG;  // chunk row / state column of this thread
         const int n = t;
         float2 hreg[32];  // h[2i .. 2i+1][n]

@@ -118,6 +118,15 @@ template <uint32_t kRegs> __device__ __forceinline__ void regs_dec()
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
+// Set this warpgroup's register count from kFrom (at launch) to kTo:
+// setmaxnreg.inc may only raise it and setmaxnreg.dec only lower it.
+template <uint32_t kTo, uint32_t kFrom> __device__ __forceinline__ void regs_set()
+{
+    static_assert(kTo % 8 == 0 && kTo >= 24 && kTo <= 256, "setmaxnreg range");
+    if constexpr (kTo > kFrom) regs_inc<kTo>();
+    else if constexpr (kTo < kFrom) regs_dec<kTo>();
+}
+
 // ---- TMA -----------------------------------------------------------------
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int x, int y, int z)
