@@ -27,7 +27,8 @@
  *   - Every data pointer is DEVICE memory owned by the caller; the library
  *     keeps no pointer after the call returns and allocates nothing.  The only
  *     state the library holds is one device error word per GPU (see
- *     ssd_read_device_error).
+ *     ssd_read_device_error) and the fixed scratch array behind
+ *     ssd_chunk_scan_static_ws.
  *   - Arrays are dense, row-major, contiguous, in the layouts stated below.
  *     Data pointers must be 16-byte aligned and the row lengths a multiple of
  *     16 bytes (Cdim * sizeof(act) and H * P * sizeof(act)); otherwise the
@@ -163,6 +164,46 @@ SSD_API ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned 
  */
 SSD_API ssd_status ssd_chunk_scan_workspace_size(const ssd_dims* dims, ssd_dtype act, unsigned flags,
                                          int conv_fused, size_t* bytes);
+
+/*
+ * ssd_chunk_scan_static_ws -- ssd_chunk_scan for callers that cannot
+ * allocate device memory.  The paper has no counterpart: this is a library
+ * convenience, not a step of the method.
+ *
+ * Who needs it: code that runs inside a host program which owns every device
+ * allocation (a plugin loaded into another runtime with its own pool), and
+ * serving loops that must not call cudaMalloc on their hot path (it can
+ * synchronise the whole device).  Such callers cannot provide the scratch
+ * ssd_chunk_scan asks for.  This entry point takes the same arguments minus
+ * the workspace and uses, as scratch, a fixed array of
+ * SSD_STATIC_SCRATCH_BYTES that the library's device image holds on every
+ * GPU that loads it, until the process exits.  It allocates nothing.
+ *
+ * Results equal ssd_chunk_scan's with a caller workspace: the same kernels
+ * run.  Limits and rules:
+ *   - Problems whose ssd_chunk_scan_workspace_size() exceeds
+ *     SSD_STATIC_SCRATCH_BYTES return SSD_ERR_UNSUPPORTED before anything is
+ *     launched (for the bf16 tensor-core path with the conv fused that size
+ *     is batch * seqlen * 2 * ngroups * dstate * 2 bytes, so with dstate 128
+ *     batch * seqlen * ngroups may be at most 32768).
+ *   - Nothing in the array has to start at zero: every call writes the
+ *     scratch rows it reads before reading them.  The array keeps the last
+ *     call's contents, which mean nothing to the next call.
+ *   - All calls on a GPU share the one array.  Calls that can overlap on that
+ *     GPU (different streams without ordering between them, or different
+ *     host threads) race on it and give wrong results; order them on one
+ *     stream, or use ssd_chunk_scan with a workspace per stream.
+ *   - The first call made on a device (with that device current) looks up the
+ *     array's device address there (cudaGetSymbolAddress) and caches it; make
+ *     that first call before any stream capture on that device.
+ */
+#define SSD_STATIC_SCRATCH_BYTES ((size_t)16 << 20) /* 16 MiB per GPU */
+SSD_API ssd_status ssd_chunk_scan_static_ws(const ssd_dims* dims, ssd_dtype act, unsigned flags,
+                                    const void* xbc, const float* conv_w, const float* conv_b,
+                                    const void* conv_state_in, void* conv_state_out,
+                                    const float* dt, const float* dt_bias, const float* A,
+                                    const float* D, const void* z, const float* ssm_state_in,
+                                    void* y, float* ssm_state_out, cudaStream_t stream);
 
 /*
  * ssd_decode_step -- one recurrent step for R rows at slot-indexed states.

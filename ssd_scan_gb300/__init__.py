@@ -31,10 +31,13 @@ SSD_BF16 = 1
 SSD_DT_SOFTPLUS = 1
 SSD_HAS_Z = 2
 
+# size of the fixed per-GPU scratch array behind ssd_chunk_scan_static_ws
+SSD_STATIC_SCRATCH_BYTES = 16 << 20
+
 # every symbol include/ssd.h declares
 EXPORTED = ("ssd_conv1d_rows", "ssd_chunk_scan", "ssd_chunk_scan_workspace_size",
             "ssd_decode_step", "ssd_status_string", "ssd_read_device_error",
-            "ssd_launch_counts")
+            "ssd_launch_counts", "ssd_chunk_scan_static_ws")
 
 KERNEL_KINDS = ("conv_rows", "conv_state", "scan_simt", "scan_tc", "bc_conv", "decode_step",
                 "decode_conv")
@@ -78,6 +81,7 @@ def load_library():
             ci, cu, sz = ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
             lib.ssd_conv1d_rows.argtypes = [P, ci, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
             lib.ssd_chunk_scan.argtypes = [P, ci, cu] + [_vp] * 14 + [sz, _vp]
+            lib.ssd_chunk_scan_static_ws.argtypes = [P, ci, cu] + [_vp] * 13 + [_vp]
             lib.ssd_chunk_scan_workspace_size.argtypes = [P, ci, cu, ci, ctypes.POINTER(sz)]
             lib.ssd_decode_step.argtypes = [P, ci, cu] + [_vp] * 10 + [ci, _vp, _vp, _vp]
             lib.ssd_status_string.argtypes = [ci]
@@ -167,6 +171,23 @@ def ssd_chunk_scan(d: ssd_dims, act: int, flags: int, xbc, conv_w, conv_b, conv_
         _ptr(ssm_state_in, f, "ssm_state_in"), _ptr(y, a, "y"),
         _ptr(ssm_state_out, f, "ssm_state_out"), _ptr(workspace, None, "workspace"),
         ws_bytes, _stream(stream)), "ssd_chunk_scan")
+
+
+def ssd_chunk_scan_static_ws(d: ssd_dims, act: int, flags: int, xbc, conv_w, conv_b,
+                             conv_state_in, conv_state_out, dt, dt_bias, A, D, z, ssm_state_in,
+                             y, ssm_state_out, stream=None) -> None:
+    """ssd_chunk_scan without a workspace argument, for callers that cannot
+    allocate device memory: the scratch is the library's fixed per-GPU array
+    (SSD_STATIC_SCRATCH_BYTES); calls that overlap on one GPU race on it."""
+    a = _ACT[act]
+    f = torch.float32
+    _check(load_library().ssd_chunk_scan_static_ws(
+        ctypes.byref(d), act, flags, _ptr(xbc, a, "xbc"), _ptr(conv_w, f, "conv_w"),
+        _ptr(conv_b, f, "conv_b"), _ptr(conv_state_in, a, "conv_state_in"),
+        _ptr(conv_state_out, a, "conv_state_out"), _ptr(dt, f, "dt"),
+        _ptr(dt_bias, f, "dt_bias"), _ptr(A, f, "A"), _ptr(D, f, "D"), _ptr(z, a, "z"),
+        _ptr(ssm_state_in, f, "ssm_state_in"), _ptr(y, a, "y"),
+        _ptr(ssm_state_out, f, "ssm_state_out"), _stream(stream)), "ssd_chunk_scan_static_ws")
 
 
 def ssd_decode_step(d: ssd_dims, act: int, flags: int, xbc, conv_w, conv_b, conv_pool, dt,
