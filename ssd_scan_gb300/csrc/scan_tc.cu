@@ -12,37 +12,44 @@
 //
 // One CTA walks all chunks of one (sequence b, head h); the fp32 state
 // h [P=64, N=128] stays in registers for the whole sequence.  Per chunk,
-// four dense contractions run on the tensor cores (bf16 operands in shared
-// memory, fp32 accumulators in TMEM):
-//   G1  CB[t,s] = C_t . B_s                 A = C  (TMA tile)   B = B (TMA)
-//   G3  Yo[t,p] = C_t . h[p,:]              A = C               B = bf16(h) rows [n][p]
-//   G4  dH[n,p] = sum_s B[s,n] xw[s,p]      A = B^T (MN-major)  B = xw rows [s][p]
-//   G2  Yd[t,p] = sum_s M[t,s] xv[s,p]      A = M (causal mask of CB)  B = xv rows [s][p]
+// four dense contractions run on the tensor cores (bf16 operands, fp32
+// accumulators in TMEM):
+//   G1  CB[t,s] = C_t . B_s               A = C (smem, TMA)   B = B (smem, TMA)
+//   G4  dH[n,p] = sum_s B[s,n] xs[s,p]    A = B^T (smem)      B = xs rows [s][p]
+//   G3  Y[t,p]  = C_t . h[p,:]            A = C (smem)        B = bf16(h) rows [n][p]
+//   G2  Y[t,p] += sum_s M[t,s] xv[s,p]    A = M (TMEM)        B = xv rows [s][p]
 // Two forms of the decay, chosen per chunk:
 //   factored (a <= 0 and the chunk's total decay is moderate): with
 //     u_t = exp(gamma_t) and v_s = exp(-gamma_s) dt_s,
-//     M = mask(CB), xv = xw = v o x, y = u_t (Yd + Yo) + D x,
-//     h <- exp(gamma_Q) (h + dH);  the mask is a plain select and convert.
+//     M = mask(CB), xv = xs = v o x, y = u_t Y + D x, h <- exp(gamma_Q) (h + dH):
+//     G3 and G2 share one accumulator and the mask is a select and convert;
 //   exact (otherwise): M = mask(CB o exp(min(gamma_t - gamma_s, 0)) dt_s),
-//     xv = x, xw = w o x with w_s = exp(min(gamma_Q - gamma_s, 0)) dt_s,
-//     y = Yd + u_t Yo + D x,  h <- exp(gamma_Q) h + dH.
+//     xv = x, xs = w o x with w_s = exp(min(gamma_Q - gamma_s, 0)) dt_s,
+//     G3 goes to its own accumulator Yo, y = Y + u_t Yo + D x,
+//     h <- exp(gamma_Q) h + dH.
 //
-// The CTA is warp-specialised and software-pipelined over chunks, four
-// warpgroups of 128 threads:
-//   conv   x conv + SiLU of the raw TMA tile (4 rows x 8 channels per task)
-//          into the x rows tile XR;
-//   front  dt and the double-float cumulative sum of a; the scaled x tile XS
-//          (v o x or w o x); the causal mask M from CB (blocks above the
-//          diagonal are zero-filled without a TMEM read);
-//   back   the state update and the epilogue y = a Yd + u Yo + D x, times
-//          silu(z);
-//   issuer one thread issues every TMA load and every MMA as soon as its
-//          operands are ready.
-// The conv and front run ahead on chunk c+1 while the back finishes chunk c;
-// the accumulators the back reads (Yd, Yo, dH) are double-buffered in TMEM,
-// and mbarriers carry every hand-off.  setmaxnreg moves registers from the
-// issuing warpgroup to the others.  Every wait is bounded in time; a wait
-// that runs out aborts the CTA and sets the device error word.
+// The masked CB is written back into TMEM (bf16 pairs) and read from there
+// by G2, so it never passes through shared memory: the tensor cores' operand
+// reads and the threads' shared-memory traffic draw on one bandwidth, and for
+// these small-N products it is the tighter limit.
+//
+// Warp roles (512 threads):
+//   conv   (warps 0-3)  raw x rows straight from global memory (the next
+//                       chunk's rows are in flight while the thread waits),
+//                       conv + SiLU, written once as x rows (XR) and once
+//                       scaled (XS);
+//   mask   (warps 4-7)  CB -> M in TMEM, one row per thread;
+//   back   (warps 8-11) the state update (one chunk ahead) and the epilogue
+//                       y = ..., times silu(z);
+//   issuer (warp 12)    one thread issues every TMA load and every MMA as soon
+//                       as its inputs are ready and its output buffer is free;
+//   gamma  (warp 13)    dt, the double-float cumulative sum of a and the
+//                       per-row scales of each chunk, ahead of the others.
+// Every hand-off is an mbarrier; buffers are double-buffered by chunk parity
+// (x rows, scaled x rows, C tile, Y and dH accumulators, bf16 state rows,
+// per-chunk values).  setmaxnreg gives each warpgroup its share of the
+// register file.  Every wait is bounded in time; a wait that runs out aborts
+// the CTA and sets the device error word.
 #include "internal.cuh"
 #include "sm100.cuh"
 
@@ -60,17 +67,17 @@ constexpr int Q = 128;  // rows per chunk
 constexpr int P = 64;   // head dim
 constexpr int N = 128;  // state dim
 constexpr int kWG = 128;                 // threads per warpgroup
-constexpr int kThreads = 4 * kWG;        // conv, front, back, issuer
+constexpr int kThreads = 4 * kWG;        // conv, mask, back, issuer + gamma
 // Registers: launched at kLaunchRegs per thread (512 x 128 = 65,536, the
 // whole pool); setmaxnreg then gives each warpgroup its share, adding up to
 // the pool: 136 + 112 + 192 + 72 = 4 x 128.
 constexpr uint32_t kLaunchRegs = 128;
-constexpr uint32_t kConvRegs = 136, kFrontRegs = 112, kBackRegs = 192, kIssuerRegs = 72;
-static_assert(kConvRegs + kFrontRegs + kBackRegs + kIssuerRegs == 4 * kLaunchRegs,
+constexpr uint32_t kConvRegs = 136, kMaskRegs = 112, kBackRegs = 192, kIssuerRegs = 72;
+static_assert(kConvRegs + kMaskRegs + kBackRegs + kIssuerRegs == 4 * kLaunchRegs,
               "register split");
 constexpr int kMaxW = 4;  // conv taps handled in the kernel (W-1 carried rows)
+constexpr int kRawRows = 16 + kMaxW - 1;     // raw rows a conv thread reads per chunk
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound on any single wait: 2 s
-constexpr uint32_t kBarConv = 1, kBarFront = 2;  // named barriers of two warpgroups
 
 // G1: A, B K-major.  G2, G3: A K-major, B MN-major (row tiles [k][p]).
 // G4: A = B^T read MN-major from the B tile, B MN-major.
@@ -78,38 +85,39 @@ constexpr uint32_t kIdCB = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdY = idesc_bf16_f32(128, 64, false, true);
 constexpr uint32_t kIdState = idesc_bf16_f32(128, 64, true, true);
 
-// TMEM columns: CB, then Yd / Yo / dH, each double-buffered by chunk parity
-constexpr uint32_t kColCB = 0, kColYd = 128, kColYo = 256, kColDH = 384;
+// TMEM columns (512 allocated)
+constexpr uint32_t kColCB = 0;    // CB fp32 [t][s]                    128
+constexpr uint32_t kColM = 128;   // M bf16 pairs [t][s/2]              64
+constexpr uint32_t kColY = 192;   // Y fp32 [t][p], by chunk parity  2 x 64
+constexpr uint32_t kColDH = 320;  // dH fp32 [n][p], by chunk parity 2 x 64
+constexpr uint32_t kColYo = 448;  // Yo fp32 [t][p] (exact chunks)      64
 
 // Below this total chunk decay (log2 units) the mask factors as
 // exp(gamma_t) * exp(-gamma_s): every factor stays within fp32 (2^90 < 2^127).
 constexpr float kFactorMinLog2 = -90.0f;
 
-struct __align__(16) ChunkVals {  // per-chunk row values, written by the front
+struct __align__(16) ChunkVals {  // per-chunk row values, written by the gamma warp
     float g2h[Q], g2l[Q];      // gamma * log2(e), double-float (hi, lo)
-    float dts[Q];              // dt_s
-    float vfac[Q];             // exp(-gamma_s) dt_s (factored mask only)
-    float wrow[Q];             // w_s = exp(min(gamma_Q - gamma_s, 0)) dt_s
+    float dts[Q];              // dt_s (0 past the last row)
+    float sc[Q];               // x scale of G4's operand: v_s (factored) or w_s (exact)
     float dec[Q];              // exp(min(gamma_t, 0))
     float decS;                // exp(min(gamma_Q, 0))
     int factored;              // which form of the decay this chunk uses
+    int pad[2];
 };
 
 struct __align__(1024) TcSmem {
-    __nv_bfloat16 C[2][Q * 64];     // C tile [t][n]: 2 panels of 64 n (TMA, SW128)
-    __nv_bfloat16 B[2][Q * 64];     // B tile [s][n]
-    __nv_bfloat16 Xr[2][Q * 64];    // raw (or post-conv) x tiles [t][p] by chunk parity
+    __nv_bfloat16 C[2][2][Q * 64];  // C tiles [t][n] by chunk parity: 2 panels of 64 n (TMA, SW128)
+    __nv_bfloat16 B[2][Q * 64];     // B tile [s][n]: 2 panels
     __nv_bfloat16 XR[2][Q * 64];    // post-conv x rows [s][p] (SW128), by parity
     __nv_bfloat16 XS[2][Q * 64];    // scaled x rows: v o x (factored) or w o x (exact)
-    __nv_bfloat16 M[2][Q * 64];     // masked CB [t][s]: G2's A (K-major)
-    __nv_bfloat16 Hs[N * 64];       // bf16 state rows [n][p]: G3's B
+    __nv_bfloat16 Hs[2][N * 64];    // bf16 state rows [n][p]: G3's B, by parity
     ChunkVals cv[2];
-    alignas(16) __nv_bfloat16 carry[2][kMaxW - 1][P];  // raw x rows before the chunk, by parity
     alignas(16) float2 wconv[P / 2][kMaxW];  // taps of channel pairs (front-padded with zeros)
     float2 bconv[P / 2];
-    float wsum_hi[4], wsum_lo[4];
-    uint64_t tma_bc, tma_x[2], g1, g2[2], g3[2], g4[2];
-    uint64_t xconv[2], xready[2], cvready[2], mready, hsready, epidone[2];
+    uint64_t full_c[2], full_b;                       // TMA landed
+    uint64_t g1, g4[2], g3[2], mfree, ydone[2], fin;  // MMA commits
+    uint64_t cvready[2], xready[2], mready, hsready[2], epidone[2];
     uint32_t tmem_base;
     int abort;
 };
@@ -119,15 +127,13 @@ constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;
 // operand tiles start on 1024-byte swizzle atoms; vector-accessed members on
 // their vector size
 static_assert(offsetof(TcSmem, C) % 1024 == 0 && offsetof(TcSmem, B) % 1024 == 0, "tile");
-static_assert(offsetof(TcSmem, Xr) % 1024 == 0 && offsetof(TcSmem, XR) % 1024 == 0, "tile");
-static_assert(offsetof(TcSmem, XS) % 1024 == 0 && offsetof(TcSmem, M) % 1024 == 0, "tile");
+static_assert(offsetof(TcSmem, XR) % 1024 == 0 && offsetof(TcSmem, XS) % 1024 == 0, "tile");
 static_assert(offsetof(TcSmem, Hs) % 1024 == 0, "tile");
 static_assert(sizeof(ChunkVals) % 16 == 0 && offsetof(TcSmem, cv) % 16 == 0, "float4 rows");
-static_assert(offsetof(ChunkVals, vfac) % 16 == 0 && offsetof(ChunkVals, wrow) % 16 == 0, "float4");
 static_assert(offsetof(ChunkVals, g2l) % 16 == 0 && offsetof(ChunkVals, dts) % 16 == 0, "float4");
-static_assert(offsetof(TcSmem, carry) % 16 == 0 && (P * 2) % 16 == 0, "uint4 carry rows");
-static_assert(offsetof(TcSmem, wconv) % 8 == 0 && offsetof(TcSmem, bconv) % 8 == 0, "float2");
-static_assert(offsetof(TcSmem, tma_bc) % 8 == 0, "mbarriers");
+static_assert(offsetof(ChunkVals, sc) % 16 == 0 && offsetof(ChunkVals, dec) % 16 == 0, "float4");
+static_assert(offsetof(TcSmem, wconv) % 16 == 0 && offsetof(TcSmem, bconv) % 8 == 0, "float2");
+static_assert(offsetof(TcSmem, full_c) % 8 == 0, "mbarriers");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ float tanh_fast(float v)
@@ -169,6 +175,11 @@ __device__ __forceinline__ void unpack4x2(uint4 r, float2* f)
     for (int i = 0; i < 4; ++i) f[i] = __bfloat1622float2(h[i]);
 }
 
+__device__ __forceinline__ float2 unpack2(uint32_t r)
+{
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r));
+}
+
 __device__ __forceinline__ uint32_t pack2(float2 a)
 {
     __nv_bfloat162 h = __float22bfloat162_rn(a);
@@ -178,6 +189,11 @@ __device__ __forceinline__ uint32_t pack2(float2 a)
 __device__ __forceinline__ uint4 pack4x2(const float2* f)
 {
     return make_uint4(pack2(f[0]), pack2(f[1]), pack2(f[2]), pack2(f[3]));
+}
+
+__device__ __forceinline__ uint2 ldg_u2(const __nv_bfloat16* p)
+{
+    return __ldg(reinterpret_cast<const uint2*>(p));
 }
 
 // byte offset of 16-byte chunk j of row r in a SW128 tile of 64-element rows.
@@ -192,31 +208,35 @@ __device__ __forceinline__ T& at(void* base, uint32_t off)
     return *reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(base) + off);
 }
 
-// Bounded wait that also gives up as soon as another role has aborted.  After
-// a few immediate polls it backs off with nanosleep so that waiting warps do
-// not take issue slots from the warps doing the work.
+__device__ __forceinline__ bool aborted(TcSmem& s)
+{
+    return *reinterpret_cast<volatile int*>(&s.abort) != 0;
+}
+
+__device__ __forceinline__ void set_abort(TcSmem& s)
+{
+    *reinterpret_cast<volatile int*>(&s.abort) = 1;
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.  The
+// hinted try_wait suspends the thread until the phase completes (or about a
+// microsecond passes), so a waiting warp takes no issue slots.
 __device__ __forceinline__ bool wait_or_abort(TcSmem& s, uint64_t* bar, uint32_t parity)
 {
-#pragma unroll 1
-    for (int i = 0; i < 4; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    uint32_t ns = 32;
     while (true) {
-        __nanosleep(ns);
-        if (mbar_try_wait(bar, parity)) return true;
-        ns = ns < 256 ? ns * 2 : 256;
-        if (*reinterpret_cast<volatile int*>(&s.abort)) return false;
+        if (mbar_try_wait_hint(bar, parity, 1000)) return true;
+        if (aborted(s)) return false;
         if (globaltimer_ns() - t0 > kWaitNs) {
-            *reinterpret_cast<volatile int*>(&s.abort) = 1;
+            set_abort(s);
             return false;
         }
     }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    scan_tc_kernel(const __grid_constant__ CUtensorMap map_x,
-                   const __grid_constant__ CUtensorMap map_bc, const TcScanParams p)
+    scan_tc_kernel(const __grid_constant__ CUtensorMap map_bc, const TcScanParams p)
 {
     // Align to the 1024-byte swizzle atom with pointer arithmetic on the
     // shared array itself, so the compiler keeps every access in the shared
@@ -224,31 +244,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     TcSmem& s = *reinterpret_cast<TcSmem*>(smem_raw + ((1024u - (sm100::smem_u32(smem_raw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wg = warp >> 2;             // 0 conv, 1 front, 2 back, 3 issuer
+    const int wg = warp >> 2;             // 0 conv, 1 mask, 2 back, 3 issuer + gamma
     const int quarter = warp & 3;         // TMEM lane quarter of this warp
     const int h = blockIdx.x, b = blockIdx.y;
-    const int H = p.H, G = p.G, W = p.W;
+    const int H = p.H, G = p.G, W = p.W, S = p.S;
     const int g = h / (H / G);
     const int Cdim = H * P + 2 * G * N;
-    const int nchunks = (p.S + Q - 1) / Q;
+    const int nchunks = (S + Q - 1) / Q;
     const bool has_z = (p.flags & kHasZ) != 0;
-    const bool softplus = (p.flags & kDtSoftplus) != 0;
 
     if (tid == 0) {
-        mbar_init(&s.tma_bc, 1);
+        mbar_init(&s.full_b, 1);
         mbar_init(&s.g1, 1);
+        mbar_init(&s.mfree, 1);
+        mbar_init(&s.fin, 1);
+        mbar_init(&s.mready, kWG);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&s.tma_x[i], 1);
-            mbar_init(&s.g2[i], 1);
-            mbar_init(&s.g3[i], 1);
+            mbar_init(&s.full_c[i], 1);
             mbar_init(&s.g4[i], 1);
-            mbar_init(&s.xconv[i], kWG);
+            mbar_init(&s.g3[i], 1);
+            mbar_init(&s.ydone[i], 1);
+            mbar_init(&s.cvready[i], 32);
             mbar_init(&s.xready[i], kWG);
-            mbar_init(&s.cvready[i], kWG);
+            mbar_init(&s.hsready[i], kWG);
             mbar_init(&s.epidone[i], kWG);
         }
-        mbar_init(&s.mready, kWG);
-        mbar_init(&s.hsready, kWG);
         s.abort = 0;
         fence_mbar_init();
     }
@@ -266,15 +286,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             s.bconv[i] = p.conv_b ? make_float2(p.conv_b[h * P + 2 * i], p.conv_b[h * P + 2 * i + 1])
                                   : make_float2(0.f, 0.f);
         }
-        // raw rows -3..-1 before chunk 0: the last rows of the conv state (or zeros)
-        const __nv_bfloat16* cs = static_cast<const __nv_bfloat16*>(p.conv_state_in);
-        for (int i = tid; i < (kMaxW - 1) * P; i += kThreads) {
-            const int j = i / P, pp = i % P;
-            const int sr = (W - 1) + (j - (kMaxW - 1));
-            __nv_bfloat16 v = __float2bfloat16_rn(0.0f);
-            if (cs && sr >= 0) v = cs[((size_t)b * (W - 1) + sr) * Cdim + h * P + pp];
-            s.carry[0][j][pp] = v;
-        }
     }
     tc_fence_before();
     __syncthreads();
@@ -284,276 +295,372 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t sbase = ((size_t)b * H + h) * P * N;
 
     if (wg == 3) {
-        // ===================== issuer: TMA + MMA (one thread) =====================
         regs_set<kIssuerRegs, kLaunchRegs>();
         if (warp == 12 && lane == 0 && nchunks > 0) {
-            prefetch_tmap(&map_x);
+            // ===================== issuer: TMA + MMA (one thread) =====================
+            // Each op is issued once its inputs are ready and its output buffer is
+            // free, in chunk order per op, with G1(c) before G3(c) before G2(c).
+            // Every phase test below is exact: the previous phase of the barrier
+            // it tests is known to be complete by then.
             prefetch_tmap(&map_bc);
             const int xB = p.bc_col0 + g * N;          // first B column in the bc source
             const int xC = p.bc_col0 + G * N + g * N;  // first C column
-            const uint32_t aC = smem_u32(s.C), aB = smem_u32(s.B);
-            const uint32_t aM = smem_u32(s.M), aH = smem_u32(s.Hs);
-            auto load_bc = [&](int c) {
-                mbar_arrive_expect_tx(&s.tma_bc, 4 * Q * 64 * 2);
-                tma_load_3d(s.C[0], &map_bc, &s.tma_bc, xC, c * Q, b);
-                tma_load_3d(s.C[1], &map_bc, &s.tma_bc, xC + 64, c * Q, b);
-                tma_load_3d(s.B[0], &map_bc, &s.tma_bc, xB, c * Q, b);
-                tma_load_3d(s.B[1], &map_bc, &s.tma_bc, xB + 64, c * Q, b);
+            const uint32_t aB = smem_u32(s.B);
+            auto load_c = [&](int c) {
+                uint64_t* bar = &s.full_c[c & 1];
+                mbar_arrive_expect_tx(bar, 2 * Q * 64 * 2);
+                tma_load_3d(s.C[c & 1][0], &map_bc, bar, xC, c * Q, b);
+                tma_load_3d(s.C[c & 1][1], &map_bc, bar, xC + 64, c * Q, b);
             };
-            auto load_x = [&](int c) {
-                mbar_arrive_expect_tx(&s.tma_x[c & 1], Q * 64 * 2);
-                tma_load_3d(s.Xr[c & 1], &map_x, &s.tma_x[c & 1], h * P, c * Q, b);
+            auto load_b = [&](int c) {
+                mbar_arrive_expect_tx(&s.full_b, 2 * Q * 64 * 2);
+                tma_load_3d(s.B[0], &map_bc, &s.full_b, xB, c * Q, b);
+                tma_load_3d(s.B[1], &map_bc, &s.full_b, xB + 64, c * Q, b);
             };
-            load_bc(0);
-            load_x(0);
-            if (nchunks > 1) load_x(1);
+            int nC = 0, nB = 0;  // tiles whose load has been issued
+            load_c(nC++);
+            if (nchunks > 1) load_c(nC++);
+            load_b(nB++);
+            int i1 = 0, i4 = 0, i3 = 0, i2 = 0;  // next chunk of G1, G4, G3, G2
+            uint64_t t_idle = 0;
             bool ok = true;
-            for (int c = 0; c < nchunks && ok; ++c) {
-                const uint32_t par = c & 1, bpar = (c >> 1) & 1;
-                const int buf = c & 1;
-                // G1(c): B, C landed; the front has read CB(c-1)
-                ok = wait_or_abort(s, &s.tma_bc, par);
-                if (ok && c > 0) ok = wait_or_abort(s, &s.mready, par ^ 1);
-                if (!ok) break;
-                tc_fence_after();
+            while (i2 < nchunks || i4 < nchunks) {
+                bool progress = false;
+                // C tile k into buffer k & 1 once G3(k-2) (and so G1(k-2)) is done
+                if (nC < nchunks && nC - 2 < i3 && mbar_test(&s.g3[nC & 1], ((nC - 2) >> 1) & 1)) {
+                    load_c(nC++);
+                    progress = true;
+                }
+                // B tile k once G4(k-1) (and so G1(k-1)) is done
+                if (nB < nchunks && nB - 1 < i4 && mbar_test(&s.g4[(nB - 1) & 1], ((nB - 1) >> 1) & 1)) {
+                    load_b(nB++);
+                    progress = true;
+                }
+                // G1(c): C(c), B(c) landed; the mask warps have read CB(c-1)
+                if (i1 < nC && i1 < nB && mbar_test(&s.full_c[i1 & 1], (i1 >> 1) & 1) &&
+                    mbar_test(&s.full_b, i1 & 1) && (i1 == 0 || mbar_test(&s.mready, (i1 - 1) & 1))) {
+                    tc_fence_after();
+                    const uint32_t aC = smem_u32(s.C[i1 & 1]);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t off = (k >> 2) * (Q * 128) + (k & 3) * 32;
-                    mma_bf16_ss(tbase + kColCB, sdesc_sw128(aC + off, 16, 1024),
-                                sdesc_sw128(aB + off, 16, 1024), kIdCB, k > 0);
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t off = (k >> 2) * (Q * 128) + (k & 3) * 32;
+                        mma_bf16_ss(tbase + kColCB, sdesc_sw128(aC + off, 16, 1024),
+                                    sdesc_sw128(aB + off, 16, 1024), kIdCB, k > 0);
+                    }
+                    mma_commit(&s.g1);
+                    ++i1;
+                    progress = true;
                 }
-                mma_commit(&s.g1);
-                // G4(c): scaled x written; dH[buf] free (the back finished chunk c-2)
-                ok = wait_or_abort(s, &s.xready[buf], bpar);
-                if (ok && c >= 2) ok = wait_or_abort(s, &s.epidone[buf], bpar ^ 1);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t aXS = smem_u32(s.XS[buf]);
+                // G4(c): B(c) in place (G1(c) issued), xs(c) written, dH[c&1] read by state(c-2)
+                if (i4 < i1 && mbar_test(&s.xready[i4 & 1], (i4 >> 1) & 1) &&
+                    (i4 < 2 || mbar_test(&s.hsready[(i4 - 1) & 1], ((i4 - 1) >> 1) & 1))) {
+                    tc_fence_after();
+                    const uint32_t aXS = smem_u32(s.XS[i4 & 1]);
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    mma_bf16_ss(tbase + kColDH + 64 * buf, sdesc_sw128(aB + k * 2048, Q * 128, 1024),
-                                sdesc_sw128(aXS + k * 2048, 8192, 1024), kIdState, k > 0);
-                mma_commit(&s.g4[buf]);
-                // raw x of chunk c+2 into Xr[buf] once the conv has read it
-                if (c + 2 < nchunks) {
-                    ok = wait_or_abort(s, &s.xconv[buf], bpar);
-                    if (!ok) break;
-                    load_x(c + 2);
+                    for (int k = 0; k < 8; ++k)
+                        mma_bf16_ss(tbase + kColDH + 64 * (i4 & 1), sdesc_sw128(aB + k * 2048, Q * 128, 1024),
+                                    sdesc_sw128(aXS + k * 2048, 8192, 1024), kIdState, k > 0);
+                    mma_commit(&s.g4[i4 & 1]);
+                    ++i4;
+                    progress = true;
                 }
-                // G3(c): the back wrote bf16 h of chunk c-1
-                ok = wait_or_abort(s, &s.hsready, par);
-                if (!ok) break;
-                tc_fence_after();
+                // G3(c): after G1(c) (so that "G3(c) done" also means "G1(c) done",
+                // which frees the C buffer); bf16 h of chunk c-1 written; Y[c&1] free
+                // (epilogue c-2); exact chunks also need Yo free (epilogue c-1)
+                if (i3 < i1 && mbar_test(&s.cvready[i3 & 1], (i3 >> 1) & 1) &&
+                    mbar_test(&s.hsready[i3 & 1], (i3 >> 1) & 1) &&
+                    (i3 < 2 || mbar_test(&s.epidone[i3 & 1], ((i3 >> 1) & 1) ^ 1))) {
+                    const bool fac = s.cv[i3 & 1].factored != 0;
+                    if (fac || i3 == 0 || mbar_test(&s.epidone[(i3 - 1) & 1], ((i3 - 1) >> 1) & 1)) {
+                        tc_fence_after();
+                        const uint32_t aC = smem_u32(s.C[i3 & 1]);
+                        const uint32_t aH = smem_u32(s.Hs[i3 & 1]);
+                        const uint32_t dY = fac ? kColY + 64 * (i3 & 1) : kColYo;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t offc = (k >> 2) * (Q * 128) + (k & 3) * 32;
-                    mma_bf16_ss(tbase + kColYo + 64 * buf, sdesc_sw128(aC + offc, 16, 1024),
-                                sdesc_sw128(aH + k * 2048, 8192, 1024), kIdY, k > 0);
+                        for (int k = 0; k < 8; ++k) {
+                            const uint32_t offc = (k >> 2) * (Q * 128) + (k & 3) * 32;
+                            mma_bf16_ss(tbase + dY, sdesc_sw128(aC + offc, 16, 1024),
+                                        sdesc_sw128(aH + k * 2048, 8192, 1024), kIdY, k > 0);
+                        }
+                        mma_commit(&s.g3[i3 & 1]);
+                        ++i3;
+                        progress = true;
+                    }
                 }
-                mma_commit(&s.g3[buf]);
-                // B, C of chunk c+1 once G1, G4, G3 of chunk c are done
-                if (c + 1 < nchunks) {
-                    ok = wait_or_abort(s, &s.g3[buf], bpar);
-                    if (!ok) break;
-                    load_bc(c + 1);
-                }
-                // G2(c): the front wrote M(c); x is XS (factored) or XR (exact)
-                ok = wait_or_abort(s, &s.mready, par);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t aXV = smem_u32(s.cv[buf].factored ? s.XS[buf] : s.XR[buf]);
+                // G2(c): M(c) in TMEM; x rows written; after G3(c) (same accumulator)
+                if (i2 < i3 && mbar_test(&s.mready, i2 & 1) &&
+                    mbar_test(&s.xready[i2 & 1], (i2 >> 1) & 1)) {
+                    tc_fence_after();
+                    const bool fac = s.cv[i2 & 1].factored != 0;
+                    const uint32_t aXV = smem_u32(fac ? s.XS[i2 & 1] : s.XR[i2 & 1]);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t offm = (k >> 2) * (Q * 128) + (k & 3) * 32;
-                    mma_bf16_ss(tbase + kColYd + 64 * buf, sdesc_sw128(aM + offm, 16, 1024),
-                                sdesc_sw128(aXV + k * 2048, 8192, 1024), kIdY, k > 0);
+                    for (int k = 0; k < 8; ++k)
+                        mma_bf16_ts(tbase + kColY + 64 * (i2 & 1), tbase + kColM + 8 * k,
+                                    sdesc_sw128(aXV + k * 2048, 8192, 1024), kIdY, fac || k > 0);
+                    mma_commit(&s.mfree);
+                    mma_commit(&s.ydone[i2 & 1]);
+                    ++i2;
+                    progress = true;
                 }
-                mma_commit(&s.g2[buf]);
+                if (progress) {
+                    t_idle = 0;
+                } else {
+                    if (aborted(s)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint64_t now = globaltimer_ns();
+                    if (t_idle == 0) {
+                        t_idle = now;
+                    } else if (now - t_idle > kWaitNs) {
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(32);
+                }
             }
-            if (!ok) *reinterpret_cast<volatile int*>(&s.abort) = 1;
+            if (!ok) set_abort(s);
+            // Nothing of ours may be in flight when the CTA leaves: wait (bounded)
+            // for the last MMAs and for tiles loaded but never consumed.
+            mma_commit(&s.fin);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_test(&s.fin, 0) && globaltimer_ns() - t0 < kWaitNs) __nanosleep(64);
+            for (int k = i1; k < nC; ++k)
+                while (!mbar_test(&s.full_c[k & 1], (k >> 1) & 1) && globaltimer_ns() - t0 < kWaitNs)
+                    __nanosleep(64);
+            for (int k = i1; k < nB; ++k)
+                while (!mbar_test(&s.full_b, k & 1) && globaltimer_ns() - t0 < kWaitNs) __nanosleep(64);
+        } else if (warp == 13 && nchunks > 0) {
+            // ===================== gamma: per-chunk row values (one warp) =====================
+            // lane l owns rows 4l .. 4l+3 of every chunk
+            const float Ah = p.A[h];
+            const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
+            const bool softplus = (p.flags & kDtSoftplus) != 0;
+            constexpr float kLog2e = 1.4426950408889634f;
+            float dtn[4];
+            auto load_dt = [&](int c) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = c * Q + 4 * lane + i;
+                    dtn[i] = r < S ? p.dt[((size_t)b * S + r) * H + h] : 0.0f;
+                }
+            };
+            load_dt(0);
+            for (int c = 0; c < nchunks; ++c) {
+                const int rows = min(Q, S - c * Q);
+                ChunkVals& cv = s.cv[c & 1];
+                float dt[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float d = softplus ? softplus_f32(dtn[i] + bias) : dtn[i];
+                    dt[i] = 4 * lane + i < rows ? d : 0.0f;
+                }
+                if (c + 1 < nchunks) load_dt(c + 1);
+                // inclusive sums of a = dt A over this lane's rows, then across lanes
+                float gh[4], gl[4];
+                gh[0] = dt[0] * Ah;
+                gl[0] = 0.0f;
+#pragma unroll
+                for (int i = 1; i < 4; ++i) {
+                    gh[i] = gh[i - 1];
+                    gl[i] = gl[i - 1];
+                    df_add(gh[i], gl[i], dt[i] * Ah, 0.0f);
+                }
+                float th = gh[3], tl = gl[3];
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const float oh = __shfl_up_sync(0xffffffffu, th, d);
+                    const float ol = __shfl_up_sync(0xffffffffu, tl, d);
+                    if (lane >= d) df_add(th, tl, oh, ol);
+                }
+                float eh = __shfl_up_sync(0xffffffffu, th, 1);
+                float el = __shfl_up_sync(0xffffffffu, tl, 1);
+                if (lane == 0) eh = el = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) df_add(gh[i], gl[i], eh, el);
+                // gamma_Q: the last element of the cumulative sum (rows past the
+                // end add a = 0, so row Q-1 holds it)
+                const float gLh = __shfl_sync(0xffffffffu, th, 31) * kLog2e;
+                const float gLl = __shfl_sync(0xffffffffu, tl, 31) * kLog2e;
+                const bool factored = Ah <= 0.0f && gLh + gLl >= kFactorMinLog2;
+                float o_h[4], o_l[4], o_sc[4], o_dec[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float g2h = gh[i] * kLog2e, g2l = gl[i] * kLog2e;
+                    o_h[i] = g2h;
+                    o_l[i] = g2l;
+                    o_dec[i] = ex2_fast(fminf(g2h + g2l, 0.0f));
+                    o_sc[i] = factored ? ex2_fast(-(g2h + g2l)) * dt[i]
+                                       : ex2_fast(fminf((gLh - g2h) + (gLl - g2l), 0.0f)) * dt[i];
+                }
+                // cv[c&1] is free once the epilogue of chunk c-2 is done
+                const bool ok = c < 2 || wait_or_abort(s, &s.epidone[c & 1], ((c >> 1) & 1) ^ 1);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                reinterpret_cast<float4*>(cv.g2h)[lane] = make_float4(o_h[0], o_h[1], o_h[2], o_h[3]);
+                reinterpret_cast<float4*>(cv.g2l)[lane] = make_float4(o_l[0], o_l[1], o_l[2], o_l[3]);
+                reinterpret_cast<float4*>(cv.dts)[lane] = make_float4(dt[0], dt[1], dt[2], dt[3]);
+                reinterpret_cast<float4*>(cv.sc)[lane] = make_float4(o_sc[0], o_sc[1], o_sc[2], o_sc[3]);
+                reinterpret_cast<float4*>(cv.dec)[lane] = make_float4(o_dec[0], o_dec[1], o_dec[2], o_dec[3]);
+                if (lane == 0) {
+                    cv.decS = ex2_fast(fminf(gLh + gLl, 0.0f));
+                    cv.factored = factored;
+                }
+                mbar_arrive(&s.cvready[c & 1]);
+            }
         }
     } else if (wg == 0) {
         // ===================== conv: x rows of each chunk =====================
         regs_set<kConvRegs, kLaunchRegs>();
-        const int cj = tid & 7;  // channel group (8 channels)
-        float2 wq[4][kMaxW], bq[4];
+        const int jq = lane & 15;                           // channels 4 jq .. 4 jq + 3
+        const int rbase = 32 * quarter + 16 * (lane >> 4);  // 16 rows of each chunk
+        float2 wq[kMaxW][2], bq[2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            bq[e] = p.conv ? s.bconv[4 * cj + e] : make_float2(0.f, 0.f);
+        for (int e = 0; e < 2; ++e) {
+            bq[e] = p.conv ? s.bconv[2 * jq + e] : make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < kMaxW; ++k)
-                wq[e][k] = p.conv ? s.wconv[4 * cj + e][k] : make_float2(0.f, 0.f);
+                wq[k][e] = p.conv ? s.wconv[2 * jq + e][k] : make_float2(0.f, 0.f);
         }
-        bool ok = true;
+        const __nv_bfloat16* xb =
+            static_cast<const __nv_bfloat16*>(p.xbc) + (size_t)b * S * Cdim + h * P + 4 * jq;
+        const __nv_bfloat16* csb =
+            p.conv_state_in
+                ? static_cast<const __nv_bfloat16*>(p.conv_state_in) + (size_t)b * (W - 1) * Cdim + h * P + 4 * jq
+                : nullptr;
+        uint2 raw[kRawRows];  // raw rows rbase-3 .. rbase+15 of the chunk (4 channels each)
+        auto load_raw = [&](int c) {
+            const int g0 = c * Q + rbase - (kMaxW - 1);
+#pragma unroll
+            for (int i = 0; i < kRawRows; ++i) {
+                const int gr = g0 + i;
+                uint2 v = make_uint2(0u, 0u);
+                if (gr >= 0) {
+                    if (gr < S) v = ldg_u2(xb + (size_t)gr * Cdim);
+                } else if (csb != nullptr && gr + W - 1 >= 0) {
+                    v = ldg_u2(csb + (size_t)(gr + W - 1) * Cdim);
+                }
+                raw[i] = v;
+            }
+        };
+        load_raw(0);
+        const uint32_t coff = (uint32_t)((jq & 1) << 3);
         for (int c = 0; c < nchunks; ++c) {
-            const uint32_t bpar = (c >> 1) & 1;
             const int buf = c & 1;
-            const int rows = min(Q, p.S - c * Q);
-            // XR[buf] is free once the back finished chunk c-2
-            if (c >= 2) ok = ok && wait_or_abort(s, &s.epidone[buf], bpar ^ 1);
-            if (ok) ok = wait_or_abort(s, &s.tma_x[buf], bpar);
-            // together: the carry rows of chunk c-1 are written; a common decision
-            ok = !named_bar_or(kBarConv, kWG, !ok);
+            const int rows = min(Q, S - c * Q);
+            bool ok = wait_or_abort(s, &s.cvready[buf], (c >> 1) & 1);
+            // XR / XS [buf] are free once the epilogue of chunk c-2 is done
+            if (ok && c >= 2) ok = wait_or_abort(s, &s.epidone[buf], ((c >> 1) & 1) ^ 1);
             if (!ok) break;
-#pragma unroll 1
-            for (int task = 0; task < 2; ++task) {
-                const int t0 = 4 * ((tid >> 3) + 16 * task);
-                float2 xo[4][4];  // [row][channel pair]
-                if (p.conv) {
-                    float2 win[7][4];  // raw rows t0-3 .. t0+3
+            const float* scv = s.cv[buf].sc;
+            float2 win[kMaxW - 1][2];
 #pragma unroll
-                    for (int k = 0; k < 7; ++k) {
-                        const int r = t0 - 3 + k;
-                        const uint4 raw = r >= 0 ? at<const uint4>(s.Xr[buf], chunk_off(r, cj))
-                                                 : *reinterpret_cast<const uint4*>(&s.carry[buf][r + 3][8 * cj]);
-                        unpack4x2(raw, win[k]);
-                        if (r >= Q - (kMaxW - 1))  // rows Q-3..Q-1 carry into the next chunk
-                            *reinterpret_cast<uint4*>(&s.carry[buf ^ 1][r - (Q - 3)][8 * cj]) = raw;
+            for (int k = 0; k < kMaxW - 1; ++k) {
+                win[k][0] = unpack2(raw[k].x);
+                win[k][1] = unpack2(raw[k].y);
+            }
+#pragma unroll
+            for (int i4 = 0; i4 < 4; ++i4) {
+                const float4 sc4 = *reinterpret_cast<const float4*>(&scv[rbase + 4 * i4]);
+                const float scs[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+#pragma unroll
+                for (int ii = 0; ii < 4; ++ii) {
+                    const int i = 4 * i4 + ii;
+                    const int r = rbase + i;
+                    const float2 u0 = unpack2(raw[i + kMaxW - 1].x), u1 = unpack2(raw[i + kMaxW - 1].y);
+                    float2 x0, x1;
+                    if (p.conv) {
+                        float2 a0 = bq[0], a1 = bq[1];
+#pragma unroll
+                        for (int k = 0; k < kMaxW - 1; ++k) {
+                            a0 = __ffma2_rn(wq[k][0], win[k][0], a0);
+                            a1 = __ffma2_rn(wq[k][1], win[k][1], a1);
+                        }
+                        a0 = __ffma2_rn(wq[kMaxW - 1][0], u0, a0);
+                        a1 = __ffma2_rn(wq[kMaxW - 1][1], u1, a1);
+                        x0 = silu2(a0);
+                        x1 = silu2(a1);
+                    } else {
+                        x0 = u0;
+                        x1 = u1;
                     }
+                    if (r >= rows) x0 = x1 = make_float2(0.f, 0.f);
+                    const float2 sc2 = make_float2(scs[ii], scs[ii]);
+                    const uint32_t off = chunk_off(r, jq >> 1) + coff;
+                    at<uint2>(s.XR[buf], off) = make_uint2(pack2(x0), pack2(x1));
+                    at<uint2>(s.XS[buf], off) =
+                        make_uint2(pack2(__fmul2_rn(sc2, x0)), pack2(__fmul2_rn(sc2, x1)));
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int k = 0; k < kMaxW - 2; ++k) {
+                        win[k][0] = win[k + 1][0];
+                        win[k][1] = win[k + 1][1];
+                    }
+                    win[kMaxW - 2][0] = u0;
+                    win[kMaxW - 2][1] = u1;
+                }
+            }
+            fence_proxy_async_smem();  // XR / XS are read by G4 / G2
+            mbar_arrive(&s.xready[buf]);
+            if (c + 1 < nchunks) load_raw(c + 1);
+        }
+    } else if (wg == 1) {
+        // ===================== mask: CB -> M in TMEM =====================
+        regs_set<kMaskRegs, kLaunchRegs>();
+        const int t = tid - kWG;  // chunk row of this thread (its TMEM lane)
+        // blocks of M strictly above the diagonal stay zero for the whole sequence
+        {
+            uint32_t zero[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) zero[i] = 0u;
+            for (int cc = quarter + 1; cc < 4; ++cc) tmem_st16(tbase + lane_off + kColM + 16 * cc, zero);
+            tmem_st_wait();
+        }
+        for (int c = 0; c < nchunks; ++c) {
+            const int buf = c & 1;
+            const ChunkVals& cv = s.cv[buf];
+            bool ok = wait_or_abort(s, &s.cvready[buf], (c >> 1) & 1);
+            if (ok) ok = wait_or_abort(s, &s.g1, c & 1);                     // CB(c)
+            if (ok && c >= 1) ok = wait_or_abort(s, &s.mfree, (c - 1) & 1);  // G2(c-1) read M
+            if (!__all_sync(0xffffffffu, ok)) {
+                set_abort(s);
+                break;
+            }
+            tc_fence_after();
+            const bool factored = cv.factored != 0;
+            const float g2h_t = cv.g2h[t], g2l_t = cv.g2l[t];
+#pragma unroll 1
+            for (int cc = 0; cc <= quarter; ++cc) {  // 32-column blocks of s
+                float v[32];
+                tmem_ld32(tbase + lane_off + kColCB + 32 * cc, v);
+                tmem_ld_wait();
+                if (!factored) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const int sb = cc * 32 + 4 * q4;
+                        const float4 gh = *reinterpret_cast<const float4*>(&cv.g2h[sb]);
+                        const float4 gl = *reinterpret_cast<const float4*>(&cv.g2l[sb]);
+                        const float4 ds = *reinterpret_cast<const float4*>(&cv.dts[sb]);
+                        const float ghs[4] = {gh.x, gh.y, gh.z, gh.w}, gls[4] = {gl.x, gl.y, gl.z, gl.w};
+                        const float dss[4] = {ds.x, ds.y, ds.z, ds.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            float2 v = bq[e];
-#pragma unroll
-                            for (int k = 0; k < kMaxW; ++k) v = __ffma2_rn(wq[e][k], win[i + k][e], v);
-                            xo[i][e] = t0 + i < rows ? silu2(v) : make_float2(0.f, 0.f);
+                            const float ex = (g2h_t - ghs[e]) + (g2l_t - gls[e]);
+                            v[4 * q4 + e] = v[4 * q4 + e] * dss[e] * ex2_fast(fminf(ex, 0.0f));
                         }
                     }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        unpack4x2(at<const uint4>(s.Xr[buf], chunk_off(t0 + i, cj)), xo[i]);
                 }
+                if (cc == quarter) {  // the diagonal block: keep s <= t
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    at<uint4>(s.XR[buf], chunk_off(t0 + i, cj)) = pack4x2(xo[i]);
-            }
-            fence_proxy_async_smem();  // XR is read by G2 in the exact form
-            mbar_arrive(&s.xconv[buf]);
-        }
-        if (!ok) *reinterpret_cast<volatile int*>(&s.abort) = 1;
-    } else if (wg == 1) {
-        // ===================== front: gamma, scaled x, mask =====================
-        regs_set<kFrontRegs, kLaunchRegs>();
-        const int t = tid - kWG;  // chunk row of this thread
-        const float Ah = p.A[h];
-        const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
-        constexpr float kLog2e = 1.4426950408889634f;
-        float dt_next = t < p.S ? p.dt[((size_t)b * p.S + t) * H + h] : 0.0f;
-        bool ok = true;
-        for (int c = 0; c < nchunks; ++c) {
-            const uint32_t par = c & 1, bpar = (c >> 1) & 1;
-            const int buf = c & 1;
-            const int r0 = c * Q;
-            const int rows = min(Q, p.S - r0);
-            ChunkVals& cv = s.cv[buf];
-            // ---- dt and the cumulative sum of a = dt A (double-float) ----
-            float dt = 0.0f;
-            if (t < rows) dt = softplus ? softplus_f32(dt_next + bias) : dt_next;
-            if (c + 1 < nchunks)
-                dt_next = r0 + Q + t < p.S ? p.dt[((size_t)b * p.S + r0 + Q + t) * H + h] : 0.0f;
-            float ghi = dt * Ah, glo = 0.0f;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const float ohi = __shfl_up_sync(0xffffffffu, ghi, d);
-                const float olo = __shfl_up_sync(0xffffffffu, glo, d);
-                if (lane >= d) df_add(ghi, glo, ohi, olo);
-            }
-            if (lane == 31) {
-                s.wsum_hi[quarter] = ghi;
-                s.wsum_lo[quarter] = glo;
-            }
-            // cv[buf] and XS[buf] are free once the back finished chunk c-2
-            if (c >= 2) ok = ok && wait_or_abort(s, &s.epidone[buf], bpar ^ 1);
-            ok = !named_bar_or(kBarFront, kWG, !ok);  // a common decision
-            if (!ok) break;
-            for (int w2 = 0; w2 < quarter; ++w2) df_add(ghi, glo, s.wsum_hi[w2], s.wsum_lo[w2]);
-            const float g2h_t = ghi * kLog2e, g2l_t = glo * kLog2e;
-            cv.g2h[t] = g2h_t;
-            cv.g2l[t] = g2l_t;
-            cv.dts[t] = dt;
-            named_bar_sync(kBarFront, kWG);
-            const float gLh = cv.g2h[rows - 1], gLl = cv.g2l[rows - 1];
-            const bool factored = Ah <= 0.0f && gLh + gLl >= kFactorMinLog2;
-            cv.dec[t] = ex2_fast(fminf(g2h_t + g2l_t, 0.0f));
-            // the row's x scale: v_t = exp(-gamma_t) dt_t or w_t = exp(min(gamma_Q-gamma_t,0)) dt_t
-            const float sc = factored ? ex2_fast(-(g2h_t + g2l_t)) * dt
-                                      : (t < rows ? ex2_fast(fminf((gLh - g2h_t) + (gLl - g2l_t), 0.0f)) * dt : 0.0f);
-            if (t == 0) {
-                cv.decS = ex2_fast(fminf(gLh + gLl, 0.0f));
-                cv.factored = factored;
-            }
-            mbar_arrive(&s.cvready[buf]);  // cv[buf] of chunk c is complete
-            // ---- XS row t = sc * XR row t ----
-            ok = wait_or_abort(s, &s.xconv[buf], bpar);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float2 xv[4];
-                unpack4x2(at<const uint4>(s.XR[buf], chunk_off(t, j)), xv);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) xv[e] = __fmul2_rn(make_float2(sc, sc), xv[e]);
-                at<uint4>(s.XS[buf], chunk_off(t, j)) = pack4x2(xv);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&s.xready[buf]);
-
-            // ---- causal mask (with the decays in the exact form) ----
-            // M is free once G2(c-1) is done; CB(c) is ready once G1(c) is done
-            if (ok && c >= 1) ok = wait_or_abort(s, &s.g2[buf ^ 1], ((c - 1) >> 1) & 1);
-            if (ok) ok = wait_or_abort(s, &s.g1, par);
-            ok = __all_sync(0xffffffffu, ok);  // warp-uniform: tcgen05.ld is .sync.aligned
-            tc_fence_after();
-#pragma unroll 1
-            for (int cc = 0; cc < 4 && ok; ++cc) {  // 32-column blocks of s
-                __nv_bfloat16* mpanel = s.M[cc >> 1];
-                if (cc > quarter) {  // strictly above the diagonal for the whole warp
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        at<uint4>(mpanel, chunk_off(t, (cc & 1) * 4 + q4)) = make_uint4(0, 0, 0, 0);
-                    continue;
+                    for (int e = 0; e < 32; ++e) v[e] = (cc * 32 + e <= t) ? v[e] : 0.0f;
                 }
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {  // 16 columns at a time
-                    const int c0 = cc * 32 + 16 * hh;
-                    float v[16];
-                    tmem_ld16(tbase + kColCB + lane_off + c0, v);
-                    tmem_ld_wait();
-                    if (!factored) {
+                uint32_t m[16];
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const int sb = c0 + 4 * q4;
-                            const float4 gh = *reinterpret_cast<const float4*>(&cv.g2h[sb]);
-                            const float4 gl = *reinterpret_cast<const float4*>(&cv.g2l[sb]);
-                            const float4 ds = *reinterpret_cast<const float4*>(&cv.dts[sb]);
-                            const float ghs[4] = {gh.x, gh.y, gh.z, gh.w}, gls[4] = {gl.x, gl.y, gl.z, gl.w};
-                            const float dss[4] = {ds.x, ds.y, ds.z, ds.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float ex = (g2h_t - ghs[e]) + (g2l_t - gls[e]);
-                                v[4 * q4 + e] = v[4 * q4 + e] * dss[e] * ex2_fast(fminf(ex, 0.0f));
-                            }
-                        }
-                    }
-                    if (cc == quarter) {  // the diagonal block: keep s <= t
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) v[e] = (c0 + e <= t) ? v[e] : 0.0f;
-                    }
-#pragma unroll
-                    for (int q2 = 0; q2 < 2; ++q2) {
-                        const float2 m[4] = {make_float2(v[8 * q2 + 0], v[8 * q2 + 1]),
-                                             make_float2(v[8 * q2 + 2], v[8 * q2 + 3]),
-                                             make_float2(v[8 * q2 + 4], v[8 * q2 + 5]),
-                                             make_float2(v[8 * q2 + 6], v[8 * q2 + 7])};
-                        at<uint4>(mpanel, chunk_off(t, (cc & 1) * 4 + 2 * hh + q2)) = pack4x2(m);
-                    }
-                }
+                for (int e = 0; e < 16; ++e) m[e] = pack2(make_float2(v[2 * e], v[2 * e + 1]));
+                tmem_st16(tbase + lane_off + kColM + 16 * cc, m);
             }
-            fence_proxy_async_smem();
+            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&s.mready);
         }
-        if (!ok) *reinterpret_cast<volatile int*>(&s.abort) = 1;
     } else {
         // ===================== back: state update, epilogue =====================
         regs_set<kBackRegs, kLaunchRegs>();
@@ -565,38 +672,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             hreg[i] = p.h0 ? make_float2(p.h0[sbase + (size_t)(2 * i) * N + n],
                                          p.h0[sbase + (size_t)(2 * i + 1) * N + n])
                            : make_float2(0.f, 0.f);
-        auto store_h = [&]() {
+        auto store_h = [&](int slot) {
 #pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8) at<uint4>(s.Hs, chunk_off(n, q8)) = pack4x2(&hreg[4 * q8]);
+            for (int q8 = 0; q8 < 8; ++q8) at<uint4>(s.Hs[slot], chunk_off(n, q8)) = pack4x2(&hreg[4 * q8]);
         };
-        store_h();
+        // h of chunk -1 (the initial state) in slot 0
+        store_h(0);
         fence_proxy_async_smem();
-        mbar_arrive(&s.hsready);
+        mbar_arrive(&s.hsready[0]);
         const __nv_bfloat16* zbase = static_cast<const __nv_bfloat16*>(p.z);
         const float Dh = p.D ? p.D[h] : 0.0f;
-        bool ok = true;
-        for (int c = 0; c < nchunks && ok; ++c) {
-            const uint32_t bpar = (c >> 1) & 1;
+        // state(c): h_c = decS h_{c-1} + b dH(c), stored to slot (c+1)&1
+        auto state = [&](int c) -> bool {
             const int buf = c & 1;
-            const int r0 = c * Q;
-            const int rows = min(Q, p.S - r0);
             const ChunkVals& cv = s.cv[buf];
-            // z of this row, early (used at the end)
-            const uint4* zr = reinterpret_cast<const uint4*>(
-                zbase + ((size_t)b * p.S + r0 + min(t, rows - 1)) * (H * P) + h * P);
-            uint4 zq[8];
-            if (has_z) {
-#pragma unroll
-                for (int q8 = 0; q8 < 8; ++q8) zq[q8] = __ldg(zr + q8);
-            }
-            // ---- state ----
-            ok = wait_or_abort(s, &s.cvready[buf], bpar);     // cv of chunk c written
-            if (ok) ok = wait_or_abort(s, &s.g4[buf], bpar);
-            if (ok) ok = wait_or_abort(s, &s.g3[buf], bpar);  // G3(c) has read Hs
-            ok = __all_sync(0xffffffffu, ok);  // warp-uniform: tcgen05.ld is .sync.aligned
-            if (!ok) break;
+            bool ok = wait_or_abort(s, &s.cvready[buf], (c >> 1) & 1);
+            if (ok) ok = wait_or_abort(s, &s.g4[buf], (c >> 1) & 1);
+            // slot (c+1)&1 was last read by G3(c-1)
+            if (ok && c >= 1) ok = wait_or_abort(s, &s.g3[(c - 1) & 1], ((c - 1) >> 1) & 1);
+            if (!__all_sync(0xffffffffu, ok)) return false;
             tc_fence_after();
-            // h <- decS h + b dH, b = decS (factored: dH carries exp(-gamma_s)) or 1
             const bool factored = cv.factored != 0;
             const float2 dS = make_float2(cv.decS, cv.decS);
             const float2 bS = factored ? dS : make_float2(1.0f, 1.0f);
@@ -610,56 +705,96 @@ __global__ void __launch_bounds__(kThreads, 1)
                     hreg[16 * half + i] = __ffma2_rn(dS, hreg[16 * half + i],
                                                      __fmul2_rn(bS, make_float2(v[2 * i], v[2 * i + 1])));
             }
-            store_h();
+            store_h((c + 1) & 1);
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&s.hsready);
-            // ---- epilogue ----
-            ok = wait_or_abort(s, &s.g2[buf], bpar);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
+            mbar_arrive(&s.hsready[(c + 1) & 1]);
+            return true;
+        };
+        bool ok = nchunks == 0 || state(0);
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int buf = c & 1;
+            const int r0 = c * Q;
+            const int rows = min(Q, S - r0);
+            // z of this row, early (used at the end)
+            uint4 zq[8];
+            if (has_z) {
+                const uint4* zr = reinterpret_cast<const uint4*>(
+                    zbase + ((size_t)b * S + r0 + min(t, rows - 1)) * (H * P) + h * P);
+#pragma unroll
+                for (int q8 = 0; q8 < 8; ++q8) zq[q8] = __ldg(zr + q8);
+            }
+            // the state runs one chunk ahead of the epilogue
+            if (c + 1 < nchunks && !state(c + 1)) {
+                ok = false;
+                break;
+            }
+            // ---- epilogue(c) ----
+            const ChunkVals& cv = s.cv[buf];
+            ok = wait_or_abort(s, &s.ydone[buf], (c >> 1) & 1);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
-            // y = a Yd + u Yo + D x, a = u (factored) or 1
+            const bool factored = cv.factored != 0;
+            // factored: y = u Y + D x;  exact: y = Y + u Yo + D x
             const float dec = cv.dec[t];
             const float2 dd = make_float2(dec, dec);
-            const float2 aa = factored ? dd : make_float2(1.0f, 1.0f);
             const float2 D2 = make_float2(Dh, Dh);
             uint4* yrow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) +
-                                                   (((size_t)b * p.S + r0 + t) * H + h) * P);
+                                                   (((size_t)b * S + r0 + t) * H + h) * P);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {  // 16 columns (2 chunks of 8 p) at a time
-                float yd[16], yo[16];
-                tmem_ld16(tbase + kColYd + 64 * buf + lane_off + 16 * q4, yd);
-                tmem_ld16(tbase + kColYo + 64 * buf + lane_off + 16 * q4, yo);
-                tmem_ld_wait();
+            for (int half = 0; half < 2; ++half) {  // 32 columns (4 chunks of 8 p) at a time
+                float yv[32];
+                tmem_ld32(tbase + kColY + 64 * buf + lane_off + 32 * half, yv);
+                if (!factored) {
+                    float yo[32];
+                    tmem_ld32(tbase + kColYo + lane_off + 32 * half, yo);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int j2 = 0; j2 < 2; ++j2) {
+                    for (int k = 0; k < 32; k += 2) {
+                        const float2 r = __ffma2_rn(dd, make_float2(yo[k], yo[k + 1]),
+                                                    make_float2(yv[k], yv[k + 1]));
+                        yv[k] = r.x;
+                        yv[k + 1] = r.y;
+                    }
+                } else {
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 32; k += 2) {
+                        const float2 r = __fmul2_rn(dd, make_float2(yv[k], yv[k + 1]));
+                        yv[k] = r.x;
+                        yv[k + 1] = r.y;
+                    }
+                }
+#pragma unroll
+                for (int j4 = 0; j4 < 4; ++j4) {
+                    const int j = 4 * half + j4;  // 16-byte chunk of the row (8 p)
                     float2 out[4], zv[4], xv[4];
-                    if (has_z) unpack4x2(zq[2 * q4 + j2], zv);
-                    unpack4x2(at<const uint4>(s.XR[buf], chunk_off(t, 2 * q4 + j2)), xv);
+                    if (has_z) unpack4x2(zq[j], zv);
+                    unpack4x2(at<const uint4>(s.XR[buf], chunk_off(t, j)), xv);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int k = j2 * 8 + 2 * e;
-                        float2 yv = __ffma2_rn(dd, make_float2(yo[k], yo[k + 1]),
-                                               __fmul2_rn(aa, make_float2(yd[k], yd[k + 1])));
-                        yv = __ffma2_rn(D2, xv[e], yv);
-                        if (has_z) yv = __fmul2_rn(yv, silu2(zv[e]));
-                        out[e] = yv;
+                        const int k = j4 * 8 + 2 * e;
+                        float2 v = __ffma2_rn(D2, xv[e], make_float2(yv[k], yv[k + 1]));
+                        if (has_z) v = __fmul2_rn(v, silu2(zv[e]));
+                        out[e] = v;
                     }
-                    if (t < rows) yrow[2 * q4 + j2] = pack4x2(out);
+                    if (t < rows) yrow[j] = pack4x2(out);
                 }
             }
             tc_fence_before();
             mbar_arrive(&s.epidone[buf]);
         }
-        if (ok && !*reinterpret_cast<volatile int*>(&s.abort)) {
+        if (ok && !aborted(s)) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 p.hS[sbase + (size_t)(2 * i) * N + n] = hreg[i].x;
                 p.hS[sbase + (size_t)(2 * i + 1) * N + n] = hreg[i].y;
             }
         } else {
-            *reinterpret_cast<volatile int*>(&s.abort) = 1;
+            set_abort(s);
         }
     }
 
@@ -711,9 +846,7 @@ cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st)
 {
     if (p.B == 0 || p.S == 0) return cudaSuccess;
     if (p.W > kMaxW || !encode_fn()) return cudaErrorNotSupported;
-    const int Cdim = p.H * P + 2 * p.G * N;
-    CUtensorMap mx, mbc;
-    if (!make_map(&mx, p.xbc, Cdim, p.S, p.B)) return cudaErrorInvalidValue;
+    CUtensorMap mbc;
     if (!make_map(&mbc, p.bc, p.bc_stride, p.S, p.B)) return cudaErrorInvalidValue;
     // The warpgroups' register split assumes the kernel was compiled to
     // exactly kLaunchRegs per thread; anything else is refused (a split that
@@ -726,7 +859,7 @@ cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st)
                              (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(p.H, p.B);
-    scan_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mx, mbc, p);
+    scan_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mbc, p);
     return cudaGetLastError();
 }
 
