@@ -207,10 +207,12 @@ ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned flags, c
     const bool bf16 = act == SSD_BF16;
     if (tc) {
         const int H = dims->nheads, P = dims->headdim, N = dims->dstate, G = dims->ngroups;
+        // the scan kernel also writes the new conv state (each CTA its head's x
+        // columns, one CTA per group its B|C columns)
         TcScanParams tp{dims->batch, dims->seqlen, H, G, dims->conv_width, flags,
                         conv_w != nullptr, xbc, xbc, (int)cdim, H * P, conv_w, conv_b,
-                        conv_state_in, dt, dt_bias, A, D, has_z ? z : nullptr, ssm_state_in, y,
-                        ssm_state_out, err};
+                        conv_state_in, conv_w != nullptr ? conv_state_out : nullptr, dt, dt_bias,
+                        A, D, has_z ? z : nullptr, ssm_state_in, y, ssm_state_out, err};
         if (conv_w != nullptr) {
             // B|C columns: conv + SiLU once per group into the workspace
             ConvParams bp{dims->batch, dims->seqlen, (int)cdim, dims->conv_width, xbc, conv_w,
@@ -229,7 +231,7 @@ ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned flags, c
         s = counted(launch_scan_simt(p, bf16, stream), SSD_KERNEL_SCAN_SIMT);
     }
     if (s != SSD_OK) return s;
-    if (conv_w != nullptr && conv_state_out != nullptr) {
+    if (conv_w != nullptr && conv_state_out != nullptr && !(tc && dims->seqlen > 0)) {
         ConvParams cp{dims->batch, dims->seqlen, (int)cdim, dims->conv_width,
                       xbc, conv_w, conv_b, conv_state_in, nullptr, conv_state_out};
         s = counted(launch_conv_state(cp, bf16, stream), SSD_KERNEL_CONV_STATE,

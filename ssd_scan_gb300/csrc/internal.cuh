@@ -98,6 +98,7 @@ struct TcScanParams {
     const float* conv_w;         // [Cdim,W] (when conv)
     const float* conv_b;         // [Cdim] or null
     const void* conv_state_in;   // [B,W-1,Cdim] bf16 or null
+    void* conv_state_out;        // [B,W-1,Cdim] bf16 or null (may alias conv_state_in)
     const float* dt;             // [B,S,H]
     const float* dt_bias;        // [H] or null
     const float* A;              // [H]

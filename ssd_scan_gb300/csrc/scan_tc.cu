@@ -776,6 +776,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.hS[sbase + (size_t)(16 * j + 2 * i + 1) * N + t] = hreg[i].y;
             }
         }
+        // new conv state: rows S .. S+W-2 of [conv state ; x|B|C], for this head's x
+        // columns and, from the first head of a group, the group's B and C columns.
+        // Every read of the old state by this CTA (its x columns, chunk 0) and by the
+        // B|C conv before it is long done; a thread reads its column's rows before
+        // writing, in increasing order, so the state may be updated in place.
+        const int hpg = H / G;
+        const int ncol = P + (h % hpg == 0 ? 2 * N : 0);
+        if (p.conv_state_out != nullptr && W > 1 && tid < ncol) {
+            const int col = tid < P ? h * P + tid
+                                    : (tid < P + N ? H * P + g * N + (tid - P) : H * P + G * N + g * N + (tid - P - N));
+            const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(p.xbc);
+            const __nv_bfloat16* si = static_cast<const __nv_bfloat16*>(p.conv_state_in);
+            __nv_bfloat16* so = static_cast<__nv_bfloat16*>(p.conv_state_out);
+            const int nh = W - 1;
+            for (int jj = 0; jj < nh; ++jj) {
+                const int r = S + jj;  // row of [conv state ; rows]
+                __nv_bfloat16 v;
+                if (r < nh) v = si ? si[((size_t)b * nh + r) * Cdim + col] : __float2bfloat16_rn(0.0f);
+                else v = xs[((size_t)b * S + (r - nh)) * Cdim + col];
+                so[((size_t)b * nh + jj) * Cdim + col] = v;
+            }
+        }
     }
 
     tc_fence_before();
