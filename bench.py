@@ -198,6 +198,16 @@ def whole_job_tokens_per_s(world: int, shape: si.Shape, ms_max: float) -> float:
     return world * shape.batch * shape.seqlen / (ms_max / 1e3)
 
 
+def queue_ahead(host_s_per_call: float, calls: int):
+    """Keep the GPU busy (a spin kernel on the current stream) for longer than
+    the host needs to queue `calls` calls, so that the start event recorded
+    after it fires with the timed calls already queued: the events then time
+    the device's work back to back, not the host's launch latency (the e2e
+    number carries that)."""
+    seconds = min(0.05, 2.0 * host_s_per_call * calls + 2e-4)
+    torch.cuda._sleep(int(seconds * 2.1e9))  # cycles at up to 2.1 GHz
+
+
 def make_prefill_sets(shape, nsets, seed_base, device):
     import ssd_scan_gb300 as ssd
     prm = {k: v.to(device) for k, v in si.params(shape, seed=seed_base).items()}
@@ -245,20 +255,28 @@ def bench_ours(args):
     nsets = max(3, -(-2 * L2_BYTES // set_bytes))  # rotate over > 2x L2 of inputs+outputs
     prm, sets, d, flags = make_prefill_sets(shape, nsets, rank_seed(rank), dev)
 
-    # ---- warm-up, then K timed steps (one ssd_chunk_scan call each)
+    # ---- warm-up (also the host's cost of one call), then K timed steps (one
+    # ssd_chunk_scan call each), queued behind a spin so that none waits on the host
+    host_s = []
     for i in range(args.warmup):
         inp, out, ws = sets[i % nsets]
+        t0 = time.perf_counter()
         prefill_call(ssd, d, flags, prm, inp, out, ws, stream)
+        host_s.append(time.perf_counter() - t0)
     torch.cuda.synchronize()
+    host_call = statistics.median(host_s[1:] or host_s)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = ssd.ssd_launch_counts()
     with ClockSampler(local) as clk:
         _barrier(world)
         torch.cuda.synchronize()
+        queue_ahead(host_call, args.steps)
         ev0.record(stream)
+        t0 = time.perf_counter()
         for i in range(args.steps):
             inp, out, ws = sets[i % nsets]
             prefill_call(ssd, d, flags, prm, inp, out, ws, stream)
+        host_loop = (time.perf_counter() - t0) / args.steps
         ev1.record(stream)
         torch.cuda.synchronize()
         _barrier(world)
@@ -300,6 +318,7 @@ def bench_ours(args):
             "roofline": roofline,
             "e2e": e2e,
             "gpu_launches": gpu_launches,
+            "host_us_per_call": round(host_loop * 1e6, 1),
             "clocks": clk.summary(),
             "decode": dec,
         }
@@ -356,12 +375,16 @@ def bench_decode(ssd, dev, stream, world, args):
                             prm["D"], inp["z"], pools["slot_ids"], nslots, pools["ssm_pool"], y,
                             stream)
 
+    host_s = []
     for t in range(max(3, args.warmup)):
+        t0 = time.perf_counter()
         step(t)
+        host_s.append(time.perf_counter() - t0)
     torch.cuda.synchronize()
     steps = si.DECODE_STEPS
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _barrier(world)
+    queue_ahead(statistics.median(host_s[1:]), steps)
     ev0.record(stream)
     for t in range(steps):
         step(t)

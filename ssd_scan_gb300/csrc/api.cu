@@ -223,7 +223,7 @@ ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned flags, c
             tp.bc_stride = 2 * G * N;
             tp.bc_col0 = 0;
         }
-        s = counted(launch_scan_tc(tp, stream), SSD_KERNEL_SCAN_TC);
+        s = counted(launch_scan_tc(tp, stream, conv_w != nullptr), SSD_KERNEL_SCAN_TC);
     } else {
         ScanParams p{dims->batch, dims->seqlen, dims->nheads, dims->headdim, dims->dstate,
                      dims->ngroups, dims->conv_width, flags, xbc, conv_w, conv_b, conv_state_in,

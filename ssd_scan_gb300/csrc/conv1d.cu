@@ -10,6 +10,7 @@
 // rows, keeping the last W-1 raw rows of its channels in registers, so a
 // warp reads and writes 512 contiguous bytes per row.
 #include "internal.cuh"
+#include "sm100.cuh"
 
 namespace ssd {
 namespace {
@@ -77,6 +78,9 @@ __global__ void __launch_bounds__(128) conv1d_rows_kernel(ConvParams p)
     constexpr int V = Vec16<T>::n;
     constexpr int R = kRowsPerThread;
     const int nvec = p.ncols / V;
+    // a scan launched to overlap this kernel may be scheduled now: it waits for
+    // this grid to finish before it reads what this grid writes
+    sm100::griddep_launch_dependents();
     const int cv = blockIdx.x * blockDim.x + threadIdx.x;
     if (cv >= nvec) return;
     const int b = blockIdx.z;

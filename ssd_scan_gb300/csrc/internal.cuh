@@ -110,7 +110,10 @@ struct TcScanParams {
     unsigned* err;
 };
 bool scan_tc_supports(int P, int N);
-cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st);
+// after_prepass: the kernel just before it on `st` is the B|C conv writing p.bc;
+// the scan is then launched to overlap that kernel's tail (programmatic
+// dependent launch) and waits for it before its first read of p.bc.
+cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st, bool after_prepass);
 
 bool decode_supports(int H, int P, int N, int G);
 cudaError_t launch_decode_step(const DecodeParams& p, bool bf16, cudaStream_t st);

@@ -306,6 +306,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // next state update.
         if (lane == 0 && nchunks > 0) {
             prefetch_tmap(&map_bc);
+            // launched to overlap the B|C conv that writes the bc tiles (when there
+            // is one): wait for it here, before the first tile load.  Every read of
+            // the old conv state by that kernel is then done too, so the new conv
+            // state written at the end (it may overwrite the old one in place) is
+            // ordered after it: its writers wait on MMAs issued after this point.
+            griddep_wait();
             const int xB = p.bc_col0 + g * N;          // first B column in the bc source
             const int xC = p.bc_col0 + G * N + g * N;  // first C column
             auto load = [&](int c) {  // C and B tiles of chunk c into buffers c & 1
@@ -844,7 +850,7 @@ bool make_map(CUtensorMap* m, const void* base, int cols, int S, int B)
 
 bool scan_tc_supports(int P_, int N_) { return P_ == P && N_ == N; }
 
-cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st)
+cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st, bool after_prepass)
 {
     if (p.B == 0 || p.S == 0) return cudaSuccess;
     if (p.W > kMaxW || !encode_fn()) return cudaErrorNotSupported;
@@ -853,9 +859,17 @@ cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st)
     cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.H, p.B);
-    scan_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mbc, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.H, p.B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_prepass ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, scan_tc_kernel, mbc, p);
 }
 
 }  // namespace ssd

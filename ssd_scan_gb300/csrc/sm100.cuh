@@ -172,6 +172,16 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch.  griddep_wait blocks until the grid this one
+// was launched to depend on has completed and its memory is visible (at once
+// when there is none); griddep_launch_dependents lets that dependent grid be
+// scheduled once every CTA of this grid has issued it.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Make generic-proxy shared-memory writes visible to the async proxy (TMA,
 // tcgen05.mma) -- each writing thread, before the barrier that orders them.
 __device__ __forceinline__ void fence_proxy_async_smem()
