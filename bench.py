@@ -293,9 +293,12 @@ def bench_ours(args):
                 "peak_source": hbm_src,
                 "kernel": "ssd_chunk_scan call (all its kernels, events around the call)",
                 "algorithmic_bytes_per_launch": pb["per_launch"]}
+    extra = None
     if args.only == "prefill":  # profiling runs: the timed prefill steps alone
         e2e = dec = None
     else:
+        if args.extra:
+            extra = bench_extra(ssd, dev, stream, args)
         # ---- end to end through the C-ABI from pinned host buffers
         e2e = bench_e2e(ssd, shape, d, flags, prm, sets[0], stream, args)
         # ---- decode step (256 rows, 1024-slot pool, 64 steps)
@@ -322,6 +325,8 @@ def bench_ours(args):
             "clocks": clk.summary(),
             "decode": dec,
         }
+        if extra is not None:
+            out["extra_workloads"] = extra
     return out
 
 
@@ -353,6 +358,78 @@ def bench_e2e(ssd, shape, d, flags, prm, dset, stream, args):
     ms = ev0.elapsed_time(ev1) / n
     return {"value": round(shape.batch * shape.seqlen / (ms / 1e3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4)}
+
+
+def chained_calls(ssd, shape, prm, inp, splits, device):
+    """Pre-sliced, contiguous per-call inputs and outputs for a sequence fed as
+    consecutive ssd_chunk_scan calls (rows `splits`), each call continuing from
+    the previous one's SSM and conv state.  Returns a function that issues the
+    calls once."""
+    B, H, P, N, G, W = (shape.batch, shape.nheads, shape.headdim, shape.dstate, shape.ngroups,
+                        shape.conv_width)
+    flags = ssd.SSD_DT_SOFTPLUS | ssd.SSD_HAS_Z
+    calls, r0 = [], 0
+    hs = [torch.empty((B, H, P, N), dtype=torch.float32, device=device) for _ in range(2)]
+    cs = [torch.empty((B, W - 1, shape.cdim), dtype=torch.bfloat16, device=device)
+          for _ in range(2)]
+    ws = ssd.workspace_for(ssd.dims(B, max(splits), H, P, N, G, W, shape.chunk), ssd.SSD_BF16,
+                           flags, True, device)
+    for i, L in enumerate(splits):
+        d = ssd.dims(B, L, H, P, N, G, W, shape.chunk)
+        c = {"d": d, "xbc": inp["xbc"][:, r0:r0 + L].contiguous(),
+             "dt": inp["dt_raw"][:, r0:r0 + L].contiguous(),
+             "z": inp["z"][:, r0:r0 + L].contiguous(),
+             "y": torch.empty((B, L, H, P), dtype=torch.bfloat16, device=device),
+             "h_in": inp["ssm_state"] if i == 0 else hs[(i - 1) % 2], "h_out": hs[i % 2],
+             "cs_in": inp["conv_state"] if i == 0 else cs[(i - 1) % 2], "cs_out": cs[i % 2]}
+        calls.append(c)
+        r0 += L
+
+    def run(stream):
+        for c in calls:
+            ssd.ssd_chunk_scan(c["d"], ssd.SSD_BF16, flags, c["xbc"], prm["conv_w"],
+                               prm["conv_b"], c["cs_in"], c["cs_out"], c["dt"], prm["dt_bias"],
+                               prm["A"], prm["D"], c["z"], c["h_in"], c["y"], c["h_out"], ws,
+                               stream)
+    return run, len(calls)
+
+
+def bench_extra(ssd, dev, stream, args):
+    """The other prefill workloads, timed like the headline one: long (8
+    sequences x 8192 rows, then a chained second call of 8192 rows each) and
+    decay stress (4 x 4096 rows with decays up to ~1e4 per row, fed as calls of
+    U{1..128} rows).  Tokens/s over all calls of one pass."""
+    out = {}
+    for name, shape, splits, stress in (
+            ("long_8x8192_plus_8192", si.LONG.with_(seqlen=2 * si.LONG.seqlen),
+             [si.LONG.seqlen, si.LONG.seqlen], False),
+            ("stress_4x4096_calls_1_to_128", si.STRESS, si.random_splits(si.STRESS.seqlen, 5),
+             True)):
+        prm = {k: v.to(dev) for k, v in si.params(shape, seed=11, stress=stress).items()}
+        inp = si.prefill_inputs(shape, seed=12, device=dev, stress=stress)
+        run, ncalls = chained_calls(ssd, shape, prm, inp, splits, dev)
+        host_s = []
+        for _ in range(3):
+            t0 = time.perf_counter()
+            run(stream)
+            host_s.append(time.perf_counter() - t0)
+        torch.cuda.synchronize()
+        steps = 5
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        queue_ahead(min(host_s), steps)
+        ev0.record(stream)
+        for _ in range(steps):
+            run(stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / steps
+        rows = shape.batch * shape.seqlen
+        out[name] = {"tokens_per_s": round(rows / (ms / 1e3), 1), "ms_per_pass": round(ms, 4),
+                     "calls_per_pass": ncalls, "rows_per_pass": rows,
+                     "host_ms_per_pass": round(min(host_s) * 1e3, 3)}
+        del inp, run
+    assert ssd.ssd_read_device_error(stream) == ssd.SSD_OK
+    return out
 
 
 def bench_decode(ssd, dev, stream, world, args):
@@ -407,7 +484,7 @@ def bench_decode(ssd, dev, stream, world, args):
 # the fp64 oracle on the host cores
 
 def oracle_sample_rows() -> int:
-    return int(os.environ.get("SSD_BENCH_ORACLE_ROWS", "128"))
+    return int(os.environ.get("SSD_BENCH_ORACLE_ROWS", str(si.PREFILL.seqlen)))
 
 
 def oracle_prefill_sample(rows: int):
@@ -431,12 +508,19 @@ def oracle_prefill_sample(rows: int):
     return dt, threads
 
 
-def cpu_baseline() -> dict:
+def cpu_baseline(min_seconds: float = 10.0) -> dict:
+    """The oracle on the prefill workload, repeated until at least
+    `min_seconds` of wall time (at least once)."""
     rows = oracle_sample_rows()
-    dt, threads = oracle_prefill_sample(rows)
-    return {"value": round(rows / dt, 2), "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"first {rows} of the 2048 rows of the prefill workload, all 128 heads "
-                      f"(conv + recurrence + gate, fp64), {dt:.2f} s"}
+    total, passes, threads = 0.0, 0, 1
+    while passes == 0 or total < min_seconds:
+        dt, threads = oracle_prefill_sample(rows)
+        total += dt
+        passes += 1
+    return {"value": round(rows * passes / total, 2), "unit": "tokens/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{passes} passes over the first {rows} of the 2048 rows of the prefill "
+                      f"workload, all 128 heads (conv + recurrence + gate, fp64), {total:.1f} s"}
 
 
 def bench_reference(args):
@@ -475,6 +559,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra", action="store_true",
+                    help="also time the long (8 x 8192 + 8192) and decay-stress prefill workloads")
     ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
                     help="time only the prefill or only the decode steps (profiler runs)")
     ap.add_argument("--decode-slots", type=int, default=si.DECODE_SLOTS,
