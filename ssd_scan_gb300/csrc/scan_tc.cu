@@ -99,10 +99,10 @@ struct __align__(16) ChunkVals {  // per-chunk row values, written by the gamma 
 };
 
 struct __align__(1024) TcSmem {
-    __nv_bfloat16 C[2][2][Q * 64];  // C tiles [t][n] by chunk parity: 2 panels of 64 n (TMA, SW128)
+    __nv_bfloat16 C[2][Q * 64];     // C tile [t][n]: 2 panels of 64 n (TMA, SW128); one chunk
     __nv_bfloat16 B[2][2][Q * 64];  // B tiles [s][n] by chunk parity
     __nv_bfloat16 XS[2][Q * 64];    // scaled x rows [s][p] (SW128): v o x or w o x, by parity
-    __nv_bfloat16 XR[Q * 64];       // x rows [s][p] (exact chunks)
+    __nv_bfloat16 XR[2][Q * 64];    // x rows [s][p] (exact chunks), by parity
     __nv_bfloat16 Hs[N * 64];       // bf16 state rows [n][p] of the previous chunk: G3's B
     ChunkVals cv[kCv];              // ring of per-chunk values
     uint4 zs[2][kCompute];          // z of each compute thread's epilogue share (cp.async)
@@ -110,7 +110,7 @@ struct __align__(1024) TcSmem {
     // pairs of a tap as one 16-byte vector, a half-warp a contiguous 256 bytes
     alignas(16) float2 wconv[kMaxW][P / 2];
     alignas(16) float2 bconv[P / 2];
-    uint64_t full_c[2], full_b[2];  // TMA landed
+    uint64_t full_c, full_b[2];     // TMA landed
     uint64_t g1, g3, g4, g2, fin;   // MMA commits
     uint64_t xready, mready, hsready;                    // compute -> control
     uint64_t cvready[kCv], epidone[kCv];                 // gamma warp <-> compute
@@ -125,6 +125,7 @@ constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;
 static_assert(offsetof(TcSmem, C) % 1024 == 0 && offsetof(TcSmem, B) % 1024 == 0, "tile");
 static_assert(offsetof(TcSmem, XS) % 1024 == 0 && offsetof(TcSmem, XR) % 1024 == 0, "tile");
 static_assert(sizeof(((TcSmem*)nullptr)->XS[0]) % 1024 == 0, "tile");
+static_assert(sizeof(((TcSmem*)nullptr)->XR[0]) % 1024 == 0, "tile");
 static_assert(offsetof(TcSmem, Hs) % 1024 == 0, "tile");
 static_assert(sizeof(ChunkVals) % 16 == 0 && offsetof(TcSmem, cv) % 16 == 0, "float4 rows");
 static_assert(offsetof(ChunkVals, g2l) % 16 == 0 && offsetof(ChunkVals, dts) % 16 == 0, "float4");
@@ -259,10 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool has_z = (p.flags & kHasZ) != 0;
 
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s.full_c[i], 1);
-            mbar_init(&s.full_b[i], 1);
-        }
+        mbar_init(&s.full_c, 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&s.full_b[i], 1);
         mbar_init(&s.g1, 1);
         mbar_init(&s.g3, 1);
         mbar_init(&s.g4, 1);
@@ -300,10 +299,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kControlWarp) {
         // ===================== control: TMA + MMA (one thread) =====================
-        // Order: G1(0), G3(0); per chunk c: G4(c), G2(c), G1(c+1), G3(c+1), then the
-        // tiles of chunk c+2.  G3(c+1) needs only h of chunk c, so it runs while the
-        // compute warps convolve chunk c+1; only G4 separates that conv from the
-        // next state update.
+        // Order: G1(0), G3(0); per chunk c: G4(c), then (once G4(c) is done, so
+        // are G1(c) and G3(c), issued before it) the C tile of chunk c+1 into the
+        // one C buffer and the B tile of chunk c+2 into B[c&1]; G2(c), G1(c+1),
+        // G3(c+1).  G3(c+1) needs only h of chunk c, so it runs while the compute
+        // warps convolve chunk c+1; only G4 separates that conv from the next
+        // state update.
         if (lane == 0 && nchunks > 0) {
             prefetch_tmap(&map_bc);
             // launched to overlap the B|C conv that writes the bc tiles (when there
@@ -314,14 +315,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             griddep_wait();
             const int xB = p.bc_col0 + g * N;          // first B column in the bc source
             const int xC = p.bc_col0 + G * N + g * N;  // first C column
-            auto load = [&](int c) {  // C and B tiles of chunk c into buffers c & 1
+            int loaded_c = 0, loaded_b = 0;  // tiles requested so far
+            auto load_c = [&](int c) {  // C tile of chunk c (the one buffer)
+                mbar_arrive_expect_tx(&s.full_c, 2 * Q * 64 * 2);
+                tma_load_3d(s.C[0], &map_bc, &s.full_c, xC, c * Q, b);
+                tma_load_3d(s.C[1], &map_bc, &s.full_c, xC + 64, c * Q, b);
+                loaded_c = c + 1;
+            };
+            auto load_b = [&](int c) {  // B tile of chunk c into buffer c & 1
                 const int kb = c & 1;
-                mbar_arrive_expect_tx(&s.full_c[kb], 2 * Q * 64 * 2);
-                tma_load_3d(s.C[kb][0], &map_bc, &s.full_c[kb], xC, c * Q, b);
-                tma_load_3d(s.C[kb][1], &map_bc, &s.full_c[kb], xC + 64, c * Q, b);
                 mbar_arrive_expect_tx(&s.full_b[kb], 2 * Q * 64 * 2);
                 tma_load_3d(s.B[kb][0], &map_bc, &s.full_b[kb], xB, c * Q, b);
                 tma_load_3d(s.B[kb][1], &map_bc, &s.full_b[kb], xB + 64, c * Q, b);
+                loaded_b = c + 1;
             };
             // K step k of a K-major operand: (k>>2)*16 KB + (k&3)*32 B; of an MN-major
             // one: 2 KB (16 rows).  Descriptors count 16-byte units in their start
@@ -330,9 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dHs = sdesc_sw128(smem_u32(s.Hs), 8192, 1024);
             const uint64_t dXS0 = sdesc_sw128(smem_u32(s.XS[0]), 8192, 1024);
             const uint64_t dXS1 = sdesc_sw128(smem_u32(s.XS[1]), 8192, 1024);
-            const uint64_t dXR = sdesc_sw128(smem_u32(s.XR), 8192, 1024);
+            const uint64_t dXR0 = sdesc_sw128(smem_u32(s.XR[0]), 8192, 1024);
+            const uint64_t dXR1 = sdesc_sw128(smem_u32(s.XR[1]), 8192, 1024);
+            const uint64_t dC = sdesc_sw128(smem_u32(s.C), 16, 1024);
             auto g1 = [&](int c) {
-                const uint64_t dA = sdesc_sw128(smem_u32(s.C[c & 1]), 16, 1024);
+                const uint64_t dA = dC;
                 const uint64_t dB = sdesc_sw128(smem_u32(s.B[c & 1]), 16, 1024);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
@@ -348,20 +356,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!r) return false;
                 tc_fence_after();
                 const uint32_t dY = (s.cv[c % kCv].factored ? kColY : kColYo) + 64 * (c & 1);
-                const uint64_t dA = sdesc_sw128(smem_u32(s.C[c & 1]), 16, 1024);
+                const uint64_t dA = dC;
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     mma_bf16_ss(tbase + dY, dA + kmaj(k), dHs + 128 * k, kIdY, k > 0);
                 mma_commit(&s.g3);
                 return true;
             };
-            int loaded = 1;
-            load(0);
-            if (nchunks > 1) {
-                load(1);
-                loaded = 2;
-            }
-            bool ok = wait_or_abort(s, &s.full_c[0], 0) && wait_or_abort(s, &s.full_b[0], 0);
+            load_c(0);
+            load_b(0);
+            if (nchunks > 1) load_b(1);
+            bool ok = wait_or_abort(s, &s.full_c, 0) && wait_or_abort(s, &s.full_b[0], 0);
             if (ok) {
                 tc_fence_after();
                 g1(0);
@@ -380,13 +385,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16_ss(tbase + kColDH, dA + 128 * k, (kb ? dXS1 : dXS0) + 128 * k, kIdState, k > 0);
                     mma_commit(&s.g4);
                 }
+                // tiles: C of chunk c+1 (G1(c), G3(c) done), B of chunk c+2 into B[kb]
+                // (G1(c), G4(c) done)
+                if (c + 1 < nchunks) {
+                    ok = wait_or_abort(s, &s.g4, c & 1);
+                    if (!ok) break;
+                    load_c(c + 1);
+                    if (c + 2 < nchunks) load_b(c + 2);
+                }
                 // G2(c): M(c) in TMEM (CB(c) consumed); onto G3(c) (factored) or fresh
                 ok = wait_or_abort(s, &s.mready, c & 1);
                 if (!ok) break;
                 tc_fence_after();
                 {
                     const bool fac = s.cv[c % kCv].factored != 0;
-                    const uint64_t dB = fac ? (kb ? dXS1 : dXS0) : dXR;
+                    const uint64_t dB = fac ? (kb ? dXS1 : dXS0) : (kb ? dXR1 : dXR0);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
                         mma_bf16_ts(tbase + kColY + 64 * kb, tbase + kColM + 8 * k, dB + 128 * k, kIdY,
@@ -395,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (c + 1 < nchunks) {
                     // G1(c+1): its tiles landed
-                    ok = wait_or_abort(s, &s.full_c[(c + 1) & 1], ((c + 1) >> 1) & 1) &&
+                    ok = wait_or_abort(s, &s.full_c, (c + 1) & 1) &&
                          wait_or_abort(s, &s.full_b[(c + 1) & 1], ((c + 1) >> 1) & 1);
                     if (!ok) break;
                     tc_fence_after();
@@ -403,25 +416,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = g3(c + 1);
                     if (!ok) break;
                 }
-                // tiles of chunk c+2 into buffers kb once G1(c), G3(c), G4(c) are done
-                if (c + 2 < nchunks) {
-                    ok = wait_or_abort(s, &s.g4, c & 1);
-                    if (!ok) break;
-                    load(c + 2);
-                    loaded = c + 3;
-                }
             }
             if (!ok) set_abort(s);
             // nothing of ours may be in flight when the CTA leaves (bounded waits)
             mma_commit(&s.fin);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_test(&s.fin, 0) && globaltimer_ns() - t0 < kWaitNs) __nanosleep(64);
-            for (int k = max(0, loaded - 2); k < loaded; ++k) {
-                while (!mbar_test(&s.full_c[k & 1], (k >> 1) & 1) && globaltimer_ns() - t0 < kWaitNs)
-                    __nanosleep(64);
+            if (loaded_c > 0) {
+                const int k = loaded_c - 1;
+                while (!mbar_test(&s.full_c, k & 1) && globaltimer_ns() - t0 < kWaitNs) __nanosleep(64);
+            }
+            for (int k = max(0, loaded_b - 2); k < loaded_b; ++k)
                 while (!mbar_test(&s.full_b[k & 1], (k >> 1) & 1) && globaltimer_ns() - t0 < kWaitNs)
                     __nanosleep(64);
-            }
         }
     } else if (warp == kGammaWarp) {
         // ===================== gamma: per-chunk row values (one warp) =====================
@@ -582,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (r >= rows) x0 = x1 = make_float2(0.f, 0.f);
                 const float2 sc2 = make_float2(scs[i], scs[i]);
                 const uint32_t off = chunk_off(r, jq >> 1) + coff;
-                if (need_x) at<uint2>(s.XR, off) = make_uint2(pack2(x0), pack2(x1));
+                if (need_x) at<uint2>(s.XR[c & 1], off) = make_uint2(pack2(x0), pack2(x1));
                 at<uint2>(s.XS[c & 1], off) = make_uint2(pack2(__fmul2_rn(sc2, x0)), pack2(__fmul2_rn(sc2, x1)));
             }
         };
@@ -710,12 +717,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&s.hsready);
 
-            // ---- conv(c+1): XS[(c+1)&1] was read by G4(c-1) and G2(c-1), which this
-            // thread saw done in the epilogue of chunk c-1; the one x-rows tile (exact
-            // chunks) was last read by G2(c) ----
+            // ---- conv(c+1): XS[(c+1)&1] and XR[(c+1)&1] were read by G4(c-1) and
+            // G2(c-1), which this thread saw done in the epilogue of chunk c-1 ----
             if (c + 1 < nchunks) {
                 if (ok) ok = wait_or_abort(s, &s.cvready[(c + 1) % kCv], ((c + 1) / kCv) & 1);
-                if (ok && s.cv[(c + 1) % kCv].factored == 0) ok = wait_or_abort(s, &s.g2, c & 1);
                 if (ok) conv(c + 1);
                 fence_proxy_async_smem();  // XR / XS are read by G4 / G2
                 mbar_arrive(&s.xready);
