@@ -52,6 +52,7 @@
 #include <cuda_fp16.h>
 
 #include <cstddef>
+#include <cstring>
 #include <mutex>
 
 namespace ssd {
@@ -104,13 +105,15 @@ struct __align__(1024) TcSmem {
     __nv_bfloat16 XS[2][Q * 64];    // scaled x rows [s][p] (SW128): v o x or w o x, by parity
     __nv_bfloat16 XR[2][Q * 64];    // x rows [s][p] (exact chunks), by parity
     __nv_bfloat16 Hs[N * 64];       // bf16 state rows [n][p] of the previous chunk: G3's B
+    __nv_bfloat16 Zt[Q * 64];       // z rows [t][p] of the epilogue's chunk (TMA, SW128)
+    __nv_bfloat16 Yt[Q * 64];       // y rows [t][p] on their way out (TMA store by 32-row
+                                    // quarters, SW128)
     ChunkVals cv[kCv];              // ring of per-chunk values
-    uint4 zs[2][kCompute];          // z of each compute thread's epilogue share (cp.async)
     // taps by [tap][channel pair] (front-padded with zeros): a thread reads its two
     // pairs of a tap as one 16-byte vector, a half-warp a contiguous 256 bytes
     alignas(16) float2 wconv[kMaxW][P / 2];
     alignas(16) float2 bconv[P / 2];
-    uint64_t full_c, full_b[2];     // TMA landed
+    uint64_t full_c, full_b[2], full_z;  // TMA landed
     uint64_t g1, g3, g4, g2, fin;   // MMA commits
     uint64_t xready, mready, hsready;                    // compute -> control
     uint64_t cvready[kCv], epidone[kCv];                 // gamma warp <-> compute
@@ -131,7 +134,7 @@ static_assert(sizeof(ChunkVals) % 16 == 0 && offsetof(TcSmem, cv) % 16 == 0, "fl
 static_assert(offsetof(ChunkVals, g2l) % 16 == 0 && offsetof(ChunkVals, dts) % 16 == 0, "float4");
 static_assert(offsetof(ChunkVals, sc) % 16 == 0 && offsetof(ChunkVals, dec) % 16 == 0, "float4");
 static_assert(offsetof(TcSmem, wconv) % 16 == 0 && offsetof(TcSmem, bconv) % 16 == 0, "float4");
-static_assert(offsetof(TcSmem, zs) % 16 == 0, "cp.async 16");
+static_assert(offsetof(TcSmem, Zt) % 1024 == 0 && offsetof(TcSmem, Yt) % 1024 == 0, "tile");
 static_assert(offsetof(TcSmem, full_c) % 8 == 0, "mbarriers");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
@@ -196,13 +199,6 @@ __device__ __forceinline__ uint2 ldg_u2(const __nv_bfloat16* p)
 }
 
 
-// 16-byte global -> shared copy that bypasses L1 and registers.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // byte offset of 16-byte chunk j of row r in a SW128 tile of 64-element rows.
 __device__ __forceinline__ uint32_t chunk_off(int r, int j)
@@ -244,7 +240,8 @@ __device__ __forceinline__ bool wait_or_abort(TcSmem& s, uint64_t* bar, uint32_t
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    scan_tc_kernel(const __grid_constant__ CUtensorMap map_bc, const TcScanParams p)
+    scan_tc_kernel(const __grid_constant__ CUtensorMap map_bc, const __grid_constant__ CUtensorMap map_z,
+                   const __grid_constant__ CUtensorMap map_y, const TcScanParams p)
 {
     // Align to the 1024-byte swizzle atom with pointer arithmetic on the
     // shared array itself, so the compiler keeps every access in the shared
@@ -261,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         mbar_init(&s.full_c, 1);
+        mbar_init(&s.full_z, 1);
         for (int i = 0; i < 2; ++i) mbar_init(&s.full_b[i], 1);
         mbar_init(&s.g1, 1);
         mbar_init(&s.g3, 1);
@@ -315,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             griddep_wait();
             const int xB = p.bc_col0 + g * N;          // first B column in the bc source
             const int xC = p.bc_col0 + G * N + g * N;  // first C column
-            int loaded_c = 0, loaded_b = 0;  // tiles requested so far
+            int loaded_c = 0, loaded_b = 0, loaded_z = 0;  // tiles requested so far
             auto load_c = [&](int c) {  // C tile of chunk c (the one buffer)
                 mbar_arrive_expect_tx(&s.full_c, 2 * Q * 64 * 2);
                 tma_load_3d(s.C[0], &map_bc, &s.full_c, xC, c * Q, b);
@@ -363,6 +361,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&s.g3);
                 return true;
             };
+            // z tile of chunk c (one buffer: the epilogue of chunk c-1 is done with it)
+            auto load_z = [&](int c) {
+                mbar_arrive_expect_tx(&s.full_z, Q * 64 * 2);
+                tma_load_3d(s.Zt, &map_z, &s.full_z, h * P, c * Q, b);
+                loaded_z = c + 1;
+            };
+            if (has_z) {
+                prefetch_tmap(&map_z);
+                load_z(0);
+            }
             load_c(0);
             load_b(0);
             if (nchunks > 1) load_b(1);
@@ -392,6 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     load_c(c + 1);
                     if (c + 2 < nchunks) load_b(c + 2);
+                }
+                // z of chunk c once the epilogue of chunk c-1 is done (it comes before
+                // the mask of chunk c, so this does not hold up G2(c))
+                if (has_z && c > 0) {
+                    ok = wait_or_abort(s, &s.epidone[(c - 1) % kCv], ((c - 1) / kCv) & 1);
+                    if (!ok) break;
+                    load_z(c);
                 }
                 // G2(c): M(c) in TMEM (CB(c) consumed); onto G3(c) (factored) or fresh
                 ok = wait_or_abort(s, &s.mready, c & 1);
@@ -429,6 +444,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = max(0, loaded_b - 2); k < loaded_b; ++k)
                 while (!mbar_test(&s.full_b[k & 1], (k >> 1) & 1) && globaltimer_ns() - t0 < kWaitNs)
                     __nanosleep(64);
+            if (loaded_z > 0) {  // z tiles are requested in order, each after the last was used
+                const int k = loaded_z - 1;
+                while (!mbar_test(&s.full_z, k & 1) && globaltimer_ns() - t0 < kWaitNs) __nanosleep(64);
+            }
         }
     } else if (warp == kGammaWarp) {
         // ===================== gamma: per-chunk row values (one warp) =====================
@@ -606,19 +625,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             at<uint4>(s.Hs, chunk_off(t, 2 * j + 1)) = pack4x2(&hreg[4]);
         };
 
-        // z of the epilogue's row and columns, one chunk ahead, copied into this
-        // thread's own slot of shared memory (no registers held meanwhile)
-        const __nv_bfloat16* zbase = static_cast<const __nv_bfloat16*>(p.z);
-        auto load_z = [&](int c) {
-            if (!has_z) return;
-            const int rows = min(Q, S - c * Q);
-            const __nv_bfloat16* zr =
-                zbase + ((size_t)b * S + c * Q + min(t, rows - 1)) * (H * P) + h * P + 16 * j;
-            cp_async16(&s.zs[0][tid], zr);
-            cp_async16(&s.zs[1][tid], zr + 8);
-            cp_async_commit();
-        };
-
         // prologue: h of chunk -1 in the state tile; M's blocks above the
         // diagonal (they stay zero); conv of chunk 0
         store_h();
@@ -638,7 +644,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();  // XR / XS are read by G4 / G2
             mbar_arrive(&s.xready);
             if (nchunks > 1) load_raw(1);
-            load_z(0);
         }
 
         for (int c = 0; c < nchunks; ++c) {
@@ -727,16 +732,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (c + 2 < nchunks) load_raw(c + 2);
             }
 
-            // ---- epilogue(c): factored y = u Y; exact y = Y + u Yo; times silu(z) ----
+            // ---- epilogue(c): factored y = u Y; exact y = Y + u Yo; times silu(z).
+            // z comes from its TMA tile; y goes to the staging tile, and each quarter's
+            // 32 rows leave with one TMA store (rows past the end are not written).
+            // The staging tile's last store finished reading it before its issuer's
+            // mask(c) arrival, which G2(c), waited on below, comes after. ----
             if (ok) ok = wait_or_abort(s, &s.g2, c & 1);
+            if (ok && has_z) ok = wait_or_abort(s, &s.full_z, c & 1);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
                 const bool fac = cv.factored != 0;
                 const float dec = cv.dec[t];
                 const float2 dd = make_float2(dec, dec);
-                if (has_z) cp_async_wait_all();  // this thread's z copy of chunk c
-                uint4* yrow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) +
-                                                       (((size_t)b * S + c * Q + t) * H + h) * P + 16 * j);
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {  // 8 columns at a time
                     float yv[8];
@@ -762,22 +769,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     float2 out[4], zv[4];
-                    if (has_z) unpack4x2(s.zs[hh][tid], zv);
+                    const uint32_t off = chunk_off(t, 2 * j + hh);  // row t, 8 columns (SW128)
+                    if (has_z) unpack4x2(at<uint4>(s.Zt, off), zv);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         float2 v = make_float2(yv[2 * e], yv[2 * e + 1]);
                         if (has_z) v = __fmul2_rn(v, silu2(zv[e]));
                         out[e] = v;
                     }
-                    if (t < rows) yrow[hh] = pack4x2(out);
+                    at<uint4>(s.Yt, off) = pack4x2(out);
                 }
             } else {
                 ok = false;
             }
+            fence_proxy_async_smem();   // the staging tile is read by the TMA store
             tc_fence_before();
             mbar_arrive(&s.epidone[c % kCv]);
-            if (c + 1 < nchunks) load_z(c + 1);
+            named_bar_sync(1 + q, 128);  // the quarter's four warps
+            if (j == 0 && lane == 0 && ok && c * Q + 32 * q < S) {  // a quarter with rows left
+                tma_store_3d(&map_y, reinterpret_cast<const char*>(s.Yt) + q * 32 * 128, h * P,
+                             c * Q + 32 * q, b);
+                bulk_commit();
+                bulk_wait_read_all();
+            }
         }
+        if (j == 0 && lane == 0) bulk_wait_all();  // y of the last chunks written
         if (!ok) {
             set_abort(s);
         } else if (!aborted(s)) {
@@ -838,12 +854,12 @@ bool encode_fn()
     return g_encode != nullptr;
 }
 
-// 3-D map over rows of `cols` bf16: dims {cols, S, B}, box {64, 128, 1}, SW128.
-bool make_map(CUtensorMap* m, const void* base, int cols, int S, int B)
+// 3-D map over rows of `cols` bf16: dims {cols, S, B}, box {64, box_rows, 1}, SW128.
+bool make_map(CUtensorMap* m, const void* base, int cols, int S, int B, int box_rows = Q)
 {
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)S, (cuuint64_t)B};
     cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * 2 * (cuuint64_t)S};
-    cuuint32_t box[3] = {64, (cuuint32_t)Q, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -859,8 +875,12 @@ cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st, bool after_pr
 {
     if (p.B == 0 || p.S == 0) return cudaSuccess;
     if (p.W > kMaxW || !encode_fn()) return cudaErrorNotSupported;
-    CUtensorMap mbc;
+    CUtensorMap mbc, mz, my;
     if (!make_map(&mbc, p.bc, p.bc_stride, p.S, p.B)) return cudaErrorInvalidValue;
+    // z tiles in (128 rows), y leaves in 32-row quarters; both [B, S, H*P]
+    memset(&mz, 0, sizeof(mz));
+    if ((p.flags & kHasZ) && !make_map(&mz, p.z, p.H * P, p.S, p.B)) return cudaErrorInvalidValue;
+    if (!make_map(&my, p.y, p.H * P, p.S, p.B, 32)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -874,7 +894,7 @@ cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st, bool after_pr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = after_prepass ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, scan_tc_kernel, mbc, p);
+    return cudaLaunchKernelEx(&cfg, scan_tc_kernel, mbc, mz, my, p);
 }
 
 }  // namespace ssd
