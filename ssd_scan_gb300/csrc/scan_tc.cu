@@ -31,20 +31,28 @@
 // back into TMEM (bf16 pairs) and read from there by G2, so it never passes
 // through shared memory.
 //
-// Threads: 16 compute warps and one control warp.  The compute warps all run
-// the same phases on every chunk, each warp on its own share: the x conv and
-// scaling (4 rows x 4 channels per thread), the mask (one 32-column block of
-// a TMEM lane quarter per warp), the state update and the epilogue (16
-// columns of a lane quarter per warp; TMEM lane quarter = warp % 4), and, for
-// warps 0-3, the per-chunk values of the next chunk (double-float cumulative
-// sum of a).  They run in lock step phase by phase -- so one instruction
-// stream per SM sub-partition at a time, which keeps the instruction caches
-// warm -- and hand work to the tensor cores through mbarriers.  The control
-// warp's one active thread issues every TMA load and every MMA as the compute
-// phases complete: G4 and G3 of a chunk run under its mask phase, G2 under
-// its state update, G1 of the next chunk under its epilogue and the next
-// chunk's conv.  Every wait is bounded in time; a wait that runs out aborts
-// the CTA (the other waits then fail fast) and sets the device error word.
+// Threads (576): 16 compute warps, a control warp and a gamma warp.
+//  - gamma warp: for up to four chunks ahead, dt (softplus + bias), the
+//    double-float cumulative sum of a = dt A, the form of the chunk and the
+//    per-row factors, into a ring of per-chunk value sets in shared memory.
+//  - control warp (one thread): every TMA load (the C tile of the next chunk
+//    into the one C buffer once G4 of this chunk -- and so G1, G3, issued
+//    before it -- is done; B tiles two chunks ahead, double-buffered; the z
+//    tile of a chunk once the epilogue before it is done) and every MMA, each
+//    as soon as its operands are ready (mbarriers from the compute warps).
+//  - compute warps, phase by phase on every chunk: mask (one 32x32 block of a
+//    TMEM lane quarter per warp, warp % 4 = quarter), state update (16 state
+//    columns per warp, h in fp32 registers, its bf16 copy into shared memory
+//    for G3), conv of the next chunk (4 rows x 4 channels per thread: causal
+//    taps over raw rows prefetched a chunk ahead in registers, SiLU, the x and
+//    scaled-x tiles), epilogue (16 columns of a lane quarter per warp: z from
+//    its TMA tile, y through a staging tile that each quarter stores with one
+//    TMA store).  At the end they write the final state and the new conv state.
+// Per-thread global accesses that would scatter a warp over 32 rows (z, y)
+// go through TMA tiles instead: the load/store unit would otherwise spend 32
+// requests on every such instruction.  Every wait is bounded in time; a wait
+// that runs out aborts the CTA (the other waits then fail fast) and sets the
+// device error word.
 #include "internal.cuh"
 #include "sm100.cuh"
 
