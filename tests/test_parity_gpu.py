@@ -152,6 +152,58 @@ def test_prefill_137_rows_full_heads_sampled():
 
 
 # ---------------------------------------------------------------------------
+# the other workloads at full size, in the calls the benchmark makes; the
+# oracle checks sampled (sequence, head) pairs.  Inputs are drawn on the GPU
+# and only the sampled sequences are copied to the host.
+
+def _device_problem(shape, seed, stress=False):
+    prm = si.params(shape, seed=seed, stress=stress)
+    inp = si.prefill_inputs(shape, seed=seed, device="cuda", stress=stress)
+    dev = {**{k: v.cuda() for k, v in prm.items()}, **inp}
+    return prm, inp, dev
+
+
+def _host_subset(prm, inp, batches):
+    sub = {k: (v[batches].cpu() if v is not None else None) for k, v in inp.items()}
+    return {**prm, **sub}
+
+
+def test_long_prefill_full_size_chained_sampled():
+    """8 sequences x 8192 rows, then a second 8192-row call fed with the first
+    call's final states, on all 128 heads; the oracle checks two sequences x two
+    heads over all 16384 rows."""
+    shape = si.LONG.with_(seqlen=2 * si.LONG.seqlen)
+    prm, inp, dev = _device_problem(shape, seed=11)
+    y, h, cs = gpu_prefill(shape, dev, [si.LONG.seqlen, si.LONG.seqlen])
+    assert torch.isfinite(y.float()).all() and torch.isfinite(h).all()
+    bb = [0, 7]
+    cpu = _host_subset(prm, inp, bb)
+    del inp, dev
+    _check_prefill(shape.with_(batch=len(bb)), cpu, y[bb], h[bb], cs[bb], torch.bfloat16,
+                   heads=[5, 98])
+
+
+def test_decay_stress_full_size_sampled():
+    """4 sequences x 4096 rows with decays up to ~1e4 per row, fed as calls of
+    U{1..128} rows: finite everywhere, and two heads of every sequence checked."""
+    shape = si.STRESS
+    prm, inp, dev = _device_problem(shape, seed=13, stress=True)
+    y, h, cs = gpu_prefill(shape, dev, si.random_splits(shape.seqlen, seed=13))
+    assert torch.isfinite(y.float()).all() and torch.isfinite(h).all()
+    cpu = _host_subset(prm, inp, list(range(shape.batch)))
+    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16, heads=[2, 121])
+
+
+def test_prefill_eight_heads_per_group():
+    """The 30B-A3B mixer shape: 64 heads of 64 in 8 groups of state size 128
+    (8 heads per group), bf16, over two calls."""
+    shape = si.Shape(batch=2, seqlen=300, nheads=64, headdim=64, dstate=128, ngroups=8)
+    cpu, dev = make_problem(shape, act=torch.bfloat16, seed=17)
+    y, h, cs = gpu_prefill(shape, dev, [200, 100])
+    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16, heads=[0, 7, 8, 33, 63])
+
+
+# ---------------------------------------------------------------------------
 # which kernels ran (launch counters), and the paths around the tensor cores
 
 def _counts():
