@@ -19,6 +19,8 @@ Functions (each cites the passage it follows in ``ssd_oracle.c``):
   #1362 summary; TensorSharp "nemotron.md" section 11).
 * :func:`mixer_prefill` / :func:`mixer_decode` -- the compositions that the
   C-ABI calls ``ssd_chunk_scan`` / ``ssd_decode_step`` compute.
+* :func:`gated_group_rmsnorm` -- group RMSNorm of y, then the SiLU(z) gate
+  (TensorSharp "nemotron.md" sections 3, 4.1 and 6).
 
 Parity unpinned: none (see tests/test_oracle.py for the pins).
 """
@@ -75,6 +77,9 @@ def open_library(path: str):
     for name in ("oracle_ssd_sequential", "oracle_ssd_chunked"):
         getattr(lib, name).restype = ctypes.c_int
     lib.oracle_decode_step.restype = ctypes.c_int
+    lib.oracle_gated_group_rmsnorm.restype = None
+    lib.oracle_gated_group_rmsnorm.argtypes = [ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_double] + [dp] * 4
     return lib
 
 
@@ -227,3 +232,19 @@ def mixer_decode(xbc_raw, conv_w, dt_raw, A, slot_ids, ssm_pool, *, H, P, N, G,
     if rc != 0:
         raise ValueError("oracle decode: slot id out of range")
     return y, pool, cp
+
+
+def gated_group_rmsnorm(y, z, w, eps, G):
+    """out = silu(z) * y / sqrt(mean over the group of y^2 + eps) * w, with G
+    groups of contiguous channels on the last axis (TensorSharp "nemotron.md"
+    sections 3, 4.1, 6).  y, z [..., C]; w [C].  Returns out [..., C]."""
+    y = _f64(y)
+    z = _f64(z)
+    w = _f64(w)
+    C = y.shape[-1]
+    assert z.shape == y.shape and w.shape == (C,) and C % G == 0
+    out = np.empty_like(y)
+    rows = y.size // C
+    _load().oracle_gated_group_rmsnorm(rows, C, G, float(eps), _dp(y), _dp(z), _dp(w), _dp(out))
+    return out
+

@@ -40,7 +40,10 @@
  *  - conv tap k = W-1 multiplies the newest row; conv state holds the W-1
  *    most recent raw rows, oldest first.
  *  - y uses the post-update state (state first, then y = state.C).
- *  - z gate is y * silu(z) (the group RMSNorm is a separate step).
+ *  - z gate is y * silu(z) (the group RMSNorm is a separate step, below).
+ *  - group RMSNorm then gate: out = silu(z) * y / sqrt(mean_group(y^2) + eps)
+ *    * w, in that order ([TS] 4.1: the norm acts on y, then the gate); eps is
+ *    not on the pages and is an argument.
  *
  * Parity unpinned: none of the functions below (each has at least one pin in
  * the CPU test-suite that does not re-type its formula).
@@ -398,4 +401,41 @@ int oracle_decode_step(int R, int H, int P, int N, int G, unsigned flags,
     }
     free(h0); free(h1);
     return rc;
+}
+
+/*
+ * Group RMSNorm of y, then the SiLU gate.  [TS] section 3 (Mamba2 branch:
+ * out = SiLU(z) * GroupRMSNorm(y), ssm_norm.weight), section 4.1 (the group
+ * norm normalises y per group before the gate SiLU(z) multiplies), section 6
+ * (ssm_norm.weight, one weight per channel of dInner).  rows x C values;
+ * group g holds the C / G contiguous channels g*C/G .. (g+1)*C/G - 1.
+ *
+ *   ms_g     = (1 / (C/G)) * sum_{c in g} y[r,c]^2
+ *   out[r,c] = silu(z[r,c]) * (y[r,c] / sqrt(ms_g + eps)) * w[c]
+ */
+void oracle_gated_group_rmsnorm(long rows, int C, int G, double eps, const double* y,
+                                const double* z, const double* w, double* out)
+{
+    const int gs = C / G;
+    for (long r = 0; r < rows; ++r) {
+        const double* yr = y + (size_t)r * C;
+        const double* zr = z + (size_t)r * C;
+        double* o = out + (size_t)r * C;
+        for (int g = 0; g < G; ++g) {
+            /* mutant 7: one norm over the whole row instead of per group */
+            const int c0 = ORACLE_MUTANT == 7 ? 0 : g * gs;
+            const int n = ORACLE_MUTANT == 7 ? C : gs;
+            double ss = 0.0;
+            for (int c = c0; c < c0 + n; ++c) {
+                double v = yr[c];
+                if (ORACLE_MUTANT == 9) v *= oracle_silu(zr[c]); /* gate before the norm */
+                ss += v * v;
+            }
+            const double ms = ss / n;
+            /* mutant 8: eps added outside the square root */
+            const double inv = ORACLE_MUTANT == 8 ? 1.0 / (sqrt(ms) + eps) : 1.0 / sqrt(ms + eps);
+            for (int c = g * gs; c < (g + 1) * gs; ++c)
+                o[c] = oracle_silu(zr[c]) * (yr[c] * inv) * w[c];
+        }
+    }
 }

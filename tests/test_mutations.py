@@ -5,7 +5,9 @@ pins of tests/test_oracle.py then run against each copy.  Mutant 1 is the
 clamped group index min(h / heads_per_group, 1) that vllm.cpp #1362 uses as its
 own mutation; mutant 3 is the dropped chunk carry; the others are a reversed
 conv tap order, y read from the pre-update state, a dropped dt bias and a
-flipped decay sign in the chunk form.
+flipped decay sign in the chunk form; mutants 7-9 are in the gated group
+RMSNorm: one norm over the whole row, eps outside the square root, and the
+gate applied before the norm.
 """
 import pytest
 
@@ -26,10 +28,13 @@ PINS = [
     pins.test_conv_impulse_returns_reversed_taps,
     pins.test_linearity_in_x_and_h0,
     pins.test_decode_steps_equal_sequential_rows,
+    pins.test_rmsnorm_constant_group_hand_value,
+    pins.test_rmsnorm_groups_are_independent,
+    pins.test_rmsnorm_gate_acts_after_the_norm,
 ]
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9])
 def test_pins_catch_mutant(mutant, tmp_path, monkeypatch):
     lib = oracle.open_library(oracle.build(out_path=str(tmp_path / f"m{mutant}.so"),
                                            mutant=mutant))

@@ -347,3 +347,72 @@ def test_decode_rejects_out_of_range_slot():
     assert rc == -1
     assert not np.array_equal(pool2[1], pool[1])  # the valid row still ran
     assert np.array_equal(pool2[0], pool[0])
+
+
+# --------------------------------------------------------------------------
+# group RMSNorm then SiLU gate (TensorSharp "nemotron.md" sections 3, 4.1, 6)
+
+def _norm_inputs(rows=5, C=24, seed=0):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((rows, C)), rng.standard_normal((rows, C)), \
+        rng.uniform(0.5, 1.5, C)
+
+
+def test_rmsnorm_constant_group_hand_value():
+    """A group of equal values a: the norm gives a / sqrt(a^2 + eps); with
+    a = 0.003 and eps = 0.000016, a^2 + eps = 0.000025 and the norm is 0.6."""
+    from scipy.special import expit
+    C, G = 8, 2
+    y = np.concatenate([np.full(4, 0.003), np.full(4, -2.0)])[None, :]
+    z = np.linspace(-1.5, 2.0, C)[None, :]
+    w = np.linspace(0.5, 1.25, C)
+    out = oracle.gated_group_rmsnorm(y, z, w, 0.000016, G)
+    silu = z * expit(z)
+    assert np.allclose(out[0, :4], 0.6 * silu[0, :4] * w[:4], rtol=1e-12, atol=0)
+    # the second group: -2 / sqrt(4 + 0.000016) = -1 / sqrt(1 + 0.000004)
+    assert np.allclose(out[0, 4:], -silu[0, 4:] * w[4:] / math.sqrt(1.000004), rtol=1e-12,
+                       atol=0)
+
+
+def test_rmsnorm_scale_invariance():
+    """With eps = 0 the norm ignores the scale of y and is odd in y."""
+    y, z, w = _norm_inputs()
+    base = oracle.gated_group_rmsnorm(y, z, w, 0.0, 3)
+    assert np.allclose(oracle.gated_group_rmsnorm(3.7 * y, z, w, 0.0, 3), base, rtol=1e-13)
+    assert np.array_equal(oracle.gated_group_rmsnorm(-y, z, w, 0.0, 3), -base)
+
+
+def test_rmsnorm_unit_rms_when_gate_is_one():
+    """silu(50) = 50 to within 1e-20, so with w = 1/50 and eps = 0 every group
+    of the output has root-mean-square 1."""
+    y, _, _ = _norm_inputs(rows=4, C=32)
+    out = oracle.gated_group_rmsnorm(y, np.full_like(y, 50.0), np.full(32, 1.0 / 50.0), 0.0, 4)
+    rms = np.sqrt(np.mean(out.reshape(4, 4, 8) ** 2, axis=2))
+    assert np.allclose(rms, 1.0, rtol=1e-13)
+
+
+def test_rmsnorm_groups_are_independent():
+    """Changing y in one group leaves every other group's output unchanged."""
+    y, z, w = _norm_inputs()
+    base = oracle.gated_group_rmsnorm(y, z, w, 1e-5, 3)
+    y2 = y.copy()
+    y2[:, 8:16] *= 5.0
+    y2[:, 9] += 1.0
+    out = oracle.gated_group_rmsnorm(y2, z, w, 1e-5, 3)
+    assert np.array_equal(out[:, :8], base[:, :8]) and np.array_equal(out[:, 16:], base[:, 16:])
+    assert not np.array_equal(out[:, 8:16], base[:, 8:16])
+
+
+def test_rmsnorm_gate_acts_after_the_norm():
+    """The norm is taken over y alone, so a change of z in one channel changes
+    that channel's output only (and by the ratio of the two silu values)."""
+    from scipy.special import expit
+    y, z, w = _norm_inputs()
+    base = oracle.gated_group_rmsnorm(y, z, w, 1e-5, 3)
+    z2 = z.copy()
+    z2[:, 5] = 2.5
+    out = oracle.gated_group_rmsnorm(y, z2, w, 1e-5, 3)
+    others = [c for c in range(24) if c != 5]
+    assert np.array_equal(out[:, others], base[:, others])
+    ratio = (2.5 * expit(2.5)) / (z[:, 5] * expit(z[:, 5]))
+    assert np.allclose(out[:, 5], base[:, 5] * ratio, rtol=1e-12)
