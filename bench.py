@@ -398,7 +398,8 @@ def bench_extra(ssd, dev, stream, args):
     """The other prefill workloads, timed like the headline one: long (8
     sequences x 8192 rows, then a chained second call of 8192 rows each) and
     decay stress (4 x 4096 rows with decays up to ~1e4 per row, fed as calls of
-    U{1..128} rows).  Tokens/s over all calls of one pass."""
+    U{1..128} rows), tokens/s over all calls of one pass; and the gated group
+    RMSNorm at the prefill width, GB/s against the HBM peak."""
     out = {}
     for name, shape, splits, stress in (
             ("long_8x8192_plus_8192", si.LONG.with_(seqlen=2 * si.LONG.seqlen),
@@ -428,6 +429,36 @@ def bench_extra(ssd, dev, stream, args):
                      "calls_per_pass": ncalls, "rows_per_pass": rows,
                      "host_ms_per_pass": round(min(host_s) * 1e3, 3)}
         del inp, run
+    # the gated group RMSNorm after the scan, at the prefill width (2048 rows x
+    # 8192 channels, 8 groups): HBM-bound, y and z read, out written once
+    sh = si.PREFILL
+    C = sh.nheads * sh.headdim
+    g = torch.Generator(device=dev).manual_seed(21)
+    sets = [(torch.randn((1, sh.seqlen, C), generator=g, device=dev).to(torch.bfloat16),
+             torch.randn((1, sh.seqlen, C), generator=g, device=dev).to(torch.bfloat16),
+             torch.empty((1, sh.seqlen, C), dtype=torch.bfloat16, device=dev)) for _ in range(3)]
+    w = torch.rand((C,), generator=g, device=dev) + 0.5
+    d = ssd.dims(1, sh.seqlen, sh.nheads, sh.headdim, sh.dstate, sh.ngroups)
+    for i in range(6):
+        y, z, o = sets[i % 3]
+        ssd.ssd_gated_group_rmsnorm(d, ssd.SSD_BF16, y, z, w, 1e-5, o, stream)
+    torch.cuda.synchronize()
+    steps = 30
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    queue_ahead(30e-6, steps)
+    ev0.record(stream)
+    for i in range(steps):
+        y, z, o = sets[i % 3]
+        ssd.ssd_gated_group_rmsnorm(d, ssd.SSD_BF16, y, z, w, 1e-5, o, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    nbytes = 3 * sh.seqlen * C * 2 + C * 4
+    hbm, _ = measured_peaks()
+    out["gated_group_rmsnorm_2048x8192"] = {
+        "us_per_call": round(ms * 1e3, 2), "bytes_per_call": nbytes,
+        "gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+        "frac_of_hbm": round(nbytes / (ms / 1e3) / 1e9 / hbm, 4)}
     assert ssd.ssd_read_device_error(stream) == ssd.SSD_OK
     return out
 

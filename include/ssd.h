@@ -7,6 +7,8 @@
  *                    the conv fused in front), with carried conv/SSM state
  *   ssd_decode_step  one recurrent step for R rows at slot-indexed states,
  *                    updated in place
+ * and ssd_gated_group_rmsnorm, the group RMSNorm + SiLU(z) gate that follows
+ * the scan in the mixer.
  *
  * Sources (page title, section):
  *   TensorRT-Model-Connect PR #2207 "perf(nemotron_h): prefill single-GPU
@@ -43,8 +45,9 @@
  *     W-1 most recent raw (pre-conv) rows, oldest first, in the activation
  *     dtype.
  *   - The SSM state is always fp32, layout [.., H, P, N] (N fastest).
- *   - With SSD_HAS_Z, y is multiplied by silu(z) (the gate of the gated norm;
- *     the group RMSNorm itself is not part of these calls).
+ *   - With SSD_HAS_Z, y is multiplied by silu(z) (the gate alone).  For the
+ *     mixer's gated group RMSNorm, run the scan without SSD_HAS_Z and then
+ *     ssd_gated_group_rmsnorm.
  */
 #ifndef SSD_GB300_SSD_H
 #define SSD_GB300_SSD_H
@@ -236,6 +239,31 @@ SSD_API ssd_status ssd_decode_step(const ssd_dims* dims, ssd_dtype act, unsigned
                            cudaStream_t stream);
 
 /*
+ * ssd_gated_group_rmsnorm -- group RMSNorm of y, then the SiLU(z) gate.
+ * (TensorSharp nemotron.md section 3, Mamba2 branch:
+ *  out = SiLU(z) * GroupRMSNorm(y, ssm_norm.weight); section 4.1: the group
+ *  norm normalises y per group before the gate multiplies; section 6:
+ *  ssm_norm.weight, one weight per channel of dInner = H*P.)
+ *
+ * For each of the B*S rows and each of the G = dims->ngroups groups of
+ * gs = H*P/G contiguous channels:
+ *   out[r,c] = silu(z[r,c]) * y[r,c] / sqrt(mean_{c' in group} y[r,c']^2 + eps)
+ *              * weight[c]
+ *
+ * y       [B,S,H*P] act: the scan output computed WITHOUT SSD_HAS_Z
+ * z       [B,S,H*P] act
+ * weight  [H*P] fp32
+ * eps     finite, >= 0 (the pages give no value; 1e-5 is the usual one)
+ * out     [B,S,H*P] act; may alias y exactly (in place), no other overlap
+ * Only batch, seqlen, nheads, headdim and ngroups of `dims` are used.  gs must
+ * be a multiple of 8 (bf16) or 4 (fp32) channels, else SSD_ERR_UNSUPPORTED.
+ * Rows are independent; S = 0 launches nothing.
+ */
+SSD_API ssd_status ssd_gated_group_rmsnorm(const ssd_dims* dims, ssd_dtype act, const void* y,
+                                           const void* z, const float* weight, float eps,
+                                           void* out, cudaStream_t stream);
+
+/*
  * Kernel-launch counters, for observability (which path ran, how many
  * kernels a call launched).  Host-side, process-wide, monotonically
  * increasing; one counter per kernel kind below.  Copies min(n,
@@ -249,7 +277,8 @@ enum {
     SSD_KERNEL_BC_CONV = 4,        /* conv of the B|C columns for the scan  */
     SSD_KERNEL_DECODE_STEP = 5,    /* slot-indexed decode step              */
     SSD_KERNEL_DECODE_CONV = 6,    /* conv-pool roll of the decode step     */
-    SSD_KERNEL_KINDS = 7
+    SSD_KERNEL_GATED_NORM = 7,     /* group RMSNorm + SiLU(z) gate          */
+    SSD_KERNEL_KINDS = 8
 };
 SSD_API int ssd_launch_counts(uint64_t* out, int n);
 

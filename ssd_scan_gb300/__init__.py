@@ -37,10 +37,10 @@ SSD_STATIC_SCRATCH_BYTES = 16 << 20
 # every symbol include/ssd.h declares
 EXPORTED = ("ssd_conv1d_rows", "ssd_chunk_scan", "ssd_chunk_scan_workspace_size",
             "ssd_decode_step", "ssd_status_string", "ssd_read_device_error",
-            "ssd_launch_counts", "ssd_chunk_scan_static_ws")
+            "ssd_launch_counts", "ssd_chunk_scan_static_ws", "ssd_gated_group_rmsnorm")
 
 KERNEL_KINDS = ("conv_rows", "conv_state", "scan_simt", "scan_tc", "bc_conv", "decode_step",
-                "decode_conv")
+                "decode_conv", "gated_norm")
 
 
 class SsdError(RuntimeError):
@@ -84,6 +84,8 @@ def load_library():
             lib.ssd_chunk_scan_static_ws.argtypes = [P, ci, cu] + [_vp] * 13 + [_vp]
             lib.ssd_chunk_scan_workspace_size.argtypes = [P, ci, cu, ci, ctypes.POINTER(sz)]
             lib.ssd_decode_step.argtypes = [P, ci, cu] + [_vp] * 10 + [ci, _vp, _vp, _vp]
+            lib.ssd_gated_group_rmsnorm.argtypes = [P, ci, _vp, _vp, _vp, ctypes.c_float, _vp,
+                                                     _vp]
             lib.ssd_status_string.argtypes = [ci]
             lib.ssd_status_string.restype = ctypes.c_char_p
             lib.ssd_read_device_error.argtypes = [_vp]
@@ -203,6 +205,17 @@ def ssd_decode_step(d: ssd_dims, act: int, flags: int, xbc, conv_w, conv_b, conv
         _ptr(ssm_pool, f, "ssm_pool"), _ptr(y, a, "y"), _stream(stream)), "ssd_decode_step")
 
 
+def ssd_gated_group_rmsnorm(d: ssd_dims, act: int, y, z, weight, eps: float, out,
+                            stream=None) -> None:
+    """out = silu(z) * GroupRMSNorm(y; weight, eps), d.ngroups groups of the
+    H*P channels of each row; out may be y itself."""
+    a = _ACT[act]
+    _check(load_library().ssd_gated_group_rmsnorm(
+        ctypes.byref(d), act, _ptr(y, a, "y"), _ptr(z, a, "z"),
+        _ptr(weight, torch.float32, "weight"), ctypes.c_float(eps), _ptr(out, a, "out"),
+        _stream(stream)), "ssd_gated_group_rmsnorm")
+
+
 def ssd_launch_counts() -> dict:
     """Process-wide number of kernels the library launched, per kernel kind."""
     buf = (ctypes.c_uint64 * len(KERNEL_KINDS))()
@@ -248,3 +261,18 @@ def chunk_scan(xbc, dt, A, *, nheads, headdim, dstate, ngroups, conv_w=None, con
     ssd_chunk_scan(d, act, flags, xbc, conv_w, conv_b, conv_state, cs, dt, dt_bias, A, D, z,
                    ssm_state, y, hs, workspace, stream)
     return y, hs, cs
+
+
+def gated_group_rmsnorm(y, z, weight, *, ngroups, eps=1e-5, out=None, stream=None):
+    """Group RMSNorm of y [B,S,H,P] (or [B,S,H*P]) then the SiLU(z) gate, z
+    [B,S,H*P]; returns out shaped like y (a new tensor unless ``out`` is given,
+    which may be y itself)."""
+    B, S = y.shape[0], y.shape[1]
+    C = weight.numel()
+    if C % ngroups:
+        raise ValueError(f"{C} channels do not split into {ngroups} groups")
+    d = dims(B, S, ngroups, C // ngroups, 1, ngroups)  # channels as ngroups heads of C/ngroups
+    o = torch.empty_like(y) if out is None else out
+    ssd_gated_group_rmsnorm(d, act_of(y), y, z, weight, eps, o, stream)
+    return o
+

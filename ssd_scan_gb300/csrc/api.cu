@@ -281,4 +281,35 @@ ssd_status ssd_decode_step(const ssd_dims* dims, ssd_dtype act, unsigned flags, 
                    conv_w != nullptr && dims->conv_width > 1);
 }
 
+ssd_status ssd_gated_group_rmsnorm(const ssd_dims* dims, ssd_dtype act, const void* y,
+                                   const void* z, const float* weight, float eps, void* out,
+                                   cudaStream_t stream)
+{
+    if (dims == nullptr || (act != SSD_F32 && act != SSD_BF16)) return SSD_ERR_INVALID_ARG;
+    if (dims->batch < 0 || dims->seqlen < 0 || dims->nheads <= 0 || dims->headdim <= 0 ||
+        dims->ngroups <= 0 || dims->nheads % dims->ngroups != 0)
+        return SSD_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || eps > 3.4e38f) return SSD_ERR_INVALID_ARG;  // rejects NaN and inf
+    const long long C = (long long)dims->nheads * dims->headdim;
+    const long long rows = (long long)dims->batch * dims->seqlen;
+    const bool bf16 = act == SSD_BF16;
+    if (C > (1LL << 30)) return SSD_ERR_INVALID_ARG;
+    if (!gated_norm_supports((int)C, dims->ngroups, bf16)) return SSD_ERR_UNSUPPORTED;
+    if (weight == nullptr || !aligned16(weight)) return SSD_ERR_INVALID_ARG;
+    if (rows > 0 && (y == nullptr || z == nullptr || out == nullptr || !aligned16(y) ||
+                     !aligned16(z) || !aligned16(out)))
+        return SSD_ERR_INVALID_ARG;
+    if (rows == 0) return SSD_OK;
+    // out may be y itself, but no other overlap with y or z
+    const size_t bytes = (size_t)rows * C * (bf16 ? 2 : 4);
+    auto overlaps = [&](const void* a, const void* b) {
+        const char* pa = static_cast<const char*>(a);
+        const char* pb = static_cast<const char*>(b);
+        return pa < pb + bytes && pb < pa + bytes;
+    };
+    if ((out != y && overlaps(out, y)) || overlaps(out, z)) return SSD_ERR_INVALID_ARG;
+    GatedNormParams p{rows, (int)C, dims->ngroups, eps, y, z, weight, out};
+    return counted(launch_gated_norm(p, bf16, stream), SSD_KERNEL_GATED_NORM);
+}
+
 }  // extern "C"

@@ -117,6 +117,18 @@ cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st, bool after_pr
 
 bool decode_supports(int H, int P, int N, int G);
 cudaError_t launch_decode_step(const DecodeParams& p, bool bf16, cudaStream_t st);
+
+struct GatedNormParams {
+    long long rows;   // B*S
+    int C, G;         // channels per row (H*P), groups
+    float eps;
+    const void* y;    // [rows, C] act
+    const void* z;    // [rows, C] act
+    const float* w;   // [C]
+    void* out;        // [rows, C] act, may alias y
+};
+bool gated_norm_supports(int C, int G, bool bf16);
+cudaError_t launch_gated_norm(const GatedNormParams& p, bool bf16, cudaStream_t st);
 cudaError_t launch_decode_conv_roll(const DecodeParams& p, bool bf16, cudaStream_t st);
 
 }  // namespace ssd

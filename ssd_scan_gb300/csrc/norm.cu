@@ -1,0 +1,128 @@
+// norm.cu -- group RMSNorm of the scan output y, then the SiLU(z) gate.
+//
+// TensorSharp nemotron.md section 3 (Mamba2 branch: out = SiLU(z) *
+// GroupRMSNorm(y, ssm_norm.weight)), section 4.1 (the group norm normalises y
+// per group, then the gate multiplies) and section 6 (ssm_norm.weight, one
+// weight per channel of dInner = H*P).  For every row and each of the G groups
+// of gs = H*P/G contiguous channels:
+//   out[c] = silu(z[c]) * y[c] / sqrt(mean_{c' in group} y[c']^2 + eps) * w[c]
+//
+// HBM-bound (reads y, z; writes out): one warp per (row, group).  The first
+// pass sums y^2 (16-byte vectors, fp32 accumulation, a warp reduction); the
+// second reads y again (from L1: the warp just read it), z and w, and writes
+// out.  Every lane writes only elements it has read, so out may alias y.
+#include "internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kWarps = 8;  // (row, group) pairs per CTA
+
+template <typename T> struct NormVec;
+template <> struct NormVec<__nv_bfloat16> {
+    static constexpr int n = 8;
+    __device__ static void load(const void* p, float* v)
+    {
+        const uint4 r = __ldg(reinterpret_cast<const uint4*>(p));
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(h[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+    __device__ static void store(void* p, const float* v)
+    {
+        uint4 r;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&r);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        *reinterpret_cast<uint4*>(p) = r;
+    }
+    // bf16 output: silu(v) = (v/2)(1 + tanh(v/2)) with the hardware tanh
+    // (relative error ~2^-11, below the bf16 rounding of the result)
+    __device__ static float silu(float v)
+    {
+        float t;
+        const float hv = 0.5f * v;
+        asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(hv));
+        return fmaf(hv, t, hv);
+    }
+};
+template <> struct NormVec<float> {
+    static constexpr int n = 4;
+    __device__ static void load(const void* p, float* v)
+    {
+        const float4 r = __ldg(reinterpret_cast<const float4*>(p));
+        v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
+    }
+    __device__ static void store(void* p, const float* v)
+    {
+        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    __device__ static float silu(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32) gated_norm_kernel(GatedNormParams p)
+{
+    constexpr int V = NormVec<T>::n;
+    const int lane = threadIdx.x & 31;
+    const long long pair = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (pair >= p.rows * p.G) return;
+    const long long row = pair / p.G;
+    const int g = (int)(pair % p.G);
+    const int gs = p.C / p.G;
+    const size_t base = (size_t)row * p.C + (size_t)g * gs;  // first element of the group
+    const T* y = static_cast<const T*>(p.y) + base;
+    const T* z = static_cast<const T*>(p.z) + base;
+    T* out = static_cast<T*>(p.out) + base;
+    const float* w = p.w + (size_t)g * gs;
+
+    float ss = 0.0f;
+    for (int e = lane * V; e < gs; e += 32 * V) {
+        float v[V];
+        NormVec<T>::load(y + e, v);
+#pragma unroll
+        for (int i = 0; i < V; ++i) ss = fmaf(v[i], v[i], ss);
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
+    const float r = rsqrtf(ss / (float)gs + p.eps);
+
+    for (int e = lane * V; e < gs; e += 32 * V) {
+        float v[V], zv[V], o[V];
+        NormVec<T>::load(y + e, v);
+        NormVec<T>::load(z + e, zv);
+#pragma unroll
+        for (int i = 0; i < V; i += 4) {
+            const float4 wv = __ldg(reinterpret_cast<const float4*>(w + e + i));
+            const float ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[i + k] = NormVec<T>::silu(zv[i + k]) * (v[i + k] * r) * ws[k];
+        }
+        NormVec<T>::store(out + e, o);
+    }
+}
+
+}  // namespace
+
+bool gated_norm_supports(int C, int G, bool bf16)
+{
+    if (G <= 0 || C % G != 0) return false;
+    const int gs = C / G;
+    return gs % (bf16 ? 8 : 4) == 0;
+}
+
+cudaError_t launch_gated_norm(const GatedNormParams& p, bool bf16, cudaStream_t st)
+{
+    if (p.rows == 0) return cudaSuccess;
+    const long long pairs = p.rows * p.G;
+    const dim3 grid((unsigned)((pairs + kWarps - 1) / kWarps));
+    if (bf16) gated_norm_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, st>>>(p);
+    else gated_norm_kernel<float><<<grid, kWarps * 32, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ssd
