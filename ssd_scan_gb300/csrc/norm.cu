@@ -106,6 +106,44 @@ __global__ void __launch_bounds__(kWarps * 32) gated_norm_kernel(GatedNormParams
     }
 }
 
+// One CTA per (row, group) when the group is a whole number of warps of
+// vectors (gs = 32 V k, k <= 32): one vector of y and of z per thread, all
+// loads in flight at once, a shared-memory reduction over the k warps.
+template <typename T>
+__global__ void __launch_bounds__(1024) gated_norm_block_kernel(GatedNormParams p)
+{
+    constexpr int V = NormVec<T>::n;
+    __shared__ float part[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long row = blockIdx.x / p.G;
+    const int g = (int)(blockIdx.x % p.G);
+    const int gs = p.C / p.G;
+    const size_t off = (size_t)row * p.C + (size_t)g * gs + (size_t)tid * V;
+    float v[V], zv[V];
+    NormVec<T>::load(static_cast<const T*>(p.y) + off, v);
+    NormVec<T>::load(static_cast<const T*>(p.z) + off, zv);
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) ss = fmaf(v[i], v[i], ss);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
+    if (lane == 0) part[warp] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += part[i];
+    const float r = rsqrtf(tot / (float)gs + p.eps);
+    const float* w = p.w + (size_t)g * gs + (size_t)tid * V;
+    float o[V];
+#pragma unroll
+    for (int i = 0; i < V; i += 4) {
+        const float4 wv = __ldg(reinterpret_cast<const float4*>(w + i));
+        const float ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[i + k] = NormVec<T>::silu(zv[i + k]) * (v[i + k] * r) * ws[k];
+    }
+    NormVec<T>::store(static_cast<T*>(p.out) + off, o);
+}
+
 }  // namespace
 
 bool gated_norm_supports(int C, int G, bool bf16)
@@ -119,6 +157,12 @@ cudaError_t launch_gated_norm(const GatedNormParams& p, bool bf16, cudaStream_t 
 {
     if (p.rows == 0) return cudaSuccess;
     const long long pairs = p.rows * p.G;
+    const int V = bf16 ? 8 : 4, gs = p.C / p.G;
+    if (gs % (32 * V) == 0 && gs / V <= 1024 && pairs <= 0x7fffffffLL) {
+        if (bf16) gated_norm_block_kernel<__nv_bfloat16><<<(unsigned)pairs, gs / V, 0, st>>>(p);
+        else gated_norm_block_kernel<float><<<(unsigned)pairs, gs / V, 0, st>>>(p);
+        return cudaGetLastError();
+    }
     const dim3 grid((unsigned)((pairs + kWarps - 1) / kWarps));
     if (bf16) gated_norm_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, st>>>(p);
     else gated_norm_kernel<float><<<grid, kWarps * 32, 0, st>>>(p);

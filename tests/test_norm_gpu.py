@@ -33,8 +33,10 @@ def _inputs(B, S, C, act, seed):
 
 @pytest.mark.parametrize("act", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("in_place", [False, True])
-def test_gated_norm_matches_oracle(act, in_place):
-    B, S, H, P, G = 2, 37, 8, 64, 2
+# groups of 256 and 2048 channels (one CTA a group) and of 136 (one warp a group)
+@pytest.mark.parametrize("H,P,G", [(8, 64, 2), (32, 128, 2), (17, 8, 1)])
+def test_gated_norm_matches_oracle(act, in_place, H, P, G):
+    B, S = 2, 37
     C = H * P
     y, z, w = _inputs(B, S, C, act, seed=3)
     ref = oracle.gated_group_rmsnorm(f64(y), f64(z), f64(w), 1e-5, G)
