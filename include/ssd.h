@@ -127,7 +127,9 @@ SSD_API ssd_status ssd_conv1d_rows(const ssd_dims* dims, ssd_dtype act,
  *   dt_t = softplus(dt[b,t,h] + dt_bias[h])            (flag SSD_DT_SOFTPLUS)
  *   state = exp(dt_t A[h]) state + dt_t x_t B_t^T       state [P,N]
  *   y[b,t,h,:] = state C_t + D[h] x_t   (times silu(z) with SSD_HAS_Z)
- * computed in 128-row chunks (bf16) or exactly row by row (fp32).
+ * computed in 128-row chunks on the tensor cores (bf16, P=64, N=128, W<=4,
+ * calls of more than 4 rows) or exactly row by row (fp32, other shapes, and
+ * bf16 calls of at most 4 rows, where the row kernel is faster).
  *
  * xbc             [B,S,Cdim] act: raw rows when conv_w != NULL (the conv of
  *                 ssd_conv1d_rows runs first), else already post-conv rows.

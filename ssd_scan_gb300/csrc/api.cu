@@ -59,11 +59,20 @@ ssd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR
 
 // The tensor-core chunk scan serves bf16 with P = 64, N = 128, W <= 4 and
 // 128-row chunks; everything else runs on the row-exact fp32-pipe kernel.
+// Calls of at most this many rows per sequence take the row-exact kernel even
+// in bf16 (one CTA per (sequence, head), the state in registers, no chunk
+// pipeline to fill).  Measured at 4 sequences x 128 heads: the tensor-core
+// path costs ~37 us for any call of up to 128 rows, the row kernel ~23 us for
+// one row and ~3.4 us more per row, so the row kernel wins up to 4 rows.
+#ifndef SSD_SHORT_CALL_ROWS
+#define SSD_SHORT_CALL_ROWS 4
+#endif
+
 bool use_tensor_cores(const ssd_dims* d, ssd_dtype act)
 {
     const int chunk = d->chunk == 0 ? 128 : d->chunk;
     return act == SSD_BF16 && chunk == 128 && scan_tc_supports(d->headdim, d->dstate) &&
-           d->conv_width <= 4 && d->seqlen > 0;
+           d->conv_width <= 4 && d->seqlen > SSD_SHORT_CALL_ROWS;
 }
 
 // Scratch of the tensor-core path with the conv fused: the post-conv B|C

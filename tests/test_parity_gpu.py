@@ -223,6 +223,19 @@ def test_bf16_runs_on_tensor_cores():
     _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
 
 
+def test_bf16_short_calls_take_row_exact_kernel():
+    """Calls of up to 4 rows run the row-exact kernel (cheaper than filling the
+    chunk pipeline); 5 rows and more run on the tensor cores."""
+    shape = si.Shape(batch=2, seqlen=9, nheads=8, headdim=64, dstate=128, ngroups=2)
+    cpu, dev = make_problem(shape, act=torch.bfloat16, seed=4)
+    c0 = _counts()
+    y, h, cs = gpu_prefill(shape, dev, [4, 5])
+    torch.cuda.synchronize()
+    c1 = _counts()
+    assert c1["scan_simt"] - c0["scan_simt"] == 1 and c1["scan_tc"] - c0["scan_tc"] == 1
+    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
+
+
 def test_bf16_tensor_cores_without_conv():
     shape = si.Shape(batch=2, seqlen=200, nheads=4, headdim=64, dstate=128, ngroups=2)
     cpu, dev = make_problem(shape, act=torch.bfloat16)
