@@ -18,7 +18,10 @@ Functions (each cites the passage it follows in ``ssd_oracle.c``):
 * :func:`decode_step` -- gather / one step / scatter at state slots (vllm.cpp
   #1362 summary; TensorSharp "nemotron.md" section 11).
 * :func:`mixer_prefill` / :func:`mixer_decode` -- the compositions that the
-  C-ABI calls ``ssd_chunk_scan`` / ``ssd_decode_step`` compute.
+  C-ABI calls ``ssd_chunk_scan`` / ``ssd_decode_step`` compute;
+  :func:`mixer_prefill_varlen` -- ``ssd_chunk_scan_varlen``: packed sequences
+  with their states at pool slots (vllm.cpp #1362 summary; TensorSharp
+  "nemotron.md" section 11).
 * :func:`gated_group_rmsnorm` -- group RMSNorm of y, then the SiLU(z) gate
   (TensorSharp "nemotron.md" sections 3, 4.1 and 6).
 
@@ -209,6 +212,41 @@ def mixer_prefill(xbc_raw, conv_w, dt_raw, A, *, H, P, N, G, conv_b=None, conv_s
     y, hS = ssd_sequential(xbc, dt_raw, A, H=H, P=P, N=N, G=G, dt_bias=dt_bias, D=D, z=z,
                            h0=h0, dt_softplus=dt_softplus, nthreads=nthreads)
     return y, hS, cs_out
+
+
+def mixer_prefill_varlen(xbc_raw, conv_w, dt_raw, A, cu_seqlens, slot_ids, ssm_pool,
+                         conv_pool, *, H, P, N, G, has_initial_state=None, conv_b=None,
+                         dt_bias=None, D=None, z=None, dt_softplus=True, nthreads=None):
+    """What one ssd_chunk_scan_varlen call computes: sequences packed row after
+    row (sequence i = rows cu_seqlens[i] .. cu_seqlens[i+1]-1), each run as one
+    mixer_prefill from the states at its pool slot (zeros when
+    has_initial_state[i] is 0: a fresh request), the final states written back
+    at the slot (vllm.cpp #1362 summary: the prefill half of a mixed batch over
+    packed rows, states at the state index; TensorSharp "nemotron.md" section
+    11: per-slot state pools).  xbc_raw [T,Cdim], dt_raw [T,H], z [T,H*P] or
+    None, pools [slots,...].  Returns (y [T,H,P], ssm_pool', conv_pool')."""
+    xbc_raw = _f64(xbc_raw)
+    dt_raw = _f64(dt_raw)
+    z = _f64(z)
+    ssm_pool = np.array(ssm_pool, dtype=np.float64, copy=True)
+    conv_pool = None if conv_pool is None else np.array(conv_pool, dtype=np.float64, copy=True)
+    T = xbc_raw.shape[0]
+    y = np.zeros((T, H, P), np.float64)
+    for i in range(len(slot_ids)):
+        r0, r1, sl = int(cu_seqlens[i]), int(cu_seqlens[i + 1]), int(slot_ids[i])
+        init = has_initial_state is None or bool(has_initial_state[i])
+        h0 = ssm_pool[sl][None] if init else None
+        cs = conv_pool[sl][None] if (init and conv_pool is not None) else None
+        yi, hS, cs_out = mixer_prefill(
+            xbc_raw[None, r0:r1], conv_w, dt_raw[None, r0:r1], A, H=H, P=P, N=N, G=G,
+            conv_b=conv_b, conv_state=cs, dt_bias=dt_bias, D=D,
+            z=None if z is None else z[None, r0:r1], h0=h0, dt_softplus=dt_softplus,
+            nthreads=nthreads)
+        y[r0:r1] = yi[0]
+        ssm_pool[sl] = hS[0]
+        if conv_pool is not None and cs_out is not None:
+            conv_pool[sl] = cs_out[0]
+    return y, ssm_pool, conv_pool
 
 
 def mixer_decode(xbc_raw, conv_w, dt_raw, A, slot_ids, ssm_pool, *, H, P, N, G,

@@ -416,3 +416,61 @@ def test_rmsnorm_gate_acts_after_the_norm():
     assert np.array_equal(out[:, others], base[:, others])
     ratio = (2.5 * expit(2.5)) / (z[:, 5] * expit(z[:, 5]))
     assert np.allclose(out[:, 5], base[:, 5] * ratio, rtol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# packed sequences with states at pool slots (vllm.cpp #1362 summary;
+# TensorSharp "nemotron.md" section 11)
+
+def _varlen_problem(lens, nslots=6, seed=0):
+    shape = TINY.with_(batch=1, seqlen=sum(lens))
+    p = si.params(shape, seed=seed)
+    a = si.prefill_inputs(shape, seed=seed, act_dtype=__import__("torch").float32, with_z=True)
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    rng = np.random.default_rng(seed)
+    pools = (rng.standard_normal((nslots, H, P, N)) * 0.1,
+             rng.standard_normal((nslots, shape.conv_width - 1, shape.cdim)))
+    prm = {k: p[k].double().numpy() for k in ("conv_w", "conv_b", "dt_bias", "A", "D")}
+    return shape, prm, a["xbc"][0].double().numpy(), a["dt_raw"][0].double().numpy(), \
+        a["z"][0].double().numpy(), pools
+
+
+def test_varlen_equals_one_call_per_sequence_and_leaves_other_slots():
+    """Each packed sequence equals a call of its own from its slot's states; a
+    fresh sequence (has_initial_state 0) equals a call from zero states; slots
+    no sequence names are untouched."""
+    lens, slots, init = [5, 1, 7], [4, 0, 2], [1, 0, 1]
+    shape, prm, xbc, dt, z, (spool, cpool) = _varlen_problem(lens)
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    y, sp, cp = oracle.mixer_prefill_varlen(
+        xbc, prm["conv_w"], dt, prm["A"], cu, slots, spool, cpool, H=H, P=P, N=N, G=G,
+        has_initial_state=init, conv_b=prm["conv_b"], dt_bias=prm["dt_bias"], D=prm["D"], z=z)
+    for i, (r0, r1) in enumerate(zip(cu[:-1], cu[1:])):
+        s = slots[i]
+        yi, hi, ci = oracle.mixer_prefill(
+            xbc[None, r0:r1], prm["conv_w"], dt[None, r0:r1], prm["A"], H=H, P=P, N=N, G=G,
+            conv_b=prm["conv_b"], conv_state=cpool[s][None] if init[i] else None,
+            dt_bias=prm["dt_bias"], D=prm["D"], z=z[None, r0:r1],
+            h0=spool[s][None] if init[i] else None)
+        assert np.array_equal(y[r0:r1], yi[0])
+        assert np.array_equal(sp[s], hi[0]) and np.array_equal(cp[s], ci[0])
+    for s in (1, 3, 5):
+        assert np.array_equal(sp[s], spool[s]) and np.array_equal(cp[s], cpool[s])
+
+
+def test_varlen_of_equal_lengths_equals_the_batched_call():
+    """Equal lengths at slots 0..B-1 with initial states: the batched mixer."""
+    lens = [4, 4, 4]
+    shape, prm, xbc, dt, z, (spool, cpool) = _varlen_problem(lens, nslots=3, seed=2)
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    cu = np.array([0, 4, 8, 12])
+    y, sp, cp = oracle.mixer_prefill_varlen(
+        xbc, prm["conv_w"], dt, prm["A"], cu, [0, 1, 2], spool, cpool, H=H, P=P, N=N, G=G,
+        conv_b=prm["conv_b"], dt_bias=prm["dt_bias"], D=prm["D"], z=z)
+    yb, hb, cb = oracle.mixer_prefill(
+        xbc.reshape(3, 4, -1), prm["conv_w"], dt.reshape(3, 4, -1), prm["A"], H=H, P=P, N=N,
+        G=G, conv_b=prm["conv_b"], conv_state=cpool, dt_bias=prm["dt_bias"], D=prm["D"],
+        z=z.reshape(3, 4, -1), h0=spool)
+    assert np.array_equal(y.reshape(yb.shape), yb)
+    assert np.array_equal(sp, hb) and np.array_equal(cp, cb)
