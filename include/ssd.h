@@ -7,8 +7,9 @@
  *                    the conv fused in front), with carried conv/SSM state
  *   ssd_decode_step  one recurrent step for R rows at slot-indexed states,
  *                    updated in place
- * and ssd_gated_group_rmsnorm, the group RMSNorm + SiLU(z) gate that follows
- * the scan in the mixer.
+ * and ssd_chunk_scan_varlen (the scan over packed sequences of different
+ * lengths with slot-indexed states) and ssd_gated_group_rmsnorm (the group
+ * RMSNorm + SiLU(z) gate that follows the scan in the mixer).
  *
  * Sources (page title, section):
  *   TensorRT-Model-Connect PR #2207 "perf(nemotron_h): prefill single-GPU
@@ -209,6 +210,48 @@ SSD_API ssd_status ssd_chunk_scan_static_ws(const ssd_dims* dims, ssd_dtype act,
                                     const float* dt, const float* dt_bias, const float* A,
                                     const float* D, const void* z, const float* ssm_state_in,
                                     void* y, float* ssm_state_out, cudaStream_t stream);
+
+/*
+ * ssd_chunk_scan_varlen -- the scan over sequences of different lengths packed
+ * row after row, each continuing from (or, when fresh, replacing) the states
+ * at its slot of the state pools, updated in place.
+ * (vllm.cpp #1362 summary: the prefill half of a mixed batch runs the chunk
+ *  scan over packed rows, states at the state index, has_initial_state for
+ *  fresh requests, in place, no gather/scatter copies; TensorSharp
+ *  nemotron.md section 11: per-slot conv + SSM state pools.)
+ *
+ * dims->batch = nseq sequences, dims->seqlen = T rows in all.  Sequence i is
+ * rows cu_seqlens[i] .. cu_seqlens[i+1]-1 (cu_seqlens[0] = 0, non-decreasing,
+ * cu_seqlens[nseq] = T; empty sequences allowed), s = slot_ids[i]:
+ *   states in  = ssm_pool[s], conv_pool[s]   if has_initial_state[i] != 0
+ *                zeros                       otherwise (a fresh request)
+ *   the rows of sequence i as one ssd_chunk_scan call from those states
+ *   ssm_pool[s], conv_pool[s] = the final states                  (in place)
+ * The decode rows of a mixed batch go to ssd_decode_step on the same pools.
+ *
+ * cu_seqlens, slot_ids       [nseq+1], [nseq] int32, DEVICE memory; slot ids
+ *                            distinct (not checked: duplicates race)
+ * has_initial_state          [nseq] int32 DEVICE memory, or NULL (all 1)
+ * xbc [T,Cdim], dt [T,H], z [T,H*P], y [T,H,P]: packed rows, as the
+ *   [B,S,..] arrays of ssd_chunk_scan with B = 1, S = T
+ * conv_w, conv_b             as in ssd_chunk_scan (conv_w NULL: post-conv
+ *                            rows, conv_pool and conv_b must be NULL)
+ * conv_pool                  [num_slots,W-1,Cdim] act (required iff conv_w)
+ * ssm_pool                   [num_slots,H,P,N] fp32
+ * workspace                  at least T*2*G*N*2 bytes when conv_w != NULL
+ * A sequence whose rows leave [0, T) or whose slot is outside [0, num_slots)
+ * sets the device error word to SSD_ERR_BAD_SLOT and writes nothing (neither
+ * pool nor y); the other sequences are unaffected.  Runs on the tensor-core
+ * path only: bf16, P=64, N=128, W<=4, chunk 128 (else SSD_ERR_UNSUPPORTED).
+ */
+SSD_API ssd_status ssd_chunk_scan_varlen(const ssd_dims* dims, ssd_dtype act, unsigned flags,
+                                 const int32_t* cu_seqlens, const int32_t* slot_ids,
+                                 const int32_t* has_initial_state, int num_slots,
+                                 const void* xbc, const float* conv_w, const float* conv_b,
+                                 void* conv_pool, const float* dt, const float* dt_bias,
+                                 const float* A, const float* D, const void* z,
+                                 float* ssm_pool, void* y, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * ssd_decode_step -- one recurrent step for R rows at slot-indexed states.

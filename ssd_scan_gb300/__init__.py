@@ -37,7 +37,8 @@ SSD_STATIC_SCRATCH_BYTES = 16 << 20
 # every symbol include/ssd.h declares
 EXPORTED = ("ssd_conv1d_rows", "ssd_chunk_scan", "ssd_chunk_scan_workspace_size",
             "ssd_decode_step", "ssd_status_string", "ssd_read_device_error",
-            "ssd_launch_counts", "ssd_chunk_scan_static_ws", "ssd_gated_group_rmsnorm")
+            "ssd_launch_counts", "ssd_chunk_scan_static_ws", "ssd_gated_group_rmsnorm",
+            "ssd_chunk_scan_varlen")
 
 KERNEL_KINDS = ("conv_rows", "conv_state", "scan_simt", "scan_tc", "bc_conv", "decode_step",
                 "decode_conv", "gated_norm")
@@ -86,6 +87,8 @@ def load_library():
             lib.ssd_decode_step.argtypes = [P, ci, cu] + [_vp] * 10 + [ci, _vp, _vp, _vp]
             lib.ssd_gated_group_rmsnorm.argtypes = [P, ci, _vp, _vp, _vp, ctypes.c_float, _vp,
                                                      _vp]
+            lib.ssd_chunk_scan_varlen.argtypes = [P, ci, cu, _vp, _vp, _vp, ci] + [_vp] * 11 + \
+                [_vp, sz, _vp]
             lib.ssd_status_string.argtypes = [ci]
             lib.ssd_status_string.restype = ctypes.c_char_p
             lib.ssd_read_device_error.argtypes = [_vp]
@@ -203,6 +206,25 @@ def ssd_decode_step(d: ssd_dims, act: int, flags: int, xbc, conv_w, conv_b, conv
         _ptr(dt_bias, f, "dt_bias"), _ptr(A, f, "A"), _ptr(D, f, "D"), _ptr(z, a, "z"),
         _ptr(slot_ids, torch.int32, "slot_ids"), int(num_slots),
         _ptr(ssm_pool, f, "ssm_pool"), _ptr(y, a, "y"), _stream(stream)), "ssd_decode_step")
+
+
+def ssd_chunk_scan_varlen(d: ssd_dims, act: int, flags: int, cu_seqlens, slot_ids,
+                          has_initial_state, num_slots: int, xbc, conv_w, conv_b, conv_pool, dt,
+                          dt_bias, A, D, z, ssm_pool, y, workspace=None, stream=None) -> None:
+    """The scan over packed sequences (d.batch sequences, d.seqlen rows in all),
+    states at pool slots, updated in place."""
+    a = _ACT[act]
+    f = torch.float32
+    i32 = torch.int32
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().ssd_chunk_scan_varlen(
+        ctypes.byref(d), act, flags, _ptr(cu_seqlens, i32, "cu_seqlens"),
+        _ptr(slot_ids, i32, "slot_ids"), _ptr(has_initial_state, i32, "has_initial_state"),
+        int(num_slots), _ptr(xbc, a, "xbc"), _ptr(conv_w, f, "conv_w"), _ptr(conv_b, f, "conv_b"),
+        _ptr(conv_pool, a, "conv_pool"), _ptr(dt, f, "dt"), _ptr(dt_bias, f, "dt_bias"),
+        _ptr(A, f, "A"), _ptr(D, f, "D"), _ptr(z, a, "z"), _ptr(ssm_pool, f, "ssm_pool"),
+        _ptr(y, a, "y"), _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)),
+        "ssd_chunk_scan_varlen")
 
 
 def ssd_gated_group_rmsnorm(d: ssd_dims, act: int, y, z, weight, eps: float, out,

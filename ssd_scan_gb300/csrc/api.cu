@@ -290,6 +290,71 @@ ssd_status ssd_decode_step(const ssd_dims* dims, ssd_dtype act, unsigned flags, 
                    conv_w != nullptr && dims->conv_width > 1);
 }
 
+ssd_status ssd_chunk_scan_varlen(const ssd_dims* dims, ssd_dtype act, unsigned flags,
+                                 const int32_t* cu_seqlens, const int32_t* slot_ids,
+                                 const int32_t* has_initial_state, int num_slots, const void* xbc,
+                                 const float* conv_w, const float* conv_b, void* conv_pool,
+                                 const float* dt, const float* dt_bias, const float* A,
+                                 const float* D, const void* z, float* ssm_pool, void* y,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    long long cdim = 0;
+    ssd_status s = check_dims(dims, act, &cdim);
+    if (s != SSD_OK) return s;
+    if (flags & ~(unsigned)(SSD_DT_SOFTPLUS | SSD_HAS_Z)) return SSD_ERR_INVALID_ARG;
+    const int nseq = dims->batch;
+    const long long T = dims->seqlen;
+    const bool has_z = (flags & SSD_HAS_Z) != 0;
+    const int chunk = dims->chunk == 0 ? 128 : dims->chunk;
+    if (act != SSD_BF16 || chunk != 128 || !scan_tc_supports(dims->headdim, dims->dstate) ||
+        dims->conv_width > 4)
+        return SSD_ERR_UNSUPPORTED;
+    if (nseq == 0) return SSD_OK;
+    if (cu_seqlens == nullptr || slot_ids == nullptr || !aligned4(cu_seqlens) ||
+        !aligned4(slot_ids) || (has_initial_state && !aligned4(has_initial_state)) ||
+        num_slots <= 0 || ssm_pool == nullptr || !aligned16(ssm_pool))
+        return SSD_ERR_INVALID_ARG;
+    if (A == nullptr || !aligned4(A) || (dt_bias && !aligned4(dt_bias)) || (D && !aligned4(D)))
+        return SSD_ERR_INVALID_ARG;
+    if (T > 0 && (xbc == nullptr || dt == nullptr || y == nullptr || !aligned16(xbc) ||
+                  !aligned16(y) || !aligned4(dt) || (has_z && (z == nullptr || !aligned16(z)))))
+        return SSD_ERR_INVALID_ARG;
+    if (conv_w == nullptr && (conv_pool || conv_b)) return SSD_ERR_INVALID_ARG;
+    if (conv_w && (!aligned4(conv_w) || (conv_b && !aligned4(conv_b)) || conv_pool == nullptr ||
+                   !aligned16(conv_pool)))
+        return SSD_ERR_INVALID_ARG;
+    const int H = dims->nheads, P = dims->headdim, N = dims->dstate, G = dims->ngroups;
+    const size_t need = conv_w ? (size_t)T * 2 * G * N * 2 : 0;  // post-conv B|C rows
+    if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned16(workspace))))
+        return SSD_ERR_INVALID_ARG;
+
+    unsigned* err = nullptr;
+    s = error_word_address(&err);
+    if (s != SSD_OK) return s;
+    TcScanParams tp{nseq, (int)T, H, G, dims->conv_width, flags, conv_w != nullptr, xbc, xbc,
+                    (int)cdim, H * P, conv_w, conv_b, conv_pool, conv_pool, dt, dt_bias, A, D,
+                    has_z ? z : nullptr, ssm_pool, y, ssm_pool, err};
+    tp.cu_seqlens = cu_seqlens;
+    tp.slot_ids = slot_ids;
+    tp.has_init = has_initial_state;
+    tp.num_slots = num_slots;
+    if (conv_w != nullptr) {
+        ConvParams bp{1, (int)T, (int)cdim, dims->conv_width, xbc, conv_w, conv_b, conv_pool,
+                      workspace, nullptr, H * P, 2 * G * N, 2 * G * N};
+        bp.cu_seqlens = cu_seqlens;
+        bp.slot_ids = slot_ids;
+        bp.has_init = has_initial_state;
+        bp.nseq = nseq;
+        bp.num_slots = num_slots;
+        s = counted(launch_conv1d_rows(bp, true, stream), SSD_KERNEL_BC_CONV, T > 0);
+        if (s != SSD_OK) return s;
+        tp.bc = workspace;
+        tp.bc_stride = 2 * G * N;
+        tp.bc_col0 = 0;
+    }
+    return counted(launch_scan_tc(tp, stream, conv_w != nullptr && T > 0), SSD_KERNEL_SCAN_TC);
+}
+
 ssd_status ssd_gated_group_rmsnorm(const ssd_dims* dims, ssd_dtype act, const void* y,
                                    const void* z, const float* weight, float eps, void* out,
                                    cudaStream_t stream)

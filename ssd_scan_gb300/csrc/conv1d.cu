@@ -138,6 +138,55 @@ __global__ void __launch_bounds__(128) conv1d_rows_kernel(ConvParams p)
     }
 }
 
+// Packed sequences: one CTA column per row, one thread per 16 bytes of
+// channels.  The row's sequence is found by binary search over cu_seqlens
+// (the last i with cu_seqlens[i] <= row, so empty sequences are skipped); taps
+// before the sequence's first row read its conv state at its slot (zeros for a
+// fresh sequence, or for a slot out of range, which the scan reports).
+template <typename T, int W>
+__global__ void __launch_bounds__(128) conv1d_rows_varlen_kernel(ConvParams p)
+{
+    sm100::griddep_launch_dependents();
+    constexpr int V = Vec16<T>::n;
+    const int nvec = p.ncols / V;
+    const int cv = blockIdx.y * blockDim.x + threadIdx.x;
+    if (cv >= nvec) return;
+    const long long r = blockIdx.x;
+    int lo = 0, hi = p.nseq;  // cu[lo] <= r < cu[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.cu_seqlens[mid] <= r) lo = mid;
+        else hi = mid;
+    }
+    const long long r0 = p.cu_seqlens[lo];
+    const int t = (int)(r - r0);
+    const int slot = p.slot_ids[lo];
+    const bool from_state = p.st_in != nullptr && (p.has_init == nullptr || p.has_init[lo] != 0) &&
+                            slot >= 0 && slot < p.num_slots;
+    const int c0 = p.col0 + cv * V, o0 = cv * V;
+    const T* __restrict__ x = static_cast<const T*>(p.x);
+    const T* __restrict__ st = static_cast<const T*>(p.st_in);
+    float o[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) o[j] = p.bias ? __ldg(p.bias + c0 + j) : 0.0f;
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+        const int u = t - (W - 1) + k;  // row of the sequence this tap reads
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        // (a malformed cu_seqlens, which the scan reports, reads nothing out of range)
+        if (u >= 0) {
+            if (r0 + u >= 0 && r0 + u <= r) raw = Vec16<T>::load(x + (r0 + u) * p.C + c0);
+        } else if (from_state) raw = Vec16<T>::load(st + ((size_t)slot * (W - 1) + (W - 1 + u)) * p.C + c0);
+        float f[V];
+        Vec16<T>::unpack(raw, f);
+#pragma unroll
+        for (int j = 0; j < V; ++j) o[j] = fmaf(__ldg(p.w + (size_t)(c0 + j) * W + k), f[j], o[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < V; ++j) o[j] = Vec16<T>::silu(o[j]);
+    Vec16<T>::store(static_cast<T*>(p.out) + r * p.out_stride + o0, o);
+}
+
 // conv_state_out[b, j, c] = u[b, S + j, c] with u = [state_in ; x].  One
 // thread per (b, c) walks j upwards, so an in-place call (st_out == st_in)
 // only ever overwrites rows it has already read.
@@ -169,6 +218,18 @@ cudaError_t launch_rows_t(ConvParams p, cudaStream_t st)
     if (p.ncols % V != 0 || p.col0 % V != 0 || p.out_stride % V != 0) return cudaErrorInvalidValue;
     const int nvec = p.ncols / V;
     dim3 block(128);
+    if (p.cu_seqlens != nullptr) {  // packed sequences: one CTA column per row
+        dim3 vgrid((unsigned)p.S, (nvec + 127) / 128);
+        switch (p.W) {
+#define SSD_CONV_VCASE(w) \
+    case w: conv1d_rows_varlen_kernel<T, w><<<vgrid, block, 0, st>>>(p); break;
+            SSD_CONV_VCASE(1) SSD_CONV_VCASE(2) SSD_CONV_VCASE(3) SSD_CONV_VCASE(4)
+            SSD_CONV_VCASE(5) SSD_CONV_VCASE(6) SSD_CONV_VCASE(7) SSD_CONV_VCASE(8)
+#undef SSD_CONV_VCASE
+            default: return cudaErrorInvalidValue;
+        }
+        return cudaGetLastError();
+    }
     dim3 grid((nvec + 127) / 128, (p.S + kRowsPerThread - 1) / kRowsPerThread, p.B);
     switch (p.W) {
 #define SSD_CONV_CASE(w) \

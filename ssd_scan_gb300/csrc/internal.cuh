@@ -24,6 +24,14 @@ struct ConvParams {
     int col0 = 0;         // first channel the rows kernel computes
     int ncols = -1;       // channels it computes (-1: all C)
     int out_stride = -1;  // output row length in elements (-1: C)
+    // packed sequences (rows kernel only; null: B sequences of S rows): nseq
+    // sequences over the S rows, sequence i = rows cu_seqlens[i] ..
+    // cu_seqlens[i+1]-1, its conv state at slot slot_ids[i] of st_in (zeros
+    // when has_init[i] == 0)
+    const int* cu_seqlens = nullptr;
+    const int* slot_ids = nullptr;
+    const int* has_init = nullptr;
+    int nseq = 0, num_slots = 0;
 };
 
 struct ScanParams {
@@ -108,6 +116,15 @@ struct TcScanParams {
     void* y;                     // [B,S,H,64] bf16
     float* hS;                   // [B,H,64,128]
     unsigned* err;
+    // Packed sequences of different lengths (null: B sequences of S rows each).
+    // Sequence i is rows cu_seqlens[i] .. cu_seqlens[i+1]-1 of the S rows of
+    // every row array (B = number of sequences, batch 1 in the row arrays); its
+    // states are slot slot_ids[i] of the pools h0 == hS and conv_state_in ==
+    // conv_state_out, read as zeros when has_init[i] == 0.
+    const int* cu_seqlens = nullptr;
+    const int* slot_ids = nullptr;
+    const int* has_init = nullptr;  // or null: every sequence continues its slot
+    int num_slots = 0;
 };
 bool scan_tc_supports(int P, int N);
 // after_prepass: the kernel just before it on `st` is the B|C conv writing p.bc;

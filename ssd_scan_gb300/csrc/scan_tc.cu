@@ -247,6 +247,7 @@ __device__ __forceinline__ bool wait_or_abort(TcSmem& s, uint64_t* bar, uint32_t
     }
 }
 
+template <bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
     scan_tc_kernel(const __grid_constant__ CUtensorMap map_bc, const __grid_constant__ CUtensorMap map_z,
                    const __grid_constant__ CUtensorMap map_y, const TcScanParams p)
@@ -257,8 +258,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     TcSmem& s = *reinterpret_cast<TcSmem*>(smem_raw + ((1024u - (sm100::smem_u32(smem_raw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x, b = blockIdx.y;
-    const int H = p.H, G = p.G, W = p.W, S = p.S;
+    const int h = blockIdx.x, b = blockIdx.y;  // head, sequence
+    const int H = p.H, G = p.G, W = p.W;
+    // this CTA's sequence: its first row in the row arrays, its rows, its state
+    // slot, and whether its states start from the slot or from zeros
+    long long row0 = (long long)b * p.S;
+    int S = p.S, slot = b;
+    bool init = true;
+    if constexpr (kVarlen) {
+        row0 = p.cu_seqlens[b];
+        const long long end = p.cu_seqlens[b + 1];
+        slot = p.slot_ids[b];
+        init = p.has_init == nullptr || p.has_init[b] != 0;
+        // a bad row range or slot: report it and leave (every thread of the CTA
+        // read the same values, so all of them leave here, before any setup)
+        if (row0 < 0 || end < row0 || end > p.S || slot < 0 || slot >= p.num_slots) {
+            if (threadIdx.x == 0) atomicOr(p.err, kErrBadSlot);
+            return;
+        }
+        S = (int)(end - row0);
+    }
+    const float* h0 = init ? p.h0 : nullptr;
+    const void* cs_in = init ? p.conv_state_in : nullptr;
+    // tile coordinates of chunk c: row and batch of the [cols, rows, batch] maps
+    const int tz = kVarlen ? 0 : b;
+    auto trow = [&](int c) { return kVarlen ? (int)(row0 + (long long)c * Q) : c * Q; };
     const int g = h / (H / G);
     const int Cdim = H * P + 2 * G * N;
     const int nchunks = (S + Q - 1) / Q;
@@ -324,15 +348,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             int loaded_c = 0, loaded_b = 0, loaded_z = 0;  // tiles requested so far
             auto load_c = [&](int c) {  // C tile of chunk c (the one buffer)
                 mbar_arrive_expect_tx(&s.full_c, 2 * Q * 64 * 2);
-                tma_load_3d(s.C[0], &map_bc, &s.full_c, xC, c * Q, b);
-                tma_load_3d(s.C[1], &map_bc, &s.full_c, xC + 64, c * Q, b);
+                tma_load_3d(s.C[0], &map_bc, &s.full_c, xC, trow(c), tz);
+                tma_load_3d(s.C[1], &map_bc, &s.full_c, xC + 64, trow(c), tz);
                 loaded_c = c + 1;
             };
             auto load_b = [&](int c) {  // B tile of chunk c into buffer c & 1
                 const int kb = c & 1;
                 mbar_arrive_expect_tx(&s.full_b[kb], 2 * Q * 64 * 2);
-                tma_load_3d(s.B[kb][0], &map_bc, &s.full_b[kb], xB, c * Q, b);
-                tma_load_3d(s.B[kb][1], &map_bc, &s.full_b[kb], xB + 64, c * Q, b);
+                tma_load_3d(s.B[kb][0], &map_bc, &s.full_b[kb], xB, trow(c), tz);
+                tma_load_3d(s.B[kb][1], &map_bc, &s.full_b[kb], xB + 64, trow(c), tz);
                 loaded_b = c + 1;
             };
             // K step k of a K-major operand: (k>>2)*16 KB + (k&3)*32 B; of an MN-major
@@ -372,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // z tile of chunk c (one buffer: the epilogue of chunk c-1 is done with it)
             auto load_z = [&](int c) {
                 mbar_arrive_expect_tx(&s.full_z, Q * 64 * 2);
-                tma_load_3d(s.Zt, &map_z, &s.full_z, h * P, c * Q, b);
+                tma_load_3d(s.Zt, &map_z, &s.full_z, h * P, trow(c), tz);
                 loaded_z = c + 1;
             };
             if (has_z) {
@@ -470,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = c * Q + 4 * lane + i;
-                dtn[i] = r < S ? p.dt[((size_t)b * S + r) * H + h] : 0.0f;
+                dtn[i] = r < S ? p.dt[((size_t)row0 + r) * H + h] : 0.0f;
             }
         };
         if (nchunks > 0) load_dt(0);
@@ -544,18 +568,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = warp >> 2;  // column group of the quarter
         const int t = 32 * q + lane;  // chunk row (mask, epilogue) / state column n (state)
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-        const size_t sbase = ((size_t)b * H + h) * P * N;
+        const size_t sbase = ((size_t)slot * H + h) * P * N;
         const float Dh = p.D ? p.D[h] : 0.0f;
         bool ok = true;  // false after any failed wait: the thread then only walks the loop
 
         // -- conv share: rows 4 rq .. 4 rq + 3, channels 4 jq .. 4 jq + 3 --
         const int rq = tid >> 4, jq = tid & 15;
         const __nv_bfloat16* xrow =
-            static_cast<const __nv_bfloat16*>(p.xbc) + (size_t)b * S * Cdim + h * P + 4 * jq;
+            static_cast<const __nv_bfloat16*>(p.xbc) + (size_t)row0 * Cdim + h * P + 4 * jq;
         const __nv_bfloat16* csb =
-            p.conv_state_in
-                ? static_cast<const __nv_bfloat16*>(p.conv_state_in) + (size_t)b * (W - 1) * Cdim + h * P + 4 * jq
-                : nullptr;
+            cs_in ? static_cast<const __nv_bfloat16*>(cs_in) + (size_t)slot * (W - 1) * Cdim + h * P + 4 * jq
+                  : nullptr;
         uint2 raw[kRaw];  // raw rows 4rq-3 .. 4rq+3 of a chunk, loaded one chunk ahead
         auto load_raw = [&](int c) {
             const int g0 = c * Q + 4 * rq - (kMaxW - 1);
@@ -625,8 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 hreg[8];  // h[16j + 2i .. +1][n]
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            hreg[i] = p.h0 ? make_float2(p.h0[sbase + (size_t)(16 * j + 2 * i) * N + t],
-                                         p.h0[sbase + (size_t)(16 * j + 2 * i + 1) * N + t])
+            hreg[i] = h0 ? make_float2(h0[sbase + (size_t)(16 * j + 2 * i) * N + t],
+                                       h0[sbase + (size_t)(16 * j + 2 * i + 1) * N + t])
                            : make_float2(0.f, 0.f);
         auto store_h = [&]() {  // bf16 h[n][16j .. 16j+15]: 2 chunks of 16 bytes
             at<uint4>(s.Hs, chunk_off(t, 2 * j)) = pack4x2(&hreg[0]);
@@ -785,7 +808,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (has_z) v = __fmul2_rn(v, silu2(zv[e]));
                         out[e] = v;
                     }
-                    at<uint4>(s.Yt, off) = pack4x2(out);
+                    if (kVarlen && c * Q + 32 * q + 32 > S) {
+                        // the sequence ends inside this quarter and the next sequence's
+                        // rows follow it: this thread stores its own row, if it has one
+                        if (t < rows)
+                            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) +
+                                                      ((size_t)(row0 + c * Q + t) * H + h) * P +
+                                                      16 * j + 8 * hh) = pack4x2(out);
+                    } else {
+                        at<uint4>(s.Yt, off) = pack4x2(out);
+                    }
                 }
             } else {
                 ok = false;
@@ -794,9 +826,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&s.epidone[c % kCv]);
             named_bar_sync(1 + q, 128);  // the quarter's four warps
-            if (j == 0 && lane == 0 && ok && c * Q + 32 * q < S) {  // a quarter with rows left
+            // a quarter with rows left (packed sequences: a whole quarter of them)
+            if (j == 0 && lane == 0 && ok && (kVarlen ? c * Q + 32 * q + 32 <= S : c * Q + 32 * q < S)) {
                 tma_store_3d(&map_y, reinterpret_cast<const char*>(s.Yt) + q * 32 * 128, h * P,
-                             c * Q + 32 * q, b);
+                             trow(c) + 32 * q, tz);
                 bulk_commit();
                 bulk_wait_read_all();
             }
@@ -822,15 +855,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col = tid < P ? h * P + tid
                                     : (tid < P + N ? H * P + g * N + (tid - P) : H * P + G * N + g * N + (tid - P - N));
             const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(p.xbc);
-            const __nv_bfloat16* si = static_cast<const __nv_bfloat16*>(p.conv_state_in);
+            const __nv_bfloat16* si = static_cast<const __nv_bfloat16*>(cs_in);
             __nv_bfloat16* so = static_cast<__nv_bfloat16*>(p.conv_state_out);
             const int nh = W - 1;
             for (int jj = 0; jj < nh; ++jj) {
                 const int r = S + jj;  // row of [conv state ; rows]
                 __nv_bfloat16 v;
-                if (r < nh) v = si ? si[((size_t)b * nh + r) * Cdim + col] : __float2bfloat16_rn(0.0f);
-                else v = xs[((size_t)b * S + (r - nh)) * Cdim + col];
-                so[((size_t)b * nh + jj) * Cdim + col] = v;
+                if (r < nh) v = si ? si[((size_t)slot * nh + r) * Cdim + col] : __float2bfloat16_rn(0.0f);
+                else v = xs[((size_t)row0 + (r - nh)) * Cdim + col];
+                so[((size_t)slot * nh + jj) * Cdim + col] = v;
             }
         }
     }
@@ -881,15 +914,23 @@ bool scan_tc_supports(int P_, int N_) { return P_ == P && N_ == N; }
 
 cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st, bool after_prepass)
 {
-    if (p.B == 0 || p.S == 0) return cudaSuccess;
+    const bool varlen = p.cu_seqlens != nullptr;
+    // packed sequences still run with no rows at all: fresh ones get zero states
+    if (p.B == 0 || (p.S == 0 && !varlen)) return cudaSuccess;
     if (p.W > kMaxW || !encode_fn()) return cudaErrorNotSupported;
+    // row arrays as [cols, rows, batch]: packed sequences are one batch of all
+    // rows; with no rows, any 16-byte aligned array stands in (no tile is read)
+    const int mS = p.S > 0 ? p.S : 1, mB = varlen ? 1 : p.B;
+    const void* stand_in = p.h0;
     CUtensorMap mbc, mz, my;
-    if (!make_map(&mbc, p.bc, p.bc_stride, p.S, p.B)) return cudaErrorInvalidValue;
+    if (!make_map(&mbc, p.S > 0 ? p.bc : stand_in, p.bc_stride, mS, mB)) return cudaErrorInvalidValue;
     // z tiles in (128 rows), y leaves in 32-row quarters; both [B, S, H*P]
     memset(&mz, 0, sizeof(mz));
-    if ((p.flags & kHasZ) && !make_map(&mz, p.z, p.H * P, p.S, p.B)) return cudaErrorInvalidValue;
-    if (!make_map(&my, p.y, p.H * P, p.S, p.B, 32)) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((p.flags & kHasZ) && !make_map(&mz, p.S > 0 ? p.z : stand_in, p.H * P, mS, mB))
+        return cudaErrorInvalidValue;
+    if (!make_map(&my, p.S > 0 ? p.y : stand_in, p.H * P, mS, mB, 32)) return cudaErrorInvalidValue;
+    auto kernel = varlen ? scan_tc_kernel<true> : scan_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -902,7 +943,7 @@ cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st, bool after_pr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = after_prepass ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, scan_tc_kernel, mbc, mz, my, p);
+    return cudaLaunchKernelEx(&cfg, kernel, mbc, mz, my, p);
 }
 
 }  // namespace ssd
