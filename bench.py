@@ -33,6 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 import ssd_inputs as si  # noqa: E402
@@ -429,6 +430,48 @@ def bench_extra(ssd, dev, stream, args):
                      "calls_per_pass": ncalls, "rows_per_pass": rows,
                      "host_ms_per_pass": round(min(host_s) * 1e3, 3)}
         del inp, run
+    # packed sequences with states at pool slots: 16 sequences of log-uniform
+    # 1..2048 rows (seeded), at slots of a 64-slot pool, a quarter of them fresh
+    sh = si.PREFILL
+    gl = torch.Generator().manual_seed(33)
+    lens = [int(v) for v in torch.exp(torch.rand(16, generator=gl) * np.log(2048.0)).round()]
+    T = sum(lens)
+    H, P, N, G, W = sh.nheads, sh.headdim, sh.dstate, sh.ngroups, sh.conv_width
+    prm = {k: v.to(dev) for k, v in si.params(sh, seed=31).items()}
+    inp = si.prefill_inputs(sh.with_(seqlen=T), seed=32, device=dev)
+    rows = {k: inp[k][0].contiguous() for k in ("xbc", "dt_raw", "z")}
+    del inp
+    nslots = 64
+    spool = torch.randn((nslots, H, P, N), device=dev) * 0.1
+    cpool = torch.randn((nslots, W - 1, sh.cdim), device=dev).to(torch.bfloat16)
+    slots = torch.randperm(nslots, generator=gl)[:16].to(torch.int32).to(dev)
+    init = (torch.arange(16) % 4 != 0).to(torch.int32).to(dev)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev)
+    y = torch.empty((T, H, P), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(T * 2 * G * N * 2, dtype=torch.uint8, device=dev)
+    d = ssd.dims(16, T, H, P, N, G, W)
+    flags = ssd.SSD_DT_SOFTPLUS | ssd.SSD_HAS_Z
+
+    def varlen_call():
+        ssd.ssd_chunk_scan_varlen(d, ssd.SSD_BF16, flags, cu, slots, init, nslots, rows["xbc"],
+                                  prm["conv_w"], prm["conv_b"], cpool, rows["dt_raw"],
+                                  prm["dt_bias"], prm["A"], prm["D"], rows["z"], spool, y, ws,
+                                  stream)
+    for _ in range(3):
+        varlen_call()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    queue_ahead(50e-6, 10)
+    ev0.record(stream)
+    for _ in range(10):
+        varlen_call()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / 10
+    out["varlen_16_sequences_1_to_2048_rows_at_slots"] = {
+        "tokens_per_s": round(T / (ms / 1e3), 1), "ms_per_call": round(ms, 4), "rows": T,
+        "lengths": lens}
+    del rows, spool, cpool, y, ws
     # the gated group RMSNorm after the scan, at the prefill width (2048 rows x
     # 8192 channels, 8 groups): HBM-bound, y and z read, out written once
     sh = si.PREFILL
