@@ -138,53 +138,91 @@ __global__ void __launch_bounds__(128) conv1d_rows_kernel(ConvParams p)
     }
 }
 
-// Packed sequences: one CTA column per row, one thread per 16 bytes of
-// channels.  The row's sequence is found by binary search over cu_seqlens
-// (the last i with cu_seqlens[i] <= row, so empty sequences are skipped); taps
-// before the sequence's first row read its conv state at its slot (zeros for a
-// fresh sequence, or for a slot out of range, which the scan reports).
+// Packed sequences: as conv1d_rows_kernel (8 rows per thread, the raw rows of
+// the window and the taps in registers), with the sequence of each row found
+// from cu_seqlens (a binary search for the first row, the last i with
+// cu_seqlens[i] <= row, then a walk past sequence ends, skipping empty
+// sequences).  A tap that reaches before its row's sequence start reads that
+// sequence's conv state at its slot instead (zeros for a fresh sequence, or
+// for a slot out of range, which the scan reports).  Rows run along grid.x.
 template <typename T, int W>
 __global__ void __launch_bounds__(128) conv1d_rows_varlen_kernel(ConvParams p)
 {
     sm100::griddep_launch_dependents();
     constexpr int V = Vec16<T>::n;
+    constexpr int R = kRowsPerThread;
     const int nvec = p.ncols / V;
     const int cv = blockIdx.y * blockDim.x + threadIdx.x;
     if (cv >= nvec) return;
-    const long long r = blockIdx.x;
-    int lo = 0, hi = p.nseq;  // cu[lo] <= r < cu[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (p.cu_seqlens[mid] <= r) lo = mid;
-        else hi = mid;
-    }
-    const long long r0 = p.cu_seqlens[lo];
-    const int t = (int)(r - r0);
-    const int slot = p.slot_ids[lo];
-    const bool from_state = p.st_in != nullptr && (p.has_init == nullptr || p.has_init[lo] != 0) &&
-                            slot >= 0 && slot < p.num_slots;
+    const long long t0 = (long long)blockIdx.x * R;
+    const int nrows = (int)min((long long)R, (long long)p.S - t0);
     const int c0 = p.col0 + cv * V, o0 = cv * V;
     const T* __restrict__ x = static_cast<const T*>(p.x);
     const T* __restrict__ st = static_cast<const T*>(p.st_in);
-    float o[V];
+    T* __restrict__ out = static_cast<T*>(p.out);
+
+    // raw rows t0-(W-1) .. t0+R-1 (rows outside [0, S) read as zeros)
+    uint4 u[R + W - 1];
 #pragma unroll
-    for (int j = 0; j < V; ++j) o[j] = p.bias ? __ldg(p.bias + c0 + j) : 0.0f;
-#pragma unroll
-    for (int k = 0; k < W; ++k) {
-        const int u = t - (W - 1) + k;  // row of the sequence this tap reads
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        // (a malformed cu_seqlens, which the scan reports, reads nothing out of range)
-        if (u >= 0) {
-            if (r0 + u >= 0 && r0 + u <= r) raw = Vec16<T>::load(x + (r0 + u) * p.C + c0);
-        } else if (from_state) raw = Vec16<T>::load(st + ((size_t)slot * (W - 1) + (W - 1 + u)) * p.C + c0);
-        float f[V];
-        Vec16<T>::unpack(raw, f);
-#pragma unroll
-        for (int j = 0; j < V; ++j) o[j] = fmaf(__ldg(p.w + (size_t)(c0 + j) * W + k), f[j], o[j]);
+    for (int k = 0; k < R + W - 1; ++k) {
+        const long long r = t0 - (W - 1) + k;
+        u[k] = (r >= 0 && r < p.S) ? Vec16<T>::load(x + r * p.C + c0) : make_uint4(0, 0, 0, 0);
     }
+    float w[W][V], bias[V];
 #pragma unroll
-    for (int j = 0; j < V; ++j) o[j] = Vec16<T>::silu(o[j]);
-    Vec16<T>::store(static_cast<T*>(p.out) + r * p.out_stride + o0, o);
+    for (int j = 0; j < V; ++j) {
+        bias[j] = p.bias ? __ldg(p.bias + c0 + j) : 0.0f;
+        const float* wc = p.w + (size_t)(c0 + j) * W;
+        if (W == 4 && (reinterpret_cast<uintptr_t>(p.w) & 15) == 0) {
+            const float4 q = __ldg(reinterpret_cast<const float4*>(wc));
+            w[0][j] = q.x; w[1 % W][j] = q.y; w[2 % W][j] = q.z; w[3 % W][j] = q.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < W; ++k) w[k][j] = __ldg(wc + k);
+        }
+    }
+    // the sequence of row t0
+    int lo = 0, hi = p.nseq;  // cu[lo] <= t0 < cu[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.cu_seqlens[mid] <= t0) lo = mid;
+        else hi = mid;
+    }
+    int i = lo;
+    long long s0 = p.cu_seqlens[i], s1 = p.cu_seqlens[i + 1];
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        if (rr >= nrows) break;
+        const long long r = t0 + rr;
+        while (r >= s1 && i + 1 < p.nseq) {  // the next non-empty sequence
+            ++i;
+            s0 = s1;
+            s1 = p.cu_seqlens[i + 1];
+        }
+        float o[V];
+#pragma unroll
+        for (int j = 0; j < V; ++j) o[j] = bias[j];
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            const long long src = r - (W - 1) + k;  // the row this tap reads
+            uint4 raw = u[rr + k];
+            if (src < s0) {  // before the sequence's first row: its conv state
+                raw = make_uint4(0, 0, 0, 0);
+                const int slot = p.slot_ids[i];
+                const long long sr = (W - 1) + (src - s0);  // row of the state
+                if (st != nullptr && (p.has_init == nullptr || p.has_init[i] != 0) && slot >= 0 &&
+                    slot < p.num_slots && sr >= 0)
+                    raw = Vec16<T>::load(st + ((size_t)slot * (W - 1) + sr) * p.C + c0);
+            }
+            float f[V];
+            Vec16<T>::unpack(raw, f);
+#pragma unroll
+            for (int j = 0; j < V; ++j) o[j] = fmaf(w[k][j], f[j], o[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < V; ++j) o[j] = Vec16<T>::silu(o[j]);
+        Vec16<T>::store(out + r * p.out_stride + o0, o);
+    }
 }
 
 // conv_state_out[b, j, c] = u[b, S + j, c] with u = [state_in ; x].  One
@@ -218,8 +256,8 @@ cudaError_t launch_rows_t(ConvParams p, cudaStream_t st)
     if (p.ncols % V != 0 || p.col0 % V != 0 || p.out_stride % V != 0) return cudaErrorInvalidValue;
     const int nvec = p.ncols / V;
     dim3 block(128);
-    if (p.cu_seqlens != nullptr) {  // packed sequences: one CTA column per row
-        dim3 vgrid((unsigned)p.S, (nvec + 127) / 128);
+    if (p.cu_seqlens != nullptr) {  // packed sequences: rows along grid.x
+        dim3 vgrid((unsigned)((p.S + kRowsPerThread - 1) / kRowsPerThread), (nvec + 127) / 128);
         switch (p.W) {
 #define SSD_CONV_VCASE(w) \
     case w: conv1d_rows_varlen_kernel<T, w><<<vgrid, block, 0, st>>>(p); break;
