@@ -62,8 +62,8 @@ ssd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR
 // Calls of at most this many rows per sequence take the row-exact kernel even
 // in bf16 (one CTA per (sequence, head), the state in registers, no chunk
 // pipeline to fill).  Measured at 4 sequences x 128 heads: the tensor-core
-// path costs ~37 us for any call of up to 128 rows, the row kernel ~23 us for
-// one row and ~3.4 us more per row, so the row kernel wins up to 4 rows.
+// path costs ~37 us for any call of up to 128 rows, the row kernel ~25 us for
+// one row and ~2.7 us more per row, so the row kernel wins up to 4 rows.
 #ifndef SSD_SHORT_CALL_ROWS
 #define SSD_SHORT_CALL_ROWS 4
 #endif

@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(1024) scan_simt_kernel(ScanParams p, int NQ)
     float* halo = post + kRows * CH;            // [HW * CH]
     float* dts = halo + HW * CH;                // [kRows]
     float* dAs = dts + kRows;                   // [kRows]
+    float* wsm = dAs + kRows;                   // conv taps [CH * W], then bias [CH]
 
     const T* xbc = static_cast<const T*>(p.xbc);
     const T* zz = static_cast<const T*>(p.z);
@@ -78,7 +79,14 @@ __global__ void __launch_bounds__(1024) scan_simt_kernel(ScanParams p, int NQ)
             const int r = i / CH, c = i % CH;
             halo[i] = cs ? to_f32(cs[((size_t)b * HW + r) * Cdim + gch(c)]) : 0.0f;
         }
+        // the taps and bias of this head's columns, once (not per row and tap)
+        for (int i = tid; i < CH * p.W; i += nt) wsm[i] = p.conv_w[(size_t)gch(i / p.W) * p.W + i % p.W];
+        for (int c = tid; c < CH; c += nt) wsm[CH * p.W + c] = p.conv_b ? p.conv_b[gch(c)] : 0.0f;
     }
+    // 16-byte row loads when every column segment (x | B | C) is a whole number
+    // of vectors (segment starts are then vector aligned too)
+    constexpr int VEC = 16 / (int)sizeof(T);
+    const bool vec_rows = P % VEC == 0 && N % VEC == 0;
     const float Ah = p.A[h];
     const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
     const float Dh = p.D ? p.D[h] : 0.0f;
@@ -87,9 +95,21 @@ __global__ void __launch_bounds__(1024) scan_simt_kernel(ScanParams p, int NQ)
         const int rows = min(kRows, p.S - t0);
         __syncthreads();
         for (int i = tid; i < HW * CH; i += nt) raw[i] = halo[i];
-        for (int i = tid; i < rows * CH; i += nt) {
-            const int r = i / CH, c = i % CH;
-            raw[HW * CH + i] = to_f32(xbc[((size_t)b * p.S + t0 + r) * Cdim + gch(c)]);
+        if (vec_rows) {
+            const int vpr = CH / VEC;  // vectors per row
+            for (int i = tid; i < rows * vpr; i += nt) {
+                const int r = i / vpr, c = (i % vpr) * VEC;
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+                    xbc + ((size_t)b * p.S + t0 + r) * Cdim + gch(c)));
+                const T* e = reinterpret_cast<const T*>(&v);
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) raw[HW * CH + r * CH + c + k] = to_f32(e[k]);
+            }
+        } else {
+            for (int i = tid; i < rows * CH; i += nt) {
+                const int r = i / CH, c = i % CH;
+                raw[HW * CH + i] = to_f32(xbc[((size_t)b * p.S + t0 + r) * Cdim + gch(c)]);
+            }
         }
         for (int r = tid; r < rows; r += nt) {
             float v = p.dt[((size_t)b * p.S + t0 + r) * H + h];
@@ -101,10 +121,9 @@ __global__ void __launch_bounds__(1024) scan_simt_kernel(ScanParams p, int NQ)
         for (int i = tid; i < rows * CH; i += nt) {
             const int r = i / CH, c = i % CH;
             if (conv) {
-                const int gc = gch(c);
-                float v = p.conv_b ? p.conv_b[gc] : 0.0f;
-                for (int k = 0; k < p.W; ++k) v = fmaf(p.conv_w[(size_t)gc * p.W + k], raw[(r + k) * CH + c], v);
-                post[i] = v / (1.0f + expf(-v));
+                float v = wsm[CH * p.W + c];
+                for (int k = 0; k < p.W; ++k) v = fmaf(wsm[c * p.W + k], raw[(r + k) * CH + c], v);
+                post[i] = __fdividef(v, 1.0f + __expf(-v));  // silu
             } else {
                 post[i] = raw[i];
             }
@@ -146,7 +165,8 @@ cudaError_t launch_t(const ScanParams& p, const SimtShape& s, cudaStream_t st)
     const int CH = p.P + 2 * p.N;
     const int HW = p.conv_w ? p.W - 1 : 0;
     const size_t smem = sizeof(float) * ((size_t)(kRows + HW) * CH + (size_t)kRows * CH +
-                                         (size_t)HW * CH + 2 * kRows);
+                                         (size_t)HW * CH + 2 * kRows +
+                                         (p.conv_w ? (size_t)CH * (p.W + 1) : 0));
     auto kern = scan_simt_kernel<T, NPT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
