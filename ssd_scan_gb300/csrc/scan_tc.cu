@@ -27,6 +27,16 @@
 //     xv = x, xs = w o x with w_s = exp(min(gamma_Q - gamma_s, 0)) dt_s,
 //     G3 goes to its own accumulator Yo, y = Y + u_t Yo,
 //     h <- exp(gamma_Q) h + dH.
+//     Split blocks: when gamma never rises in the chunk (every a <= 0), the
+//     decay of a 32-row block j of columns splits at its middle row m_j as
+//     exp(gamma_t - gamma_m) exp(gamma_m - gamma_s).  The column factor
+//     V_s = exp(gamma_m - gamma_s) dt_s scales the x rows G2 reads
+//     (xv = V o x) and the mask keeps one factor per row, R_t =
+//     exp(gamma_t - gamma_m): M = mask(CB R_t) with D R_t / dt_t on the
+//     diagonal.  Below the diagonal R_t <= 1; inside block j both factors
+//     stay within 2^60 when neither half of the block decays by more than
+//     2^60, the condition for the split (else the block's columns keep the
+//     per-element exponential and xv = x).
 // The skip term D x_t rides on the diagonal of M.  The masked CB is written
 // back into TMEM (bf16 pairs) and read from there by G2, so it never passes
 // through shared memory.
@@ -96,15 +106,20 @@ constexpr uint32_t kColDH = 448;  // dH fp32 [n][p]                         64
 // Below this total chunk decay (log2 units) the mask factors as
 // exp(gamma_t) * exp(-gamma_s): every factor stays within fp32 (2^90 < 2^127).
 constexpr float kFactorMinLog2 = -90.0f;
+// Exact form: a column block splits at its middle row when neither half decays
+// by more than this (log2 units): R_t and V_s / dt_s then stay within 2^60.
+constexpr float kSplitMaxLog2 = 60.0f;
 
 struct __align__(16) ChunkVals {  // per-chunk row values, written by the gamma warp
     float g2h[Q], g2l[Q];      // gamma * log2(e), double-float (hi, lo)
     float dts[Q];              // dt_s (0 past the last row)
     float sc[Q];               // x scale of G4's operand: v_s (factored) or w_s (exact)
-    float dec[Q];              // exp(min(gamma_t, 0))
+    float vb[Q];               // scale of the x rows G2 reads in the exact form: V_s
+                               // (split blocks) or 1
     float decS;                // exp(min(gamma_Q, 0))
     int factored;              // which form of the decay this chunk uses
-    int pad[2];
+    int split;                 // exact form: bit j set when column block j is split
+    int pad;
 };
 
 struct __align__(1024) TcSmem {
@@ -140,7 +155,7 @@ static_assert(sizeof(((TcSmem*)nullptr)->XR[0]) % 1024 == 0, "tile");
 static_assert(offsetof(TcSmem, Hs) % 1024 == 0, "tile");
 static_assert(sizeof(ChunkVals) % 16 == 0 && offsetof(TcSmem, cv) % 16 == 0, "float4 rows");
 static_assert(offsetof(ChunkVals, g2l) % 16 == 0 && offsetof(ChunkVals, dts) % 16 == 0, "float4");
-static_assert(offsetof(ChunkVals, sc) % 16 == 0 && offsetof(ChunkVals, dec) % 16 == 0, "float4");
+static_assert(offsetof(ChunkVals, sc) % 16 == 0 && offsetof(ChunkVals, vb) % 16 == 0, "float4");
 static_assert(offsetof(TcSmem, wconv) % 16 == 0 && offsetof(TcSmem, bconv) % 16 == 0, "float4");
 static_assert(offsetof(TcSmem, Zt) % 1024 == 0 && offsetof(TcSmem, Yt) % 1024 == 0, "tile");
 static_assert(offsetof(TcSmem, full_c) % 8 == 0, "mbarriers");
@@ -538,15 +553,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float gLh = __shfl_sync(0xffffffffu, th, 31) * kLog2e;
             const float gLl = __shfl_sync(0xffffffffu, tl, 31) * kLog2e;
             const bool factored = __all_sync(0xffffffffu, dt_ok) && Ah <= 0.0f && gLh + gLl >= kFactorMinLog2;
-            float o_h[4], o_l[4], o_sc[4], o_dec[4];
+            float o_h[4], o_l[4], o_sc[4], o_vb[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float g2h = gh[i] * kLog2e, g2l = gl[i] * kLog2e;
-                o_h[i] = g2h;
-                o_l[i] = g2l;
-                o_dec[i] = ex2_fast(fminf(g2h + g2l, 0.0f));
-                o_sc[i] = factored ? ex2_fast(-(g2h + g2l)) * dt[i]
-                                   : ex2_fast(fminf((gLh - g2h) + (gLl - g2l), 0.0f)) * dt[i];
+                o_h[i] = gh[i] * kLog2e;
+                o_l[i] = gl[i] * kLog2e;
+                o_sc[i] = factored ? ex2_fast(-(o_h[i] + o_l[i])) * dt[i]
+                                   : ex2_fast(fminf((gLh - o_h[i]) + (gLl - o_l[i]), 0.0f)) * dt[i];
+            }
+            // exact form: the split of this lane's 32-row block (lanes 8j .. 8j+7
+            // hold block j) from gamma at its first, middle and last rows, when
+            // gamma never rises in the chunk and every row has dt > 0 with D / dt
+            // bounded (the diagonal's D R_t / dt_t).  This warp runs close to the
+            // chunk period, so factored chunks skip it.
+            int split_bits = 0;
+            if (!factored) {
+                const int l0 = lane & ~7;
+                const float gfh = __shfl_sync(0xffffffffu, o_h[0], l0), gfl = __shfl_sync(0xffffffffu, o_l[0], l0);
+                const float gmh = __shfl_sync(0xffffffffu, o_h[0], l0 + 4), gml = __shfl_sync(0xffffffffu, o_l[0], l0 + 4);
+                const float geh = __shfl_sync(0xffffffffu, o_h[3], l0 + 7), gel = __shfl_sync(0xffffffffu, o_l[3], l0 + 7);
+                bool lane_ok = Ah <= 0.0f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    lane_ok = lane_ok && (4 * lane + i >= rows || (dt[i] > 0.0f && Dabs < dt[i] * 0x1p60f));
+                lane_ok = lane_ok && (gfh - gmh) + (gfl - gml) <= kSplitMaxLog2 &&
+                          (gmh - geh) + (gml - gel) <= kSplitMaxLog2;
+                const bool mono = __all_sync(0xffffffffu, Ah <= 0.0f && dt[0] >= 0.0f && dt[1] >= 0.0f &&
+                                                              dt[2] >= 0.0f && dt[3] >= 0.0f);
+                const unsigned blk_ok = __ballot_sync(0xffffffffu, lane_ok);
+                const bool split = mono && ((blk_ok >> l0) & 0xffu) == 0xffu;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) split_bits |= (mono && ((blk_ok >> (8 * k)) & 0xffu) == 0xffu) << k;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o_vb[i] = split ? ex2_fast((gmh - o_h[i]) + (gml - o_l[i])) * dt[i] : 1.0f;
             }
             // cv[c % kCv] is free once the epilogue of chunk c-kCv is done
             const bool ok = c < kCv || wait_or_abort(s, &s.epidone[c % kCv], ((c / kCv) - 1) & 1);
@@ -555,10 +595,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             reinterpret_cast<float4*>(cv.g2l)[lane] = make_float4(o_l[0], o_l[1], o_l[2], o_l[3]);
             reinterpret_cast<float4*>(cv.dts)[lane] = make_float4(dt[0], dt[1], dt[2], dt[3]);
             reinterpret_cast<float4*>(cv.sc)[lane] = make_float4(o_sc[0], o_sc[1], o_sc[2], o_sc[3]);
-            reinterpret_cast<float4*>(cv.dec)[lane] = make_float4(o_dec[0], o_dec[1], o_dec[2], o_dec[3]);
+            if (!factored)  // (read only by exact chunks)
+                reinterpret_cast<float4*>(cv.vb)[lane] = make_float4(o_vb[0], o_vb[1], o_vb[2], o_vb[3]);
             if (lane == 0) {
                 cv.decS = ex2_fast(fminf(gLh + gLl, 0.0f));
                 cv.factored = factored;
+                cv.split = split_bits;
             }
             mbar_arrive(&s.cvready[c % kCv]);
         }
@@ -601,6 +643,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool need_x = cv.factored == 0;  // x rows feed G2 in the exact form
             const float4 sc4 = *reinterpret_cast<const float4*>(&cv.sc[4 * rq]);
             const float scs[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+            float vbs[4] = {1.f, 1.f, 1.f, 1.f};
+            if (need_x) {
+                const float4 vb4 = *reinterpret_cast<const float4*>(&cv.vb[4 * rq]);
+                vbs[0] = vb4.x; vbs[1] = vb4.y; vbs[2] = vb4.z; vbs[3] = vb4.w;
+            }
             // out[i] = b + sum_k w[k] u[i+k] over raw rows i .. i+3, tap by tap (only
             // one tap's weights live at a time: registers are scarce with 18 warps)
             float2 acc[4][2];
@@ -639,7 +686,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (r >= rows) x0 = x1 = make_float2(0.f, 0.f);
                 const float2 sc2 = make_float2(scs[i], scs[i]);
                 const uint32_t off = chunk_off(r, jq >> 1) + coff;
-                if (need_x) at<uint2>(s.XR[c & 1], off) = make_uint2(pack2(x0), pack2(x1));
+                if (need_x) {
+                    const float2 vb2 = make_float2(vbs[i], vbs[i]);
+                    at<uint2>(s.XR[c & 1], off) = make_uint2(pack2(__fmul2_rn(vb2, x0)), pack2(__fmul2_rn(vb2, x1)));
+                }
                 at<uint2>(s.XS[c & 1], off) = make_uint2(pack2(__fmul2_rn(sc2, x0)), pack2(__fmul2_rn(sc2, x1)));
             }
         };
@@ -683,22 +733,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             const ChunkVals& cv = s.cv[c % kCv];
 
             // ---- mask(c): CB -> M in TMEM (this warp's 32-column block) ----
+            const bool fac = cv.factored != 0;
             if (ok) ok = wait_or_abort(s, &s.g1, c & 1);
             if (__all_sync(0xffffffffu, ok)) {
                 if (j <= q) {
                     tc_fence_after();
-                    const bool fac = cv.factored != 0;
-                    const float g2h_t = cv.g2h[t], g2l_t = cv.g2l[t];
-                    // the skip term on the diagonal: D (exact) or D / dt_t (factored:
-                    // y = u_t Y and u_t v_t = dt_t); rows past the end get nothing
-                    const float diag = (j == q && t < rows) ? (fac ? __fdividef(Dh, cv.dts[t]) : Dh) : 0.0f;
+                    // exact form, a split column block: one factor per row, R_t =
+                    // exp(gamma_t - gamma_m), m the block's middle row (the column
+                    // factor is on the x rows)
+                    const bool split = !fac && ((cv.split >> j) & 1);
+                    const float g2h_t = cv.g2h[t], g2l_t = cv.g2l[t], dts_t = cv.dts[t];
+                    const float gmh = cv.g2h[32 * j + 16], gml = cv.g2l[32 * j + 16];
+                    const float rt = split ? ex2_fast((g2h_t - gmh) + (g2l_t - gml)) : 1.0f;
+                    // the skip term on the diagonal, so that M_tt xv_t carries D x_t:
+                    // D / dt_t (factored: y = u_t Y, u_t v_t = dt_t), D R_t / dt_t (split:
+                    // xv_t = V_t x_t, R_t V_t = dt_t) or D; rows past the end get nothing
+                    const float diag = (j == q && t < rows)
+                                           ? (fac ? __fdividef(Dh, dts_t) : split ? __fdividef(Dh * rt, dts_t) : Dh)
+                                           : 0.0f;
 #pragma unroll 1
                     for (int hf = 0; hf < 2; ++hf) {  // 16 columns at a time
                         const int c0 = 32 * j + 16 * hf;
                         float v[16];
                         tmem_ld16(tbase + lane_off + kColCB + c0, v);
                         tmem_ld_wait();
-                        if (!fac) {
+                        if (split) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] *= rt;
+                        } else if (!fac) {
 #pragma unroll
                             for (int q4 = 0; q4 < 4; ++q4) {
                                 const int sb = c0 + 4 * q4;
@@ -736,7 +798,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) ok = wait_or_abort(s, &s.g4, c & 1) && wait_or_abort(s, &s.g3, c & 1);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
-                const bool fac = cv.factored != 0;
                 const float2 dS = make_float2(cv.decS, cv.decS);
                 const float2 bS = fac ? dS : make_float2(1.0f, 1.0f);
                 float v[16];
@@ -772,8 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && has_z) ok = wait_or_abort(s, &s.full_z, c & 1);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
-                const bool fac = cv.factored != 0;
-                const float dec = cv.dec[t];
+                const float dec = ex2_fast(fminf(cv.g2h[t] + cv.g2l[t], 0.0f));  // exp(min(gamma_t, 0))
                 const float2 dd = make_float2(dec, dec);
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {  // 8 columns at a time

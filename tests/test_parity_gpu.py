@@ -293,3 +293,45 @@ def test_decay_range_across_factored_threshold(scale):
     dev["A"] = cpu["A"].cuda()
     y, h, cs = gpu_prefill(shape, dev)
     _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
+
+
+@pytest.mark.parametrize("row", [0, 31, 32, 63, 95, 127])
+def test_exact_chunk_decay_spike_at_block_edges(row):
+    """A spike of decay (~e^-300 per head) at a row on either side of a 32-row
+    block edge of the mask: the exact form splits the decay of the blocks below
+    the diagonal at their last row, so a spike there must land on the right
+    side of the split."""
+    shape = si.Shape(batch=1, seqlen=200, nheads=4, headdim=64, dstate=128, ngroups=1)
+    cpu, dev = make_problem(shape, act=torch.bfloat16, seed=11)
+    dt_raw = cpu["dt_raw"].clone()
+    dt_raw[0, row, :] = 60.0
+    dt_raw[0, 128 + row // 2, :] = 40.0  # and one in the second, ragged chunk
+    cpu["dt_raw"] = dt_raw
+    dev["dt_raw"] = dt_raw.cuda()
+    y, h, cs = gpu_prefill(shape, dev, [70, 130])
+    assert torch.isfinite(y.float()).all() and torch.isfinite(h).all()
+    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
+
+
+def test_exact_chunk_rising_and_falling_gamma():
+    """dt taken as given (no softplus) with negative entries: gamma rises and
+    falls inside a chunk.  The chunk form then differs from the row recurrence
+    (each exponent is clamped at 0), so the reference is the oracle's chunk
+    form over the same 128-row chunks; no column block may split its decay at
+    a middle row here (the clamps do not factor)."""
+    shape = si.Shape(batch=1, seqlen=256, nheads=4, headdim=64, dstate=128, ngroups=1)
+    cpu, dev = make_problem(shape, act=torch.bfloat16, seed=13)
+    g = torch.Generator().manual_seed(5)
+    dt_raw = torch.rand(cpu["dt_raw"].shape, generator=g) * 0.2 - 0.05  # [-0.05, 0.15)
+    cpu["dt_raw"] = dt_raw
+    dev["dt_raw"] = dt_raw.cuda()
+    y, h, cs = gpu_prefill(shape, dev, dt_softplus=False)
+    assert torch.isfinite(y.float()).all() and torch.isfinite(h).all()
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    xbc, _ = oracle.conv1d(f64(cpu["xbc"]), f64(cpu["conv_w"]), f64(cpu["conv_b"]),
+                           f64(cpu.get("conv_state")), apply_silu=True)
+    yo, ho = oracle.ssd_chunked(xbc, f64(dt_raw), f64(cpu["A"]), [128, 128], H=H, P=P, N=N, G=G,
+                                dt_bias=f64(cpu["dt_bias"]), D=f64(cpu["D"]), z=f64(cpu.get("z")),
+                                h0=f64(cpu.get("ssm_state")), dt_softplus=False)
+    assert_close(y, yo, TOL[torch.bfloat16], count=y.numel(), what="y")
+    assert_close(h, ho, TOL[torch.bfloat16], count=h.numel(), what="ssm_state")
