@@ -643,11 +643,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool need_x = cv.factored == 0;  // x rows feed G2 in the exact form
             const float4 sc4 = *reinterpret_cast<const float4*>(&cv.sc[4 * rq]);
             const float scs[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
-            float vbs[4] = {1.f, 1.f, 1.f, 1.f};
-            if (need_x) {
-                const float4 vb4 = *reinterpret_cast<const float4*>(&cv.vb[4 * rq]);
-                vbs[0] = vb4.x; vbs[1] = vb4.y; vbs[2] = vb4.z; vbs[3] = vb4.w;
-            }
             // out[i] = b + sum_k w[k] u[i+k] over raw rows i .. i+3, tap by tap (only
             // one tap's weights live at a time: registers are scarce with 18 warps)
             float2 acc[4][2];
@@ -687,7 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float2 sc2 = make_float2(scs[i], scs[i]);
                 const uint32_t off = chunk_off(r, jq >> 1) + coff;
                 if (need_x) {
-                    const float2 vb2 = make_float2(vbs[i], vbs[i]);
+                    const float vbi = cv.vb[4 * rq + i];
+                    const float2 vb2 = make_float2(vbi, vbi);
                     at<uint2>(s.XR[c & 1], off) = make_uint2(pack2(__fmul2_rn(vb2, x0)), pack2(__fmul2_rn(vb2, x1)));
                 }
                 at<uint2>(s.XS[c & 1], off) = make_uint2(pack2(__fmul2_rn(sc2, x0)), pack2(__fmul2_rn(sc2, x1)));
@@ -742,9 +738,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // exp(gamma_t - gamma_m), m the block's middle row (the column
                     // factor is on the x rows)
                     const bool split = !fac && ((cv.split >> j) & 1);
-                    const float g2h_t = cv.g2h[t], g2l_t = cv.g2l[t], dts_t = cv.dts[t];
-                    const float gmh = cv.g2h[32 * j + 16], gml = cv.g2l[32 * j + 16];
-                    const float rt = split ? ex2_fast((g2h_t - gmh) + (g2l_t - gml)) : 1.0f;
+                    const float dts_t = cv.dts[t];
+                    float g2h_t = 0.0f, g2l_t = 0.0f, rt = 1.0f;
+                    if (!fac) {  // (factored chunks read neither)
+                        g2h_t = cv.g2h[t];
+                        g2l_t = cv.g2l[t];
+                        if (split)
+                            rt = ex2_fast((g2h_t - cv.g2h[32 * j + 16]) + (g2l_t - cv.g2l[32 * j + 16]));
+                    }
                     // the skip term on the diagonal, so that M_tt xv_t carries D x_t:
                     // D / dt_t (factored: y = u_t Y, u_t v_t = dt_t), D R_t / dt_t (split:
                     // xv_t = V_t x_t, R_t V_t = dt_t) or D; rows past the end get nothing
