@@ -173,7 +173,7 @@ SSD_API ssd_status ssd_chunk_scan_workspace_size(const ssd_dims* dims, ssd_dtype
 
 /*
  * ssd_chunk_scan_static_ws -- ssd_chunk_scan for callers that cannot
- * allocate device memory.  The paper has no counterpart: this is a library
+ * allocate device memory.  None of the cited pages has a counterpart: this is a library
  * convenience, not a step of the method.
  *
  * Who needs it: code that runs inside a host program which owns every device
