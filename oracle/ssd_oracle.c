@@ -56,7 +56,10 @@
 #include <pthread.h>
 
 /* ORACLE_MUTANT (default 0) plants one known mistake, for the mutation tests
- * that prove the pins can see it; a normal build never defines it. */
+ * that prove the pins can see it; a normal build never defines it.  In the
+ * chunk form: 10 drops every clamp, 11 takes gamma_L from a separate
+ * reduction (fp32, rows in reverse) with the state exponent unclamped, 12
+ * clamps gamma_t and gamma_s one by one instead of their difference. */
 #ifndef ORACLE_MUTANT
 #define ORACLE_MUTANT 0
 #endif
@@ -226,6 +229,16 @@ static void seq_one(const oracle_scan_args* a, int b, int h, double* st)
  * gamma_L is the last element of the cumulative sum, not a separate sum.
  * No step of the recurrence above is used here.
  */
+/* exp of the clamped exponent gamma_t - gamma_s of the chunk form ([TRT]
+ * Implementation: every exponent is at most 0). */
+static double decay_of(double gt, double gs)
+{
+    if (ORACLE_MUTANT == 12) return exp((gt < 0.0 ? gt : 0.0) - (gs < 0.0 ? gs : 0.0));
+    double e = gt - gs;
+    if (e > 0.0 && ORACLE_MUTANT != 10) e = 0.0;
+    return exp(e);
+}
+
 static void chunked_one(const oracle_scan_args* a, int b, int h, double* st, double* gam,
                         double* dts, double* st_next)
 {
@@ -253,28 +266,29 @@ static void chunked_one(const oracle_scan_args* a, int b, int h, double* st, dou
                     const double* rs = a->xbc + ((size_t)b * S + r0 + s) * Cdim;
                     double cb = 0.0;
                     for (int n = 0; n < N; ++n) cb += rt[col_C(d, g, n)] * rs[col_B(d, g, n)];
-                    double e = gam[t] - gam[s];
-                    if (e > 0.0) e = 0.0;
-                    yv += cb * exp(e) * dts[s] * rs[col_x(d, h, p)];
+                    yv += cb * decay_of(gam[t], gam[s]) * dts[s] * rs[col_x(d, h, p)];
                 }
                 double ch = 0.0;
                 for (int n = 0; n < N; ++n) ch += rt[col_C(d, g, n)] * st[(size_t)p * N + n];
-                double e0 = gam[t] < 0.0 ? gam[t] : 0.0;
-                yv += exp(e0) * ch;
+                yv += decay_of(gam[t], 0.0) * ch;
                 if (a->D) yv += a->D[h] * rt[col_x(d, h, p)];
                 gate_and_store(a, b, r0 + t, h, p, yv);
             }
         }
-        const double gL = gam[L - 1];
-        const double eL = exp(gL < 0.0 ? gL : 0.0);
+        double gL = gam[L - 1];
+        if (ORACLE_MUTANT == 11) {
+            float r = 0.0f;
+            for (int s = L - 1; s >= 0; --s) r += (float)(dts[s] * a->A[h]);
+            gL = (double)r;
+        }
+        const double eL = decay_of(gL, 0.0);
         for (int p = 0; p < P; ++p)
             for (int n = 0; n < N; ++n) {
                 double acc = eL * st[(size_t)p * N + n];
                 for (int s = 0; s < L; ++s) {
                     const double* rs = a->xbc + ((size_t)b * S + r0 + s) * Cdim;
-                    double e = gL - gam[s];
-                    if (e > 0.0) e = 0.0;
-                    acc += exp(e) * dts[s] * rs[col_x(d, h, p)] * rs[col_B(d, g, n)];
+                    const double w = ORACLE_MUTANT == 11 ? exp(gL - gam[s]) : decay_of(gL, gam[s]);
+                    acc += w * dts[s] * rs[col_x(d, h, p)] * rs[col_B(d, g, n)];
                 }
                 st_next[(size_t)p * N + n] = acc;
             }

@@ -7,7 +7,11 @@ own mutation; mutant 3 is the dropped chunk carry; the others are a reversed
 conv tap order, y read from the pre-update state, a dropped dt bias and a
 flipped decay sign in the chunk form; mutants 7-9 are in the gated group
 RMSNorm: one norm over the whole row, eps outside the square root, and the
-gate applied before the norm.
+gate applied before the norm.  Mutants 10-12 are in the chunk form's clamp
+(TensorRT-Model-Connect #2207 "Implementation": gamma_S is the last element
+of the cumulative sum, not a separate reduction, and every exponent is
+clamped at 0): no clamp at all, gamma_L from a separate fp32 reduction with
+its state exponent unclamped, and gamma_t, gamma_s clamped one by one.
 """
 import pytest
 
@@ -31,10 +35,13 @@ PINS = [
     pins.test_rmsnorm_constant_group_hand_value,
     pins.test_rmsnorm_groups_are_independent,
     pins.test_rmsnorm_gate_acts_after_the_norm,
+    pins.test_chunk_form_clamp_hand_values,
+    pins.test_chunk_form_clamp_carries_across_chunks,
+    lambda: pins.test_huge_decay_limit("chunked"),
 ]
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12])
 def test_pins_catch_mutant(mutant, tmp_path, monkeypatch):
     lib = oracle.open_library(oracle.build(out_path=str(tmp_path / f"m{mutant}.so"),
                                            mutant=mutant))

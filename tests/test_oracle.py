@@ -159,6 +159,50 @@ def test_chunked_equals_sequential(parts, with_z):
     assert _relerr(h2, h1) < 1e-12
 
 
+def test_chunk_form_clamp_hand_values():
+    """The clamp of the chunk form where gamma rises (TensorRT-Model-Connect
+    #2207 "Implementation": every exponent of the chunk form is at most 0).
+
+    One chunk of 3 rows, H = P = N = G = 1, dt taken as given, A = -1,
+    dt = (1, -2, 0.5): a = (-1, 2, -0.5), gamma = (-1, 1, 0.5), gamma_L = 0.5.
+    x = (1.5, -0.5, 2), B = (0.5, 2, -1), C = (1, -1.5, 0.25), D = 0.5, h0 = 0.75,
+    so dt*x = (1.5, 1, 1).  Clamped exponents min(gamma_t - gamma_s, 0):
+      t=0: s=0 -> 0;         h0 term min(-1, 0) = -1
+      t=1: s=0 -> min(2,0)=0, s=1 -> 0;           h0 term min(1, 0) = 0
+      t=2: s=0 -> min(1.5,0)=0, s=1 -> -0.5, s=2 -> 0; h0 term 0
+      state: L - s: min(1.5,0)=0, min(-0.5,0)=-0.5, 0;  h0 term min(0.5, 0) = 0
+    y0 = 0.5*1.5 + e^-1*1*0.75 + 0.5*1.5              = 1.5 + 0.75 e^-1
+    y1 = -0.75*1.5 + -3*1 + 1*(-1.5*0.75) + 0.5*(-0.5) = -5.5
+    y2 = 0.125*1.5 + 0.5*e^-0.5*1 + -0.25*1 + 0.25*0.75 + 0.5*2 = 1.125 + 0.5 e^-0.5
+    h  = 0.75 + 1.5*0.5 + e^-0.5*1*2 + 1*(-1)          = 0.5 + 2 e^-0.5
+    Without the clamp (or with gamma_t and gamma_s clamped one by one) rows 1
+    and 2 and the state pick up factors e^1, e^1.5 or e^2 instead."""
+    xbc = _scalar_xbc([1.5, -0.5, 2.0], [0.5, 2.0, -1.0], [1.0, -1.5, 0.25])
+    dt = np.array([1.0, -2.0, 0.5]).reshape(1, 3, 1)
+    y, hS = oracle.ssd_chunked(xbc, dt, np.array([-1.0]), [3], H=1, P=1, N=1, G=1,
+                               D=np.array([0.5]), h0=np.array([[[[0.75]]]]), dt_softplus=False)
+    y_expect = np.array([1.5 + 0.75 * math.exp(-1.0), -5.5, 1.125 + 0.5 * math.exp(-0.5)])
+    assert _relerr(y.reshape(3), y_expect) < 1e-14
+    assert abs(hS.item() - (0.5 + 2.0 * math.exp(-0.5))) < 1e-14
+
+
+def test_chunk_form_clamp_carries_across_chunks():
+    """The same 3 rows as two chunks 2 + 1: gamma restarts at each chunk.
+    Chunk 1 (rows 0,1): gamma = (-1, 1), gamma_L = 1.
+      y0 = 1.5 + 0.75 e^-1 (as in one chunk); y1 = -5.5 (as in one chunk);
+      h1 = e^min(1,0)*0.75 + e^min(2,0)*1.5*0.5 + e^0*1*2 = 0.75 + 0.75 + 2 = 3.5
+    Chunk 2 (row 2): gamma = (-0.5), gamma_L = -0.5.
+      y2 = -0.25*1 + e^-0.5*0.25*3.5 + 0.5*2 = 0.75 + 0.875 e^-0.5
+      h  = e^-0.5*3.5 + 1*(-1) = 3.5 e^-0.5 - 1"""
+    xbc = _scalar_xbc([1.5, -0.5, 2.0], [0.5, 2.0, -1.0], [1.0, -1.5, 0.25])
+    dt = np.array([1.0, -2.0, 0.5]).reshape(1, 3, 1)
+    y, hS = oracle.ssd_chunked(xbc, dt, np.array([-1.0]), [2, 1], H=1, P=1, N=1, G=1,
+                               D=np.array([0.5]), h0=np.array([[[[0.75]]]]), dt_softplus=False)
+    y_expect = np.array([1.5 + 0.75 * math.exp(-1.0), -5.5, 0.75 + 0.875 * math.exp(-0.5)])
+    assert _relerr(y.reshape(3), y_expect) < 1e-14
+    assert abs(hS.item() - (3.5 * math.exp(-0.5) - 1.0)) < 1e-14
+
+
 def test_chunked_rejects_bad_partition():
     prob = _tiny_problem()
     with pytest.raises(ValueError):
