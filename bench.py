@@ -3,14 +3,16 @@ and decode-step state GB/s, each against the HBM roofline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One step = one ssd_chunk_scan call (conv + SiLU + chunked scan + z gate, with
-carried conv/SSM state) over the Nemotron-H-8B-shaped prefill workload
-(B=1 sequence, S=2048 rows, 128-row chunks, H=128, P=64, N=128, G=8, W=4, bf16
-activations, fp32 state).  Inputs rotate over several resident sets whose
-total exceeds the 129 MB L2, so no step reads its inputs from L2.  The decode
-step (256 rows at slots of a 1024-slot fp32 pool [1024,128,64,128], conv pool
-fused, 64 successive steps) is measured in the same run and reported under
-"decode".  Under torchrun every rank runs its own replica (independent
+One step = one pass of the long-prefill workload: 8 independent sequences x
+8192 rows in one ssd_chunk_scan call (conv + SiLU + chunked scan + z gate,
+carried conv/SSM state), then a second 8192-row call of each sequence fed
+with the first call's final states (Nemotron-H-8B mixer: 128-row chunks,
+H=128, P=64, N=128, G=8, W=4, bf16 activations, fp32 state).  Its inputs
+(7 GB) are far larger than the 129 MB L2.  The same run also reports the
+2048-row single-sequence prefill (inputs rotating over resident sets larger
+than L2) under "prefill_2048", and the decode step (256 rows at slots of a
+1024-slot fp32 pool [1024,128,64,128], conv pool fused, 64 successive steps)
+under "decode".  Under torchrun every rank runs its own replica (independent
 sequences: weak scaling, no collective on the data path); the times are the
 max over ranks.
 
@@ -113,14 +115,15 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host time, line)
         self.t = None
+        self.window = None  # (t0, t1) of the timed region, host clock
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -131,7 +134,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self, t0: float, t1: float):
+        """The timed region, on the host clock: only samples read inside it
+        (with 50 ms of slack for the sampler's own latency) are summarised,
+        when there are any."""
+        self.window = (t0 - 0.05, t1 + 0.05)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -147,7 +156,11 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = [ln for t, ln in self.lines]
+        if self.window is not None:
+            inside = [ln for t, ln in self.lines if self.window[0] <= t <= self.window[1]]
+            lines = inside or lines
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -236,6 +249,111 @@ def prefill_call(ssd, d, flags, prm, inp, out, ws, stream):
                        prm["D"], inp["z"], inp["ssm_state"], out["y"], out["hS"], ws, stream)
 
 
+LONG_STEP = si.LONG.with_(seqlen=2 * si.LONG.seqlen)  # two chained calls of 8192 rows
+LONG_SPLITS = [si.LONG.seqlen, si.LONG.seqlen]
+
+
+def long_step_bytes() -> dict:
+    """Algorithmic bytes of one long step: two calls of 8 x 8192 rows, each
+    with its per-row bytes and its per-sequence state bytes."""
+    per_call = prefill_bytes(si.LONG)["per_launch"]
+    pb = prefill_bytes(si.LONG)
+    return {"per_row": pb["per_row"], "per_seq_per_call": pb["per_seq"], "per_call": per_call,
+            "per_step": len(LONG_SPLITS) * per_call}
+
+
+def bench_long(ssd, dev, stream, world, rank, args):
+    """The headline: K steps of the long workload (two chained calls each),
+    queued behind a spin so that none waits on the host, timed with CUDA
+    events on the launching stream; clocks sampled during the timed loop."""
+    shape = LONG_STEP
+    prm = {k: v.to(dev) for k, v in si.params(shape, seed=rank_seed(rank)).items()}
+    inp = si.prefill_inputs(shape, seed=rank_seed(rank) + 1, device=dev)
+    run, ncalls = chained_calls(ssd, shape, prm, inp, LONG_SPLITS, dev)
+    host_s = []
+    for _ in range(args.warmup):
+        t0 = time.perf_counter()
+        run(stream)
+        host_s.append(time.perf_counter() - t0)
+    torch.cuda.synchronize()
+    host_step = statistics.median(host_s[1:] or host_s)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = ssd.ssd_launch_counts()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        _barrier(world)
+        torch.cuda.synchronize()
+        queue_ahead(host_step, args.steps)
+        ev0.record(stream)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            run(stream)
+        host_loop = (time.perf_counter() - t0) / args.steps
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        clk.mark(t0, time.perf_counter())
+        _barrier(world)
+    launches1 = ssd.ssd_launch_counts()
+    assert ssd.ssd_read_device_error(stream) == ssd.SSD_OK
+    ms = _max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+    nb = long_step_bytes()
+    hbm, hbm_src = measured_peaks()
+    achieved = nb["per_step"] / (ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": ncu_traffic("long"),
+                "peak_source": hbm_src,
+                "kernel": "one ssd_chunk_scan call of 8 x 8192 rows (its B|C conv and scan "
+                          "kernels; events around the calls, two equal calls per step)",
+                "algorithmic_bytes_per_launch": nb["per_call"],
+                "algorithmic_bytes_per_row": nb["per_row"],
+                "algorithmic_state_bytes_per_sequence": nb["per_seq_per_call"],
+                "ms_per_launch": round(ms / ncalls, 5)}
+    del run, inp
+    return {"ms": ms, "value": whole_job_tokens_per_s(world, shape, ms), "roofline": roofline,
+            "gpu_launches": sum(launches1[k] - launches0[k] for k in launches0),
+            "host_us_per_step": round(host_loop * 1e6, 1), "clocks": clk.summary()}
+
+
+def bench_prefill_2048(ssd, dev, stream, world, rank, args):
+    """The 2048-row single-sequence prefill, one ssd_chunk_scan call per step,
+    inputs rotating over resident sets whose total exceeds twice the L2."""
+    shape = si.PREFILL
+    pb = prefill_bytes(shape)
+    set_bytes = pb["per_launch"]
+    nsets = max(3, -(-2 * L2_BYTES // set_bytes))
+    prm, sets, d, flags = make_prefill_sets(shape, nsets, rank_seed(rank), dev)
+    host_s = []
+    for i in range(args.warmup):
+        inp, out, ws = sets[i % nsets]
+        t0 = time.perf_counter()
+        prefill_call(ssd, d, flags, prm, inp, out, ws, stream)
+        host_s.append(time.perf_counter() - t0)
+    torch.cuda.synchronize()
+    host_call = statistics.median(host_s[1:] or host_s)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    queue_ahead(host_call, args.steps)
+    ev0.record(stream)
+    for i in range(args.steps):
+        inp, out, ws = sets[i % nsets]
+        prefill_call(ssd, d, flags, prm, inp, out, ws, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = _max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+    hbm, hbm_src = measured_peaks()
+    achieved = pb["per_launch"] / (ms / 1e3) / 1e9
+    res = {"workload": "B=1 x S=2048 rows, one ssd_chunk_scan call per step",
+           "tokens_per_s": round(whole_job_tokens_per_s(world, shape, ms), 1),
+           "ms_per_call": round(ms, 5),
+           "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                        "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                        "traffic": ncu_traffic("prefill"), "peak_source": hbm_src,
+                        "algorithmic_bytes_per_launch": pb["per_launch"]},
+           "l2": f"inputs rotate over {nsets} resident sets "
+                 f"({nsets * set_bytes / 1e6:.0f} MB > 129 MB L2)"}
+    return res, (shape, d, flags, prm, sets[0])
+
+
 def bench_ours(args):
     import ssd_scan_gb300 as ssd
 
@@ -250,80 +368,42 @@ def bench_ours(args):
     if args.only == "decode":
         dec = bench_decode(ssd, dev, stream, world, args)
         return {"metric": "decode-step state GB/s", "decode": dec} if rank == 0 else None
-    shape = si.PREFILL
-    pb = prefill_bytes(shape)
-    set_bytes = pb["per_launch"]
-    nsets = max(3, -(-2 * L2_BYTES // set_bytes))  # rotate over > 2x L2 of inputs+outputs
-    prm, sets, d, flags = make_prefill_sets(shape, nsets, rank_seed(rank), dev)
-
-    # ---- warm-up (also the host's cost of one call), then K timed steps (one
-    # ssd_chunk_scan call each), queued behind a spin so that none waits on the host
-    host_s = []
-    for i in range(args.warmup):
-        inp, out, ws = sets[i % nsets]
-        t0 = time.perf_counter()
-        prefill_call(ssd, d, flags, prm, inp, out, ws, stream)
-        host_s.append(time.perf_counter() - t0)
-    torch.cuda.synchronize()
-    host_call = statistics.median(host_s[1:] or host_s)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches0 = ssd.ssd_launch_counts()
-    with ClockSampler(local) as clk:
-        _barrier(world)
-        torch.cuda.synchronize()
-        queue_ahead(host_call, args.steps)
-        ev0.record(stream)
-        t0 = time.perf_counter()
-        for i in range(args.steps):
-            inp, out, ws = sets[i % nsets]
-            prefill_call(ssd, d, flags, prm, inp, out, ws, stream)
-        host_loop = (time.perf_counter() - t0) / args.steps
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        _barrier(world)
-    launches1 = ssd.ssd_launch_counts()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    ms = _max_over_ranks(ms, world)
-    gpu_launches = sum(launches1[k] - launches0[k] for k in launches0)
-    value = whole_job_tokens_per_s(world, shape, ms)
-
-    hbm, hbm_src = measured_peaks()
-    achieved = pb["per_launch"] / (ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": ncu_traffic("prefill"),
-                "peak_source": hbm_src,
-                "kernel": "ssd_chunk_scan call (all its kernels, events around the call)",
-                "algorithmic_bytes_per_launch": pb["per_launch"]}
-    extra = None
-    if args.only == "prefill":  # profiling runs: the timed prefill steps alone
-        e2e = dec = None
-    else:
+    if args.only == "prefill":  # profiling runs: the 2048-row calls alone
+        p2048, _ = bench_prefill_2048(ssd, dev, stream, world, rank, args)
+        return {"metric": "prefill_2048", "prefill_2048": p2048} if rank == 0 else None
+    head = bench_long(ssd, dev, stream, world, rank, args)
+    extra = e2e = dec = p2048 = None
+    if args.only == "all":
+        p2048, _ = bench_prefill_2048(ssd, dev, stream, world, rank, args)
         if args.extra:
             extra = bench_extra(ssd, dev, stream, args)
         # ---- end to end through the C-ABI from pinned host buffers
-        e2e = bench_e2e(ssd, shape, d, flags, prm, sets[0], stream, args)
+        e2e = bench_e2e_long(ssd, dev, stream, rank, args)
         # ---- decode step (256 rows, 1024-slot pool, 64 steps)
         dec = bench_decode(ssd, dev, stream, world, args)
 
     out = None
     if rank == 0:
+        shape = LONG_STEP
         out = {
-            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "nemotron-h-8b mixer prefill: B=1 x S=2048 rows per GPU, "
-                                   "chunk 128, H=128 P=64 N=128 G=8 W=4, conv+SiLU and z-gate "
-                                   "fused, carried conv/ssm state",
-                       "batch_per_gpu": shape.batch, "seq_len": shape.seqlen,
+            "metric": METRIC, "value": round(head["value"], 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(head["ms"], 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "nemotron-h-8b mixer long prefill: 8 sequences x 8192 rows "
+                                   "per GPU in one call, then a second 8192-row call of each fed "
+                                   "with the final conv/ssm states; chunk 128, H=128 P=64 N=128 "
+                                   "G=8 W=4, conv+SiLU and z-gate fused",
+                       "batch_per_gpu": si.LONG.batch, "seq_len": shape.seqlen,
+                       "calls_per_step": len(LONG_SPLITS),
                        "parallelism": f"replicas x{world} (independent sequences)",
-                       "l2": f"inputs rotate over {nsets} resident sets "
-                             f"({nsets * set_bytes / 1e6:.0f} MB > 129 MB L2)"},
-            "roofline": roofline,
+                       "l2": "inputs of one step 7.2 GB > 129 MB L2"},
+            "roofline": head["roofline"],
             "e2e": e2e,
-            "gpu_launches": gpu_launches,
-            "host_us_per_call": round(host_loop * 1e6, 1),
-            "clocks": clk.summary(),
+            "gpu_launches": head["gpu_launches"],
+            "host_us_per_step": head["host_us_per_step"],
+            "clocks": head["clocks"],
+            "prefill_2048": p2048,
             "decode": dec,
         }
         if extra is not None:
@@ -331,25 +411,83 @@ def bench_ours(args):
     return out
 
 
-def bench_e2e(ssd, shape, d, flags, prm, dset, stream, args):
+def bench_e2e_long(ssd, dev, stream, rank, args):
     """End to end through the C-ABI from pinned host buffers: every step copies
-    its inputs host -> device, makes the ssd_chunk_scan call and copies its
-    outputs device -> host, all inside the timed region.  The steps are
-    pipelined the way a serving loop runs them: inputs go in on one copy
-    stream, outputs come back on another, and the call runs on the compute
-    stream, so step i+1's input copy and step i-1's output copy overlap step
-    i's call (device inputs and outputs double-buffered, ordered by events).
-    The same steps run one after the other are reported as `serial`."""
-    inp, out, ws = dset
-    host_in = {k: v.cpu().pin_memory() for k, v in inp.items() if v is not None}
-    host_out = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
-                for _ in range(2)]
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
-    dev_in = [{k: torch.empty_like(v, device="cuda") for k, v in host_in.items()} for _ in range(2)]
-    dev_out = [out, {k: torch.empty_like(v) for k, v in out.items()}]
+    its inputs (the rows of both calls and the initial states) host -> device,
+    makes the two chained ssd_chunk_scan calls and copies y and the final
+    states device -> host, all inside the timed region.  Steps are pipelined
+    as a serving loop runs them: inputs go in on one copy stream, outputs come
+    back on another, the calls run on the compute stream, device tensors are
+    double-buffered and ordered by events, so one step's copies overlap the
+    neighbouring steps' calls.  The same steps run one after the other are
+    reported as `serial`."""
+    shape = LONG_STEP
+    B, H, P, N, G, W = (shape.batch, shape.nheads, shape.headdim, shape.dstate, shape.ngroups,
+                        shape.conv_width)
+    L = si.LONG.seqlen
+    prm = {k: v.to(dev) for k, v in si.params(shape, seed=rank_seed(rank)).items()}
+    src = si.prefill_inputs(shape, seed=rank_seed(rank) + 1, device=dev)
+    rows = ("xbc", "dt_raw", "z")
+    # host inputs per call (each call's rows contiguous, so every copy is one
+    # contiguous pinned transfer) and the initial states
+    host_in = {"calls": [{k: src[k][:, c * L:(c + 1) * L].contiguous().cpu().pin_memory()
+                          for k in rows} for c in range(2)],
+               "ssm_state": src["ssm_state"].cpu().pin_memory(),
+               "conv_state": src["conv_state"].cpu().pin_memory()}
+    del src
+    flags = ssd.SSD_DT_SOFTPLUS | ssd.SSD_HAS_Z
+    d = ssd.dims(B, L, H, P, N, G, W, shape.chunk)
+    ws = ssd.workspace_for(d, ssd.SSD_BF16, flags, True, dev)
+
+    def dev_set():
+        ins = {"calls": [{k: torch.empty_like(v, device=dev) for k, v in hc.items()}
+                         for hc in host_in["calls"]],
+               "ssm_state": torch.empty_like(host_in["ssm_state"], device=dev),
+               "conv_state": torch.empty_like(host_in["conv_state"], device=dev)}
+        outs = {"y": [torch.empty((B, L, H, P), dtype=torch.bfloat16, device=dev)
+                      for _ in range(2)],
+                "hS": [torch.empty((B, H, P, N), dtype=torch.float32, device=dev)
+                       for _ in range(2)],
+                "cs": [torch.empty((B, W - 1, shape.cdim), dtype=torch.bfloat16, device=dev)
+                       for _ in range(2)]}
+        return ins, outs
+
+    sets = [dev_set(), dev_set()]
+    host_out = [{"y": [torch.empty((B, L, H, P), dtype=torch.bfloat16, pin_memory=True)
+                       for _ in range(2)],
+                 "hS": torch.empty((B, H, P, N), dtype=torch.float32, pin_memory=True),
+                 "cs": torch.empty((B, W - 1, shape.cdim), dtype=torch.bfloat16,
+                                   pin_memory=True)} for _ in range(2)]
+    nbytes = lambda t: t.numel() * t.element_size()  # noqa: E731
+    h2d = sum(nbytes(v) for hc in host_in["calls"] for v in hc.values()) + \
+        nbytes(host_in["ssm_state"]) + nbytes(host_in["conv_state"])
+    d2h = sum(nbytes(v) for v in host_out[0]["y"]) + nbytes(host_out[0]["hS"]) + \
+        nbytes(host_out[0]["cs"])
+
+    def copy_in(ins):
+        ins["ssm_state"].copy_(host_in["ssm_state"], non_blocking=True)
+        ins["conv_state"].copy_(host_in["conv_state"], non_blocking=True)
+        for c in range(2):
+            for k in rows:
+                ins["calls"][c][k].copy_(host_in["calls"][c][k], non_blocking=True)
+
+    def calls(ins, outs, st):
+        for c in range(2):
+            ci = ins["calls"][c]
+            ssd.ssd_chunk_scan(d, ssd.SSD_BF16, flags, ci["xbc"], prm["conv_w"], prm["conv_b"],
+                               ins["conv_state"] if c == 0 else outs["cs"][0], outs["cs"][c],
+                               ci["dt_raw"], prm["dt_bias"], prm["A"], prm["D"], ci["z"],
+                               ins["ssm_state"] if c == 0 else outs["hS"][0], outs["y"][c],
+                               outs["hS"][c], ws, st)
+
+    def copy_out(outs, ho):
+        for c in range(2):
+            ho["y"][c].copy_(outs["y"][c], non_blocking=True)
+        ho["hS"].copy_(outs["hS"][1], non_blocking=True)
+        ho["cs"].copy_(outs["cs"][1], non_blocking=True)
+
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev = lambda: torch.cuda.Event()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
     in_ready, in_free = [ev(), ev()], [ev(), ev()]
     done, out_free = [ev(), ev()], [ev(), ev()]
     for e in in_free + out_free:
@@ -357,33 +495,31 @@ def bench_e2e(ssd, shape, d, flags, prm, dset, stream, args):
 
     def step(i):
         b = i % 2
+        ins, outs = sets[b]
         with torch.cuda.stream(s_in):
-            s_in.wait_event(in_free[b])  # the call of step i-2 is done with dev_in[b]
-            for k, v in host_in.items():
-                dev_in[b][k].copy_(v, non_blocking=True)
+            s_in.wait_event(in_free[b])
+            copy_in(ins)
             in_ready[b].record(s_in)
         stream.wait_event(in_ready[b])
-        stream.wait_event(out_free[b])  # step i-2's outputs have left dev_out[b]
-        prefill_call(ssd, d, flags, prm, dev_in[b], dev_out[b], ws, stream)
+        stream.wait_event(out_free[b])
+        calls(ins, outs, stream)
         in_free[b].record(stream)
         done[b].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(done[b])
-            for k, v in dev_out[b].items():
-                host_out[b][k].copy_(v, non_blocking=True)
+            copy_out(outs, host_out[b])
             out_free[b].record(s_out)
 
     def serial_step():
-        for k, v in host_in.items():
-            dev_in[0][k].copy_(v, non_blocking=True)
-        prefill_call(ssd, d, flags, prm, dev_in[0], dev_out[0], ws, stream)
-        for k, v in dev_out[0].items():
-            host_out[0][k].copy_(v, non_blocking=True)
+        ins, outs = sets[0]
+        copy_in(ins)
+        calls(ins, outs, stream)
+        copy_out(outs, host_out[0])
 
-    n = max(3, min(args.steps, 20))
-    timing = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    # serial: one stream, each step's copies and call in turn
-    for _ in range(max(3, args.warmup)):
+    n = max(3, min(args.steps, 10))
+    timing = lambda: (torch.cuda.Event(enable_timing=True),  # noqa: E731
+                      torch.cuda.Event(enable_timing=True))
+    for _ in range(3):
         serial_step()
     torch.cuda.synchronize()
     e0, e1 = timing()
@@ -393,9 +529,7 @@ def bench_e2e(ssd, shape, d, flags, prm, dset, stream, args):
     e1.record(stream)
     torch.cuda.synchronize()
     serial_ms = e0.elapsed_time(e1) / n
-    # pipelined: every stream waits on the start event; the end event follows the
-    # last output copy, which follows every call and (by stream order) every copy
-    for i in range(max(3, args.warmup)):
+    for i in range(3):
         step(i)
     torch.cuda.synchronize()
     e0, e1 = timing()
@@ -409,12 +543,15 @@ def bench_e2e(ssd, shape, d, flags, prm, dset, stream, args):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / n
+    assert ssd.ssd_read_device_error(stream) == ssd.SSD_OK
     tok = shape.batch * shape.seqlen
+    del sets, host_out, host_in
     return {"value": round(tok / (ms / 1e3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
-            "pipelined": "input copy, call and output copy of consecutive steps overlap "
+            "pipelined": "input copy, calls and output copy of consecutive steps overlap "
                          "(two copy streams, double-buffered device tensors)",
-            "serial": {"value": round(tok / (serial_ms / 1e3), 1), "ms_per_step": round(serial_ms, 4)}}
+            "serial": {"value": round(tok / (serial_ms / 1e3), 1),
+                       "ms_per_step": round(serial_ms, 4)}}
 
 
 def chained_calls(ssd, shape, prm, inp, splits, device):
@@ -614,15 +751,18 @@ def bench_decode(ssd, dev, stream, world, args):
 # the fp64 oracle on the host cores
 
 def oracle_sample_rows() -> int:
-    return int(os.environ.get("SSD_BENCH_ORACLE_ROWS", str(si.PREFILL.seqlen)))
+    return int(os.environ.get("SSD_BENCH_ORACLE_ROWS", str(si.LONG.seqlen)))
 
 
 def oracle_prefill_sample(rows: int):
-    """Time the oracle on the first ``rows`` rows of the prefill workload (all
-    heads: conv + SiLU + recurrence + gate).  Returns (seconds, threads)."""
+    """Time the oracle on one sequence of the long workload's first call (its
+    first ``rows`` rows, all 128 heads: conv + SiLU + recurrence + gate).  The
+    oracle's cost per row does not depend on the sequence or on the row's
+    position, so its rate on this sample is its rate on the whole workload.
+    Returns (seconds, threads)."""
     import oracle
     import numpy as np
-    shape = si.PREFILL.with_(seqlen=rows)
+    shape = si.LONG.with_(batch=1, seqlen=rows)
     prm = si.params(shape, seed=0)
     inp = si.prefill_inputs(shape, seed=1)
     f = lambda t: None if t is None else t.to(torch.float64).numpy()  # noqa: E731
@@ -639,7 +779,7 @@ def oracle_prefill_sample(rows: int):
 
 
 def cpu_baseline(min_seconds: float = 10.0) -> dict:
-    """The oracle on the prefill workload, repeated until at least
+    """The oracle on a sample of the long workload, repeated until at least
     `min_seconds` of wall time (at least once)."""
     rows = oracle_sample_rows()
     total, passes, threads = 0.0, 0, 1
@@ -647,10 +787,13 @@ def cpu_baseline(min_seconds: float = 10.0) -> dict:
         dt, threads = oracle_prefill_sample(rows)
         total += dt
         passes += 1
-    return {"value": round(rows * passes / total, 2), "unit": "tokens/s", "cores": threads,
-            "kind": "oracle",
-            "sample": f"{passes} passes over the first {rows} of the 2048 rows of the prefill "
-                      f"workload, all 128 heads (conv + recurrence + gate, fp64), {total:.1f} s"}
+    rate = rows * passes / total
+    step_rows = LONG_STEP.batch * LONG_STEP.seqlen
+    return {"value": round(rate, 2), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{passes} passes over one {rows}-row sequence of the long workload's "
+                      f"first call, all 128 heads (conv + recurrence + gate, fp64), "
+                      f"{total:.1f} s; a whole step ({step_rows} rows) extrapolates to "
+                      f"{step_rows / rate:.0f} s"}
 
 
 def bench_reference(args):
@@ -672,11 +815,13 @@ def bench_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "nemotron-h-8b mixer prefill (as the main arm); each step is a "
-                               f"bounded sample: the first {rows} rows, all 128 heads",
+        "config": {"workload": "nemotron-h-8b mixer long prefill (as the main arm); each step "
+                               f"is a bounded sample: one {rows}-row sequence of the first call, "
+                               "all 128 heads",
                    "batch_per_gpu": 1, "seq_len": rows, "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": threads,
-                         "kind": "oracle", "sample": f"first {rows} rows x 128 heads per step"},
+                         "kind": "oracle",
+                         "sample": f"one {rows}-row sequence x 128 heads per step"},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -691,8 +836,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra", action="store_true",
                     help="also time the long (8 x 8192 + 8192) and decay-stress prefill workloads")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
-                    help="time only the prefill or only the decode steps (profiler runs)")
+    ap.add_argument("--only", choices=["all", "long", "prefill", "decode"], default="all",
+                    help="time only the long-prefill steps, the 2048-row prefill calls or "
+                         "the decode steps (profiler runs)")
     ap.add_argument("--decode-slots", type=int, default=si.DECODE_SLOTS,
                     help="slots in the decode pool (the 256 rows touch the same bytes "
                          "whatever the pool size; a smaller pool keeps profiler captures small)")

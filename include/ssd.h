@@ -73,7 +73,10 @@ typedef enum {
     SSD_ERR_UNSUPPORTED = 2,  /* valid problem that no kernel here implements  */
     SSD_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, query)     */
     SSD_ERR_BAD_SLOT = 4,     /* device error word: a slot id out of range      */
-    SSD_ERR_TIMEOUT = 5       /* device error word: a bounded wait ran out      */
+    SSD_ERR_TIMEOUT = 5,      /* device error word: a bounded wait ran out      */
+    SSD_ERR_DUPLICATE_SLOT = 6 /* device error word: a slot id given twice in one
+                                  call (reported only with
+                                  SSD_CHECK_DISTINCT_SLOTS on)                */
 } ssd_status;
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype; /* activation dtype */
@@ -191,7 +194,11 @@ SSD_API ssd_status ssd_chunk_scan_workspace_size(const ssd_dims* dims, ssd_dtype
  *     SSD_STATIC_SCRATCH_BYTES return SSD_ERR_UNSUPPORTED before anything is
  *     launched (for the bf16 tensor-core path with the conv fused that size
  *     is batch * seqlen * 2 * ngroups * dstate * 2 bytes, so with dstate 128
- *     batch * seqlen * ngroups may be at most 32768).
+ *     batch * seqlen * ngroups may be at most 32768).  This size check runs
+ *     first, before the pointer checks of ssd_chunk_scan: a problem that is
+ *     too large gets SSD_ERR_UNSUPPORTED even if a pointer is also bad.
+ *   - The array used is the one of the CURRENT device (cudaGetDevice), which
+ *     must be the device `stream` belongs to.
  *   - Nothing in the array has to start at zero: every call writes the
  *     scratch rows it reads before reading them.  The array keeps the last
  *     call's contents, which mean nothing to the next call.
@@ -230,7 +237,8 @@ SSD_API ssd_status ssd_chunk_scan_static_ws(const ssd_dims* dims, ssd_dtype act,
  * The decode rows of a mixed batch go to ssd_decode_step on the same pools.
  *
  * cu_seqlens, slot_ids       [nseq+1], [nseq] int32, DEVICE memory; slot ids
- *                            distinct (not checked: duplicates race)
+ *                            distinct (checked only with
+ *                            SSD_CHECK_DISTINCT_SLOTS on; else duplicates race)
  * has_initial_state          [nseq] int32 DEVICE memory, or NULL (all 1)
  * xbc [T,Cdim], dt [T,H], z [T,H*P], y [T,H,P]: packed rows, as the
  *   [B,S,..] arrays of ssd_chunk_scan with B = 1, S = T
@@ -269,10 +277,11 @@ SSD_API ssd_status ssd_chunk_scan_varlen(const ssd_dims* dims, ssd_dtype act, un
  * xbc        [R,Cdim] act (raw when conv_w != NULL)
  * conv_pool  [num_slots,W-1,Cdim] act; required iff conv_w != NULL
  * dt         [R,H] fp32;  dt_bias, A, D, z as in ssd_chunk_scan ([R,H*P] for z)
- * slot_ids   [R] int32, DEVICE memory.  Ids must be distinct (not checked:
- *            duplicate ids race).  An id outside [0, num_slots) sets the
- *            device error word to SSD_ERR_BAD_SLOT and that row writes
- *            nothing (neither pool nor y); other rows are unaffected.
+ * slot_ids   [R] int32, DEVICE memory.  Ids must be distinct (checked only
+ *            with SSD_CHECK_DISTINCT_SLOTS on; else duplicate ids race).
+ *            An id outside [0, num_slots) sets the device error word to
+ *            SSD_ERR_BAD_SLOT and that row writes nothing (neither pool nor
+ *            y); other rows are unaffected.
  * ssm_pool   [num_slots,H,P,N] fp32, updated in place
  * y          [R,H,P] act
  */
@@ -327,14 +336,40 @@ enum {
 };
 SSD_API int ssd_launch_counts(uint64_t* out, int n);
 
+/*
+ * Debug checks (process-wide, off by default; they cost time on every call).
+ * SSD_CHECK_DISTINCT_SLOTS: ssd_decode_step and ssd_chunk_scan_varlen check
+ * on the device that no slot id appears twice in one call (the slot-id rule
+ * of both entry points).  A row (decode) or sequence (varlen) whose slot id
+ * already appeared at an earlier index sets SSD_ERR_DUPLICATE_SLOT in the
+ * device error word and writes nothing (neither pool nor y); the earlier
+ * occurrence runs normally, so the pools stay consistent.  Without the check
+ * duplicate ids race.  Returns the flags that were set before.
+ */
+enum { SSD_CHECK_DISTINCT_SLOTS = 1u };
+SSD_API unsigned ssd_set_debug_checks(unsigned flags);
+
+/*
+ * Bound, in nanoseconds, on each wait between the warps of the tensor-core
+ * scan kernel (ssd_chunk_scan / ssd_chunk_scan_varlen / _static_ws on the
+ * tensor-core path).  A wait that runs out ends the kernel early: the
+ * outputs of that call are undefined and the device error word reports
+ * SSD_ERR_TIMEOUT; the context stays usable (no trap).  Default 2 s, which
+ * no healthy call comes near; 0 restores the default.  The kernel's final
+ * waits for its own copies and tensor-core work in flight keep the 2 s bound
+ * whatever this is.  Meant for failure-detection tests and watchdogs; it is
+ * process-wide and read at each launch.  Returns the previous bound.
+ */
+SSD_API uint64_t ssd_set_wait_limit_ns(uint64_t ns);
+
 /* Static text for a status code (never NULL). */
 SSD_API const char* ssd_status_string(ssd_status status);
 
 /*
  * Synchronises `stream`, then returns and clears the device error word of the
- * current device: SSD_OK, SSD_ERR_BAD_SLOT or SSD_ERR_TIMEOUT (the first
- * error kind recorded since the last read), or SSD_ERR_CUDA if a CUDA call
- * failed.
+ * current device: SSD_OK, or SSD_ERR_BAD_SLOT, SSD_ERR_DUPLICATE_SLOT,
+ * SSD_ERR_TIMEOUT (the first of these, in this order, among the kinds
+ * recorded since the last read), or SSD_ERR_CUDA if a CUDA call failed.
  */
 SSD_API ssd_status ssd_read_device_error(cudaStream_t stream);
 

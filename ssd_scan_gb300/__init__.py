@@ -24,6 +24,9 @@ SSD_ERR_UNSUPPORTED = 2
 SSD_ERR_CUDA = 3
 SSD_ERR_BAD_SLOT = 4
 SSD_ERR_TIMEOUT = 5
+SSD_ERR_DUPLICATE_SLOT = 6
+
+SSD_CHECK_DISTINCT_SLOTS = 1
 
 SSD_F32 = 0
 SSD_BF16 = 1
@@ -38,7 +41,7 @@ SSD_STATIC_SCRATCH_BYTES = 16 << 20
 EXPORTED = ("ssd_conv1d_rows", "ssd_chunk_scan", "ssd_chunk_scan_workspace_size",
             "ssd_decode_step", "ssd_status_string", "ssd_read_device_error",
             "ssd_launch_counts", "ssd_chunk_scan_static_ws", "ssd_gated_group_rmsnorm",
-            "ssd_chunk_scan_varlen")
+            "ssd_chunk_scan_varlen", "ssd_set_debug_checks", "ssd_set_wait_limit_ns")
 
 KERNEL_KINDS = ("conv_rows", "conv_state", "scan_simt", "scan_tc", "bc_conv", "decode_step",
                 "decode_conv", "gated_norm")
@@ -93,11 +96,26 @@ def load_library():
             lib.ssd_status_string.restype = ctypes.c_char_p
             lib.ssd_read_device_error.argtypes = [_vp]
             lib.ssd_launch_counts.argtypes = [ctypes.POINTER(ctypes.c_uint64), ci]
+            lib.ssd_set_debug_checks.argtypes = [cu]
+            lib.ssd_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             for n in EXPORTED:
                 if n != "ssd_status_string":
                     getattr(lib, n).restype = ci
+            lib.ssd_set_debug_checks.restype = cu
+            lib.ssd_set_wait_limit_ns.restype = ctypes.c_uint64
             _lib = lib
     return _lib
+
+
+def ssd_set_debug_checks(flags: int) -> int:
+    """Process-wide debug checks (SSD_CHECK_DISTINCT_SLOTS); returns the old flags."""
+    return int(load_library().ssd_set_debug_checks(int(flags)))
+
+
+def ssd_set_wait_limit_ns(ns: int) -> int:
+    """Bound on each wait inside the tensor-core scan kernel (0: the default
+    2 s); returns the old bound."""
+    return int(load_library().ssd_set_wait_limit_ns(int(ns)))
 
 
 def ssd_status_string(status: int) -> str:

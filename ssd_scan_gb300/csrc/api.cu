@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 
 namespace {
 
@@ -18,11 +19,18 @@ __device__ unsigned g_ssd_error_word;
 
 constexpr int kMaxDevices = 64;
 unsigned* g_err_addr[kMaxDevices];  // host cache of each device's symbol address
+std::mutex g_err_mutex;             // first calls on a device from several threads
+
+// process-wide settings read at every launch (ssd_set_debug_checks,
+// ssd_set_wait_limit_ns)
+std::atomic<unsigned> g_debug_checks{0};
+std::atomic<uint64_t> g_wait_ns{0};  // 0: the kernel's default
 
 ssd_status error_word_address(unsigned** out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_err_mutex);
     if (g_err_addr[dev] == nullptr) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_ssd_error_word) != cudaSuccess) return SSD_ERR_CUDA;
@@ -97,6 +105,13 @@ ssd_status counted(cudaError_t e, int kind, bool launched = true)
 
 extern "C" {
 
+unsigned ssd_set_debug_checks(unsigned flags)
+{
+    return g_debug_checks.exchange(flags & SSD_CHECK_DISTINCT_SLOTS);
+}
+
+uint64_t ssd_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns); }
+
 int ssd_launch_counts(uint64_t* out, int n)
 {
     for (int i = 0; out != nullptr && i < n && i < SSD_KERNEL_KINDS; ++i)
@@ -113,6 +128,7 @@ const char* ssd_status_string(ssd_status s)
         case SSD_ERR_CUDA: return "CUDA runtime error";
         case SSD_ERR_BAD_SLOT: return "slot id out of range (device)";
         case SSD_ERR_TIMEOUT: return "bounded device wait ran out (device)";
+        case SSD_ERR_DUPLICATE_SLOT: return "slot id given twice in one call (device)";
     }
     return "unknown status";
 }
@@ -128,6 +144,7 @@ ssd_status ssd_read_device_error(cudaStream_t stream)
     if (cudaMemcpy(addr, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
         return SSD_ERR_CUDA;
     if (v & kErrBadSlot) return SSD_ERR_BAD_SLOT;
+    if (v & kErrDupSlot) return SSD_ERR_DUPLICATE_SLOT;
     if (v & kErrTimeout) return SSD_ERR_TIMEOUT;
     return SSD_OK;
 }
@@ -222,6 +239,7 @@ ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned flags, c
                         conv_w != nullptr, xbc, xbc, (int)cdim, H * P, conv_w, conv_b,
                         conv_state_in, conv_w != nullptr ? conv_state_out : nullptr, dt, dt_bias,
                         A, D, has_z ? z : nullptr, ssm_state_in, y, ssm_state_out, err};
+        tp.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
         if (conv_w != nullptr) {
             // B|C columns: conv + SiLU once per group into the workspace
             ConvParams bp{dims->batch, dims->seqlen, (int)cdim, dims->conv_width, xbc, conv_w,
@@ -284,6 +302,7 @@ ssd_status ssd_decode_step(const ssd_dims* dims, ssd_dtype act, unsigned flags, 
     DecodeParams p{dims->batch, dims->nheads, dims->headdim, dims->dstate, dims->ngroups,
                    dims->conv_width, flags, xbc, conv_w, conv_b, conv_pool, dt, dt_bias, A, D,
                    has_z ? z : nullptr, slot_ids, num_slots, ssm_pool, y, err};
+    p.check_dups = (g_debug_checks.load(std::memory_order_relaxed) & SSD_CHECK_DISTINCT_SLOTS) != 0;
     s = counted(launch_decode_step(p, bf16, stream), SSD_KERNEL_DECODE_STEP);
     if (s != SSD_OK) return s;
     return counted(launch_decode_conv_roll(p, bf16, stream), SSD_KERNEL_DECODE_CONV,
@@ -338,6 +357,8 @@ ssd_status ssd_chunk_scan_varlen(const ssd_dims* dims, ssd_dtype act, unsigned f
     tp.slot_ids = slot_ids;
     tp.has_init = has_initial_state;
     tp.num_slots = num_slots;
+    tp.check_dups = (g_debug_checks.load(std::memory_order_relaxed) & SSD_CHECK_DISTINCT_SLOTS) != 0;
+    tp.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     if (conv_w != nullptr) {
         ConvParams bp{1, (int)T, (int)cdim, dims->conv_width, xbc, conv_w, conv_b, conv_pool,
                       workspace, nullptr, H * P, 2 * G * N, 2 * G * N};

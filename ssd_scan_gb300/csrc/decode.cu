@@ -37,6 +37,10 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
         if (threadIdx.x == 0 && g == 0) atomicOr(p.err, kErrBadSlot);
         return;
     }
+    if (p.check_dups && slot_seen_before(p.slots, i, s)) {  // the earlier row owns the slot
+        if (threadIdx.x == 0 && g == 0) atomicOr(p.err, kErrDupSlot);
+        return;
+    }
     const T* xbc = static_cast<const T*>(p.xbc);
     const T* cpool = static_cast<const T*>(p.conv_pool);
     const int HW = p.W - 1;
@@ -140,6 +144,7 @@ __global__ void decode_conv_roll_kernel(DecodeParams p)
     if (c >= Cdim) return;
     const int s = p.slots[i];
     if (s < 0 || s >= p.num_slots) return;
+    if (p.check_dups && slot_seen_before(p.slots, i, s)) return;
     const int HW = p.W - 1;
     T* cp = static_cast<T*>(p.conv_pool) + (size_t)s * HW * Cdim;
     for (int k = 0; k + 1 < HW; ++k) cp[(size_t)k * Cdim + c] = cp[(size_t)(k + 1) * Cdim + c];

@@ -9,7 +9,7 @@
 namespace ssd {
 
 // Bits of the per-device error word (first error kind wins in the report).
-enum : unsigned { kErrBadSlot = 1u, kErrTimeout = 2u };
+enum : unsigned { kErrBadSlot = 1u, kErrTimeout = 2u, kErrDupSlot = 4u };
 
 enum : unsigned { kDtSoftplus = 1u, kHasZ = 2u };
 
@@ -69,7 +69,16 @@ struct DecodeParams {
     float* pool;            // [num_slots,H,P,N]
     void* y;                // [R,H,P] act
     unsigned* err;
+    int check_dups = 0;     // a row whose slot id appeared at an earlier row: report, skip
 };
+
+// Has slot id `s` already appeared among ids[0 .. i-1]?  (debug check)
+__device__ __forceinline__ bool slot_seen_before(const int32_t* ids, int i, int s)
+{
+    for (int k = 0; k < i; ++k)
+        if (ids[k] == s) return true;
+    return false;
+}
 
 // ---- element conversions --------------------------------------------------
 __device__ __forceinline__ float to_f32(float v) { return v; }
@@ -125,6 +134,8 @@ struct TcScanParams {
     const int* slot_ids = nullptr;
     const int* has_init = nullptr;  // or null: every sequence continues its slot
     int num_slots = 0;
+    int check_dups = 0;             // packed sequences: report and skip a repeated slot id
+    unsigned long long wait_ns = 0; // bound on each wait between the kernel's warps
 };
 bool scan_tc_supports(int P, int N);
 // after_prepass: the kernel just before it on `st` is the B|C conv writing p.bc;

@@ -88,7 +88,7 @@ constexpr int kThreads = kCompute + 64;
 constexpr int kCv = 4;                     // per-chunk value sets in flight
 constexpr int kMaxW = 4;  // conv taps handled in the kernel (W-1 carried rows)
 constexpr int kRaw = 4 + kMaxW - 1;          // raw rows a conv thread reads per chunk
-constexpr uint64_t kWaitNs = 2000000000ull;  // bound on any single wait: 2 s
+constexpr uint64_t kWaitNs = 2000000000ull;  // default bound on a wait (the final drain's always)
 
 // G1: A, B K-major.  G2, G3: A K-major, B MN-major (row tiles [k][p]).
 // G4: A = B^T read MN-major from the B tile, B MN-major.
@@ -248,14 +248,15 @@ __device__ __forceinline__ void set_abort(TcSmem& s)
 // Bounded wait that also gives up as soon as another thread has aborted.
 // The hinted try_wait suspends the thread until the phase completes (or
 // about a microsecond passes), so a waiting warp takes no issue slots.
-__device__ __forceinline__ bool wait_or_abort(TcSmem& s, uint64_t* bar, uint32_t parity)
+__device__ __forceinline__ bool wait_or_abort(TcSmem& s, uint64_t* bar, uint32_t parity,
+                                              uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait_hint(bar, parity, 1000)) return true;
         if (aborted(s)) return false;
-        if (globaltimer_ns() - t0 > kWaitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             set_abort(s);
             return false;
         }
@@ -291,6 +292,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (threadIdx.x == 0) atomicOr(p.err, kErrBadSlot);
             return;
         }
+        // debug check: an earlier sequence of this call owns the slot
+        if (p.check_dups && slot_seen_before(p.slot_ids, b, slot)) {
+            if (threadIdx.x == 0 && h == 0) atomicOr(p.err, kErrDupSlot);
+            return;
+        }
         S = (int)(end - row0);
     }
     const float* h0 = init ? p.h0 : nullptr;
@@ -302,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int Cdim = H * P + 2 * G * N;
     const int nchunks = (S + Q - 1) / Q;
     const bool has_z = (p.flags & kHasZ) != 0;
+    const uint64_t wlim = p.wait_ns ? p.wait_ns : kWaitNs;  // pipeline waits
 
     if (tid == 0) {
         mbar_init(&s.full_c, 1);
@@ -395,9 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // G3(c): h of chunk c-1 in the state tile; Y / Yo [c&1] read by the
             // epilogue of chunk c-2; the values of chunk c say which accumulator
             auto g3 = [&](int c) -> bool {
-                bool r = wait_or_abort(s, &s.hsready, c & 1) &&
-                         wait_or_abort(s, &s.cvready[c % kCv], (c / kCv) & 1);
-                if (r && c >= 2) r = wait_or_abort(s, &s.epidone[(c - 2) % kCv], ((c - 2) / kCv) & 1);
+                bool r = wait_or_abort(s, &s.hsready, c & 1, wlim) &&
+                         wait_or_abort(s, &s.cvready[c % kCv], (c / kCv) & 1, wlim);
+                if (r && c >= 2) r = wait_or_abort(s, &s.epidone[(c - 2) % kCv], ((c - 2) / kCv) & 1, wlim);
                 if (!r) return false;
                 tc_fence_after();
                 const uint32_t dY = (s.cv[c % kCv].factored ? kColY : kColYo) + 64 * (c & 1);
@@ -421,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             load_c(0);
             load_b(0);
             if (nchunks > 1) load_b(1);
-            bool ok = wait_or_abort(s, &s.full_c, 0) && wait_or_abort(s, &s.full_b[0], 0);
+            bool ok = wait_or_abort(s, &s.full_c, 0, wlim) && wait_or_abort(s, &s.full_b[0], 0, wlim);
             if (ok) {
                 tc_fence_after();
                 g1(0);
@@ -430,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < nchunks && ok; ++c) {
                 const int kb = c & 1;
                 // G4(c): x rows of chunk c in place; dH read by state(c-1)
-                ok = wait_or_abort(s, &s.xready, c & 1) && wait_or_abort(s, &s.hsready, c & 1);
+                ok = wait_or_abort(s, &s.xready, c & 1, wlim) && wait_or_abort(s, &s.hsready, c & 1, wlim);
                 if (!ok) break;
                 tc_fence_after();
                 {
@@ -443,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // tiles: C of chunk c+1 (G1(c), G3(c) done), B of chunk c+2 into B[kb]
                 // (G1(c), G4(c) done)
                 if (c + 1 < nchunks) {
-                    ok = wait_or_abort(s, &s.g4, c & 1);
+                    ok = wait_or_abort(s, &s.g4, c & 1, wlim);
                     if (!ok) break;
                     load_c(c + 1);
                     if (c + 2 < nchunks) load_b(c + 2);
@@ -451,12 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // z of chunk c once the epilogue of chunk c-1 is done (it comes before
                 // the mask of chunk c, so this does not hold up G2(c))
                 if (has_z && c > 0) {
-                    ok = wait_or_abort(s, &s.epidone[(c - 1) % kCv], ((c - 1) / kCv) & 1);
+                    ok = wait_or_abort(s, &s.epidone[(c - 1) % kCv], ((c - 1) / kCv) & 1, wlim);
                     if (!ok) break;
                     load_z(c);
                 }
                 // G2(c): M(c) in TMEM (CB(c) consumed); onto G3(c) (factored) or fresh
-                ok = wait_or_abort(s, &s.mready, c & 1);
+                ok = wait_or_abort(s, &s.mready, c & 1, wlim);
                 if (!ok) break;
                 tc_fence_after();
                 {
@@ -470,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (c + 1 < nchunks) {
                     // G1(c+1): its tiles landed
-                    ok = wait_or_abort(s, &s.full_c, (c + 1) & 1) &&
-                         wait_or_abort(s, &s.full_b[(c + 1) & 1], ((c + 1) >> 1) & 1);
+                    ok = wait_or_abort(s, &s.full_c, (c + 1) & 1, wlim) &&
+                         wait_or_abort(s, &s.full_b[(c + 1) & 1], ((c + 1) >> 1) & 1, wlim);
                     if (!ok) break;
                     tc_fence_after();
                     g1(c + 1);
@@ -589,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     o_vb[i] = split ? ex2_fast((gmh - o_h[i]) + (gml - o_l[i])) * dt[i] : 1.0f;
             }
             // cv[c % kCv] is free once the epilogue of chunk c-kCv is done
-            const bool ok = c < kCv || wait_or_abort(s, &s.epidone[c % kCv], ((c / kCv) - 1) & 1);
+            const bool ok = c < kCv || wait_or_abort(s, &s.epidone[c % kCv], ((c / kCv) - 1) & 1, wlim);
             if (!__all_sync(0xffffffffu, ok)) break;
             reinterpret_cast<float4*>(cv.g2h)[lane] = make_float4(o_h[0], o_h[1], o_h[2], o_h[3]);
             reinterpret_cast<float4*>(cv.g2l)[lane] = make_float4(o_l[0], o_l[1], o_l[2], o_l[3]);
@@ -716,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (nchunks > 0) {
             load_raw(0);
-            ok = wait_or_abort(s, &s.cvready[0], 0);
+            ok = wait_or_abort(s, &s.cvready[0], 0, wlim);
             if (ok) conv(0);
             fence_proxy_async_smem();  // XR / XS are read by G4 / G2
             mbar_arrive(&s.xready);
@@ -730,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // ---- mask(c): CB -> M in TMEM (this warp's 32-column block) ----
             const bool fac = cv.factored != 0;
-            if (ok) ok = wait_or_abort(s, &s.g1, c & 1);
+            if (ok) ok = wait_or_abort(s, &s.g1, c & 1, wlim);
             if (__all_sync(0xffffffffu, ok)) {
                 if (j <= q) {
                     tc_fence_after();
@@ -796,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&s.mready);
 
             // ---- state(c): h_c = decS h_{c-1} + b dH(c) ----
-            if (ok) ok = wait_or_abort(s, &s.g4, c & 1) && wait_or_abort(s, &s.g3, c & 1);
+            if (ok) ok = wait_or_abort(s, &s.g4, c & 1, wlim) && wait_or_abort(s, &s.g3, c & 1, wlim);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
                 const float2 dS = make_float2(cv.decS, cv.decS);
@@ -818,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- conv(c+1): XS[(c+1)&1] and XR[(c+1)&1] were read by G4(c-1) and
             // G2(c-1), which this thread saw done in the epilogue of chunk c-1 ----
             if (c + 1 < nchunks) {
-                if (ok) ok = wait_or_abort(s, &s.cvready[(c + 1) % kCv], ((c + 1) / kCv) & 1);
+                if (ok) ok = wait_or_abort(s, &s.cvready[(c + 1) % kCv], ((c + 1) / kCv) & 1, wlim);
                 if (ok) conv(c + 1);
                 fence_proxy_async_smem();  // XR / XS are read by G4 / G2
                 mbar_arrive(&s.xready);
@@ -830,8 +837,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // 32 rows leave with one TMA store (rows past the end are not written).
             // The staging tile's last store finished reading it before its issuer's
             // mask(c) arrival, which G2(c), waited on below, comes after. ----
-            if (ok) ok = wait_or_abort(s, &s.g2, c & 1);
-            if (ok && has_z) ok = wait_or_abort(s, &s.full_z, c & 1);
+            if (ok) ok = wait_or_abort(s, &s.g2, c & 1, wlim);
+            if (ok && has_z) ok = wait_or_abort(s, &s.full_z, c & 1, wlim);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
                 const float dec = ex2_fast(fminf(cv.g2h[t] + cv.g2l[t], 0.0f));  // exp(min(gamma_t, 0))

@@ -122,3 +122,81 @@ def oracle_prefill(shape: si.Shape, cpu: dict, conv=True, dt_softplus=True, head
         dt_bias=f64(cpu["dt_bias"])[hh], D=f64(cpu["D"])[hh], z=z, h0=h0,
         dt_softplus=dt_softplus, nthreads=nthreads)
     return y, hS, cs_out, cols
+
+
+class MaxRel:
+    """max|gpu - oracle| / max|oracle| over a tensor compared piece by piece
+    (the same number assert_close computes on the whole tensor), for outputs
+    too large to hold in fp64 on the host at once."""
+
+    def __init__(self, what):
+        self.what, self.err, self.den, self.n = what, 0.0, 0.0, 0
+
+    def add(self, gpu, ref):
+        g = f64(gpu) if isinstance(gpu, torch.Tensor) else np.asarray(gpu, np.float64)
+        r = np.asarray(ref, np.float64)
+        assert g.shape == r.shape, (self.what, g.shape, r.shape)
+        assert np.all(np.isfinite(g)), f"{self.what}: non-finite GPU output"
+        if g.size:
+            self.err = max(self.err, float(np.max(np.abs(g - r))))
+            self.den = max(self.den, float(np.max(np.abs(r))))
+        self.n += g.size
+
+    def check(self, tol, count):
+        assert self.n == count, (self.what, self.n, count)
+        e = self.err / self.den if self.den > 0 else self.err
+        assert e <= tol, f"{self.what}: relative error {e:.3e} > {tol:.1e}"
+        return e
+
+
+def oracle_prefill_by_group(shape: si.Shape, cpu: dict, b: int, g: int, conv=True,
+                            dt_softplus=True, nthreads=None):
+    """fp64 oracle of sequence ``b`` for the heads of group ``g`` only, with the
+    group's own B/C columns (one group per call keeps the fp64 copies of a
+    long sequence small).  ``cpu`` holds host tensors [B, ...].  Returns
+    (heads, y [S,hpg,P], hS [hpg,P,N], conv state [W-1, cols] or None, cols)."""
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    hpg = H // G
+    heads = np.arange(g * hpg, (g + 1) * hpg)
+    cols = np.concatenate([np.arange(g * hpg * P, (g + 1) * hpg * P),
+                           H * P + g * N + np.arange(N),
+                           H * P + G * N + g * N + np.arange(N)])
+    tc, th = torch.from_numpy(cols), torch.from_numpy(heads)
+    xbc = f64(cpu["xbc"][b][:, tc])[None]
+    cs = cpu.get("conv_state")
+    cs = f64(cs[b][:, tc])[None] if (cs is not None and conv) else None
+    z = cpu.get("z")
+    z = f64(z[b][:, g * hpg * P:(g + 1) * hpg * P])[None] if z is not None else None
+    h0 = cpu.get("ssm_state")
+    h0 = f64(h0[b][th])[None] if h0 is not None else None
+    y, hS, cs_out = oracle.mixer_prefill(
+        xbc, f64(cpu["conv_w"][tc]) if conv else None, f64(cpu["dt_raw"][b][:, th])[None],
+        f64(cpu["A"][th]), H=hpg, P=P, N=N, G=1,
+        conv_b=f64(cpu["conv_b"][tc]) if conv else None, conv_state=cs,
+        dt_bias=f64(cpu["dt_bias"][th]), D=f64(cpu["D"][th]), z=z, h0=h0,
+        dt_softplus=dt_softplus, nthreads=nthreads)
+    return heads, y[0], hS[0], (cs_out[0] if cs_out is not None else None), cols
+
+
+def check_prefill_every_element(shape: si.Shape, cpu: dict, y, h, cs, act, batches=None,
+                                conv=True, gpu_batch_of=None):
+    """Compare every element of y and of the final SSM state of the listed
+    sequences (all by default) with the oracle, one (sequence, group) at a
+    time, and the conv state bit for bit.  ``gpu_batch_of[i]`` is the index in
+    the GPU tensors of the i-th listed sequence (default: the same index)."""
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    batches = list(range(shape.batch)) if batches is None else list(batches)
+    ey, eh = MaxRel("y"), MaxRel("ssm_state")
+    for i, b in enumerate(batches):
+        gb = b if gpu_batch_of is None else gpu_batch_of[i]
+        for g in range(G):
+            heads, yo, ho, co, cols = oracle_prefill_by_group(shape, cpu, b, g, conv=conv)
+            h0_, h1_ = int(heads[0]), int(heads[-1]) + 1
+            ey.add(y[gb, :, h0_:h1_], yo)
+            eh.add(h[gb, h0_:h1_], ho)
+            if conv and cs is not None:
+                gcs = f64(cs[gb][:, torch.from_numpy(cols).to(cs.device)])
+                assert np.array_equal(gcs, co), "conv state must be the raw rows, bit for bit"
+    tol = TOL[act]
+    n = len(batches)
+    return (ey.check(tol, n * shape.seqlen * H * P), eh.check(tol, n * H * P * N))

@@ -44,9 +44,20 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for s in range(6):
-        assert ssd.ssd_status_string(s)
+    for s in range(7):
+        assert ssd.ssd_status_string(s) != "unknown status"
     assert "slot" in ssd.ssd_status_string(ssd.SSD_ERR_BAD_SLOT)
+    assert "twice" in ssd.ssd_status_string(ssd.SSD_ERR_DUPLICATE_SLOT)
+
+
+def test_process_wide_settings_round_trip(lib):
+    """The debug-check and wait-limit setters return the previous value and
+    touch no device (host-side settings read at each launch)."""
+    assert ssd.ssd_set_debug_checks(ssd.SSD_CHECK_DISTINCT_SLOTS) == 0
+    assert ssd.ssd_set_debug_checks(0xff) == ssd.SSD_CHECK_DISTINCT_SLOTS
+    assert ssd.ssd_set_debug_checks(0) == ssd.SSD_CHECK_DISTINCT_SLOTS  # unknown bits dropped
+    assert ssd.ssd_set_wait_limit_ns(500) == 0
+    assert ssd.ssd_set_wait_limit_ns(0) == 500
 
 
 def _d(**kw):

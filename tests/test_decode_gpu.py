@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import ssd_inputs as si
-from tests.helpers import TOL, assert_close, f64
+from tests.helpers import TOL, MaxRel, assert_close, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -137,30 +137,43 @@ def test_bad_slot_sets_error_word_and_writes_nothing():
     assert torch.isfinite(y[0].float()).all() and torch.isfinite(y[2].float()).all()
 
 
-def test_decode_full_size_sampled():
-    """256 rows in a 1024-slot pool [1024,128,64,128] fp32, 64 steps; the oracle
-    follows 3 rows through all steps."""
+def test_decode_full_size_every_row():
+    """256 rows in a 1024-slot pool [1024,128,64,128] fp32, 64 steps: every y of
+    every row and step, every touched slot's SSM state (tolerance) and conv
+    state (bit for bit) against the oracle, which follows each row through the
+    64 steps as one 64-row sequence from the slot's initial states.  Untouched
+    slots stay bit-identical."""
     shape = si.DECODE
     prm, pools = _setup(shape, si.DECODE_SLOTS)
-    rows = [0, 101, 255]
-    slots = pools["slot_ids"].cpu().numpy()
-    h0 = f64(pools["ssm_pool"][pools["slot_ids"][rows].long()])
-    c0 = f64(pools["conv_pool"][pools["slot_ids"][rows].long()])
+    sl = pools["slot_ids"].long()
+    h0_all = pools["ssm_pool"][sl].clone()
+    c0_all = pools["conv_pool"][sl].clone()
+    untouched = torch.ones(si.DECODE_SLOTS, dtype=torch.bool, device="cuda")
+    untouched[sl] = False
+    probe = torch.nonzero(untouched).flatten()[:64]
+    pool_probe = pools["ssm_pool"][probe].clone()
+    cpool_probe = pools["conv_pool"][probe].clone()
     xs, dts, zs, ys = [], [], [], []
     for t in range(si.DECODE_STEPS):
         inp = _inputs(shape, t)
-        y = _step(shape, prm, pools, inp)
-        xs.append(f64(inp["xbc"][rows]))
-        dts.append(f64(inp["dt_raw"][rows]))
-        zs.append(f64(inp["z"][rows]))
-        ys.append(y[rows].float().cpu())
+        ys.append(_step(shape, prm, pools, inp))
+        xs.append(inp["xbc"])
+        dts.append(inp["dt_raw"])
+        zs.append(inp["z"])
+    X, DT, Z, Y = (torch.stack(v, 1) for v in (xs, dts, zs, ys))  # [R, steps, ...]
+    assert torch.equal(pools["ssm_pool"][probe], pool_probe)
+    assert torch.equal(pools["conv_pool"][probe], cpool_probe)
     H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
-    y_o, h_o, c_o = oracle.mixer_prefill(
-        np.stack(xs, 1), f64(prm["conv_w"]), np.stack(dts, 1), f64(prm["A"]), H=H, P=P, N=N,
-        G=G, conv_b=f64(prm["conv_b"]), conv_state=c0, dt_bias=f64(prm["dt_bias"]),
-        D=f64(prm["D"]), z=np.stack(zs, 1), h0=h0)
-    assert_close(torch.stack(ys, 1), y_o, TOL[torch.bfloat16], what="y")
-    assert_close(pools["ssm_pool"][pools["slot_ids"][rows].long()], h_o, TOL[torch.bfloat16],
-                 what="pool")
-    assert np.array_equal(f64(pools["conv_pool"][pools["slot_ids"][rows].long()]), c_o)
-    assert torch.isfinite(pools["ssm_pool"][pools["slot_ids"].long()]).all()
+    R = si.DECODE_ROWS
+    ey, eh = MaxRel("y"), MaxRel("pool")
+    for r0 in range(0, R, 32):
+        rr = slice(r0, r0 + 32)
+        y_o, h_o, c_o = oracle.mixer_prefill(
+            f64(X[rr]), f64(prm["conv_w"]), f64(DT[rr]), f64(prm["A"]), H=H, P=P, N=N, G=G,
+            conv_b=f64(prm["conv_b"]), conv_state=f64(c0_all[rr]), dt_bias=f64(prm["dt_bias"]),
+            D=f64(prm["D"]), z=f64(Z[rr]), h0=f64(h0_all[rr]))
+        ey.add(Y[rr], y_o)
+        eh.add(pools["ssm_pool"][sl[rr]], h_o)
+        assert np.array_equal(f64(pools["conv_pool"][sl[rr]]), c_o)
+    ey.check(TOL[torch.bfloat16], R * si.DECODE_STEPS * H * P)
+    eh.check(TOL[torch.bfloat16], R * H * P * N)

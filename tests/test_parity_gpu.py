@@ -9,8 +9,8 @@ import torch
 
 import oracle
 import ssd_inputs as si
-from tests.helpers import (TOL, assert_close, f64, gpu_prefill, make_problem,
-                           oracle_prefill)
+from tests.helpers import (TOL, assert_close, check_prefill_every_element, f64, gpu_prefill,
+                           make_problem, oracle_prefill)
 
 pytestmark = pytest.mark.gpu
 
@@ -58,13 +58,11 @@ def test_tiny_fp32(splits, init):
 def test_tiny_fp32_no_conv_no_z_no_softplus():
     shape = si.TINY
     cpu, dev = make_problem(shape, act=torch.float32, with_z=False)
+    dt = cpu["dt_raw"].abs() * 0.1  # dt taken as given: positive, moderate
+    cpu["dt_raw"] = dt
+    dev["dt_raw"] = dt.cuda()
     y, h, _ = gpu_prefill(shape, dev, [7, 4], conv=False, dt_softplus=False)
-    dev2 = dict(dev)
-    dev2["dt_raw"] = dev["dt_raw"].abs() * 0.1
-    cpu2 = dict(cpu)
-    cpu2["dt_raw"] = cpu["dt_raw"].abs() * 0.1
-    y, h, _ = gpu_prefill(shape, dev2, [7, 4], conv=False, dt_softplus=False)
-    _check_prefill(shape, cpu2, y, h, None, torch.float32, conv=False, dt_softplus=False)
+    _check_prefill(shape, cpu, y, h, None, torch.float32, conv=False, dt_softplus=False)
 
 
 def test_dt_zero_leaves_state_bit_unchanged():
@@ -134,27 +132,27 @@ def test_decay_stress_small():
 
 
 # ---------------------------------------------------------------------------
-# Nemotron-H-8B-shaped prefill at full size: B=1, S=2048, H=128 (sampled heads)
+# Nemotron-H-8B-shaped prefill at full size: B=1, S=2048, H=128; every
+# element of y and of the final states against the oracle
 
-def test_prefill_full_size_sampled_heads():
+def test_prefill_full_size_every_element():
     shape = si.PREFILL
     cpu, dev = make_problem(shape, act=torch.bfloat16)
     y, h, cs = gpu_prefill(shape, dev)
-    assert torch.isfinite(y.float()).all() and torch.isfinite(h).all()
-    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16, heads=[0, 17, 63, 64, 127])
+    check_prefill_every_element(shape, cpu, y, h, cs, torch.bfloat16)
 
 
-def test_prefill_137_rows_full_heads_sampled():
+def test_prefill_137_rows_every_element():
     shape = si.PREFILL.with_(seqlen=137)
     cpu, dev = make_problem(shape, act=torch.bfloat16, seed=5, initial_state=False)
     y, h, cs = gpu_prefill(shape, dev)
-    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16, heads=[1, 30, 99, 126])
+    check_prefill_every_element(shape, cpu, y, h, cs, torch.bfloat16)
 
 
 # ---------------------------------------------------------------------------
-# the other workloads at full size, in the calls the benchmark makes; the
-# oracle checks sampled (sequence, head) pairs.  Inputs are drawn on the GPU
-# and only the sampled sequences are copied to the host.
+# the other workloads at full size, in the calls the benchmark makes.  Inputs
+# are drawn on the GPU; the checked sequences are copied to the host and the
+# oracle runs one (sequence, group of heads) at a time.
 
 def _device_problem(shape, seed, stress=False):
     prm = si.params(shape, seed=seed, stress=stress)
@@ -168,10 +166,11 @@ def _host_subset(prm, inp, batches):
     return {**prm, **sub}
 
 
-def test_long_prefill_full_size_chained_sampled():
+def test_long_prefill_full_size_chained_every_element():
     """8 sequences x 8192 rows, then a second 8192-row call fed with the first
-    call's final states, on all 128 heads; the oracle checks two sequences x two
-    heads over all 16384 rows."""
+    call's final states, on all 128 heads; every element of two sequences
+    (all heads, all 16384 rows, both final states) against the oracle, and
+    every output finite."""
     shape = si.LONG.with_(seqlen=2 * si.LONG.seqlen)
     prm, inp, dev = _device_problem(shape, seed=11)
     y, h, cs = gpu_prefill(shape, dev, [si.LONG.seqlen, si.LONG.seqlen])
@@ -179,19 +178,44 @@ def test_long_prefill_full_size_chained_sampled():
     bb = [0, 7]
     cpu = _host_subset(prm, inp, bb)
     del inp, dev
-    _check_prefill(shape.with_(batch=len(bb)), cpu, y[bb], h[bb], cs[bb], torch.bfloat16,
-                   heads=[5, 98])
+    check_prefill_every_element(shape.with_(batch=len(bb)), cpu, y, h, cs, torch.bfloat16,
+                                gpu_batch_of=bb)
 
 
-def test_decay_stress_full_size_sampled():
+def test_decay_stress_full_size_every_element():
     """4 sequences x 4096 rows with decays up to ~1e4 per row, fed as calls of
-    U{1..128} rows: finite everywhere, and two heads of every sequence checked."""
+    U{1..128} rows, one split shared by the batch: every element against the
+    oracle."""
     shape = si.STRESS
     prm, inp, dev = _device_problem(shape, seed=13, stress=True)
     y, h, cs = gpu_prefill(shape, dev, si.random_splits(shape.seqlen, seed=13))
     assert torch.isfinite(y.float()).all() and torch.isfinite(h).all()
     cpu = _host_subset(prm, inp, list(range(shape.batch)))
-    _check_prefill(shape, cpu, y, h, cs, torch.bfloat16, heads=[2, 121])
+    check_prefill_every_element(shape, cpu, y, h, cs, torch.bfloat16)
+
+
+def test_decay_stress_independent_splits_per_sequence():
+    """The same stress sequences, each on its own (batch 1) with its own seeded
+    split of U{1..128}-row calls: every element against the oracle, and the
+    same numbers (within the tolerance of each against the oracle, twice over)
+    as one call over the whole sequence and as the shared-split batched run."""
+    shape = si.STRESS
+    prm, inp, dev = _device_problem(shape, seed=13, stress=True)
+    yb, hb, _ = gpu_prefill(shape, dev, si.random_splits(shape.seqlen, seed=13))
+    one = shape.with_(batch=1)
+    for b in range(shape.batch):
+        dev1 = {k: (v[b:b + 1].contiguous() if (k in inp and v is not None) else v)
+                for k, v in dev.items()}
+        splits = si.random_splits(shape.seqlen, seed=100 + b)
+        y, h, cs = gpu_prefill(one, dev1, splits)
+        cpu = _host_subset(prm, inp, [b])
+        check_prefill_every_element(one, cpu, y, h, cs, torch.bfloat16)
+        y1, h1, _ = gpu_prefill(one, dev1)  # the whole sequence in one call
+        tol2 = 2 * TOL[torch.bfloat16]
+        assert_close(y, f64(y1), tol2, what="y vs one call")
+        assert_close(h, f64(h1), tol2, what="state vs one call")
+        assert_close(y, f64(yb[b:b + 1]), tol2, what="y vs batched")
+        assert_close(h, f64(hb[b:b + 1]), tol2, what="state vs batched")
 
 
 def test_prefill_eight_heads_per_group():

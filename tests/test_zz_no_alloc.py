@@ -68,12 +68,18 @@ def _run_both(shape, seed):
 
 
 def _compare(shape, got, ref):
+    """Both entry points run the same kernels on the same inputs, so every
+    output must agree bit for bit (a stale scratch row that moved a few values
+    within the tolerance would still show); the tolerance check is kept as the
+    bound the other parity tests use."""
     tol = TOL[torch.bfloat16]
     B, S, H, P, N = shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate
     assert_close(got[0], ref[0].float().cpu().double().numpy(), tol, count=B * S * H * P,
                  what="y")
     assert_close(got[1], ref[1].cpu().double().numpy(), tol, count=B * H * P * N,
                  what="ssm_state")
+    assert torch.equal(got[0], ref[0]), "y must equal the workspace entry's, bit for bit"
+    assert torch.equal(got[1], ref[1]), "ssm state must equal the workspace entry's"
     assert torch.equal(got[2], ref[2]), "conv state must be the raw rows, bit for bit"
 
 
@@ -102,3 +108,20 @@ def test_static_scratch_rejects_problems_larger_than_the_array():
     assert e.value.status == ssd.SSD_ERR_UNSUPPORTED
     assert ssd.ssd_launch_counts() == before, "a rejected call must launch nothing"
     assert torch.isnan(out[0]).all()
+
+
+def test_static_scratch_size_check_comes_before_the_argument_checks():
+    """A problem too large for the array is refused as unsupported before any
+    other argument is looked at: even with a null y it returns
+    SSD_ERR_UNSUPPORTED (ssd_chunk_scan itself would say invalid argument)."""
+    shape = si.Shape(batch=1, seqlen=33024, nheads=2, headdim=64, dstate=128, ngroups=1)
+    d = ssd.dims(shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate,
+                 shape.ngroups, shape.conv_width, shape.chunk)
+    flags = ssd.SSD_DT_SOFTPLUS | ssd.SSD_HAS_Z
+    _, dev = make_problem(shape, seed=3, act=torch.bfloat16)
+    y, h, cs = _outputs(shape, dev)
+    args = list(_args(dev, (y, h, cs)))
+    args[11] = None  # y
+    with pytest.raises(ssd.SsdError) as e:
+        ssd.ssd_chunk_scan_static_ws(d, ssd.SSD_BF16, flags, *args)
+    assert e.value.status == ssd.SSD_ERR_UNSUPPORTED
