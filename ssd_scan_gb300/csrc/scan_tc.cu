@@ -193,6 +193,22 @@ __device__ __forceinline__ void df_add(float& hi, float& lo, float bhi, float bl
     lo = e - (hi - s);
 }
 
+// (hi, lo) * log2(e) as a double-float: the product of hi with the fp32 part
+// of log2(e), its exact rounding error by FMA (Dekker's product), plus the
+// terms of lo and of log2(e)'s low part, renormalised.  A plain fp32 product
+// hi * log2(e) would drop up to half an ulp of |gamma| (0.06 at |gamma| ~ 1e6),
+// which exp2 turns into a relative error of several percent.
+__device__ __forceinline__ void df_to_log2(float hi, float lo, float& rh, float& rl)
+{
+    constexpr float kL = 1.4426950408889634f;     // log2(e) rounded to fp32
+    constexpr float kLlo = 1.925963e-8f;          // log2(e) - kL
+    const float p = hi * kL;
+    float e = fmaf(hi, kL, -p);
+    e += fmaf(hi, kLlo, lo * kL);
+    rh = p + e;
+    rl = e - (rh - p);
+}
+
 __device__ __forceinline__ void unpack4x2(uint4 r, float2* f)
 {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
@@ -510,7 +526,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
         const float Dabs = p.D ? fabsf(p.D[h]) : 0.0f;
         const bool softplus = (p.flags & kDtSoftplus) != 0;
-        constexpr float kLog2e = 1.4426950408889634f;
         float dtn[4];
         auto load_dt = [&](int c) {
 #pragma unroll
@@ -555,16 +570,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) eh = el = 0.0f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) df_add(gh[i], gl[i], eh, el);
-            // gamma_Q: the last element of the cumulative sum (rows past the end
-            // add a = 0, so row Q-1 holds it)
-            const float gLh = __shfl_sync(0xffffffffu, th, 31) * kLog2e;
-            const float gLl = __shfl_sync(0xffffffffu, tl, 31) * kLog2e;
-            const bool factored = __all_sync(0xffffffffu, dt_ok) && Ah <= 0.0f && gLh + gLl >= kFactorMinLog2;
+            // gamma in log2 units, per row; gamma_Q is the last element of the
+            // cumulative sum as stored for row Q-1 (rows past the end add a = 0),
+            // so its difference with that row is exactly 0
             float o_h[4], o_l[4], o_sc[4], o_vb[4];
 #pragma unroll
+            for (int i = 0; i < 4; ++i) df_to_log2(gh[i], gl[i], o_h[i], o_l[i]);
+            const float gLh = __shfl_sync(0xffffffffu, o_h[3], 31);
+            const float gLl = __shfl_sync(0xffffffffu, o_l[3], 31);
+            const bool factored = __all_sync(0xffffffffu, dt_ok) && Ah <= 0.0f && gLh + gLl >= kFactorMinLog2;
+#pragma unroll
             for (int i = 0; i < 4; ++i) {
-                o_h[i] = gh[i] * kLog2e;
-                o_l[i] = gl[i] * kLog2e;
                 o_sc[i] = factored ? ex2_fast(-(o_h[i] + o_l[i])) * dt[i]
                                    : ex2_fast(fminf((gLh - o_h[i]) + (gLl - o_l[i]), 0.0f)) * dt[i];
             }

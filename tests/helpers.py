@@ -200,3 +200,17 @@ def check_prefill_every_element(shape: si.Shape, cpu: dict, y, h, cs, act, batch
     tol = TOL[act]
     n = len(batches)
     return (ey.check(tol, n * shape.seqlen * H * P), eh.check(tol, n * H * P * N))
+
+
+def oracle_sequence(shape: si.Shape, cpu: dict, b: int, conv=True, dt_softplus=True):
+    """The oracle's y [S,H,P] and final SSM state [H,P,N] of sequence ``b``
+    over all heads, computed one group of heads at a time."""
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    y = np.empty((shape.seqlen, H, P))
+    hS = np.empty((H, P, N))
+    for g in range(G):
+        heads, yo, ho, _, _ = oracle_prefill_by_group(shape, cpu, b, g, conv=conv,
+                                                      dt_softplus=dt_softplus)
+        y[:, heads] = yo
+        hS[heads] = ho
+    return y, hS

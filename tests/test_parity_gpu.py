@@ -10,7 +10,7 @@ import torch
 import oracle
 import ssd_inputs as si
 from tests.helpers import (TOL, assert_close, check_prefill_every_element, f64, gpu_prefill,
-                           make_problem, oracle_prefill)
+                           make_problem, oracle_prefill, oracle_sequence)
 
 pytestmark = pytest.mark.gpu
 
@@ -195,27 +195,29 @@ def test_decay_stress_full_size_every_element():
 
 
 def test_decay_stress_independent_splits_per_sequence():
-    """The same stress sequences, each on its own (batch 1) with its own seeded
-    split of U{1..128}-row calls: every element against the oracle, and the
-    same numbers (within the tolerance of each against the oracle, twice over)
-    as one call over the whole sequence and as the shared-split batched run."""
+    """The same stress sequences, each on its own (batch 1): once with its own
+    seeded split of U{1..128}-row calls and once as one 4096-row call.  Both
+    against the oracle, every element; and the shared-split batched run too.
+    (One long call is where every chunk's total decay is ~1e6: gamma_Q must be
+    the last row's own cumulative-sum value, converted to log2 units without
+    losing its low part, or the final state is off by several percent.)"""
     shape = si.STRESS
     prm, inp, dev = _device_problem(shape, seed=13, stress=True)
     yb, hb, _ = gpu_prefill(shape, dev, si.random_splits(shape.seqlen, seed=13))
     one = shape.with_(batch=1)
+    tol = TOL[torch.bfloat16]
+    n_y, n_h = shape.seqlen * shape.nheads * shape.headdim, shape.nheads * 64 * 128
     for b in range(shape.batch):
         dev1 = {k: (v[b:b + 1].contiguous() if (k in inp and v is not None) else v)
                 for k, v in dev.items()}
-        splits = si.random_splits(shape.seqlen, seed=100 + b)
-        y, h, cs = gpu_prefill(one, dev1, splits)
         cpu = _host_subset(prm, inp, [b])
-        check_prefill_every_element(one, cpu, y, h, cs, torch.bfloat16)
+        yo, ho = oracle_sequence(one, cpu, 0)
+        ys, hs, _ = gpu_prefill(one, dev1, si.random_splits(shape.seqlen, seed=100 + b))
         y1, h1, _ = gpu_prefill(one, dev1)  # the whole sequence in one call
-        tol2 = 2 * TOL[torch.bfloat16]
-        assert_close(y, f64(y1), tol2, what="y vs one call")
-        assert_close(h, f64(h1), tol2, what="state vs one call")
-        assert_close(y, f64(yb[b:b + 1]), tol2, what="y vs batched")
-        assert_close(h, f64(hb[b:b + 1]), tol2, what="state vs batched")
+        for what, yy, hh in (("split", ys[0], hs[0]), ("one call", y1[0], h1[0]),
+                             ("batched", yb[b], hb[b])):
+            assert_close(yy, yo, tol, count=n_y, what=f"seq {b} y ({what})")
+            assert_close(hh, ho, tol, count=n_h, what=f"seq {b} state ({what})")
 
 
 def test_prefill_eight_heads_per_group():
