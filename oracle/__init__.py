@@ -24,6 +24,11 @@ Functions (each cites the passage it follows in ``ssd_oracle.c``):
   "nemotron.md" section 11).
 * :func:`gated_group_rmsnorm` -- group RMSNorm of y, then the SiLU(z) gate
   (TensorSharp "nemotron.md" sections 3, 4.1 and 6).
+* :func:`segment_decay` / :func:`state_combine` -- a segment's total decay
+  (the last element of its cumulative sum of dt A) and the state after two
+  consecutive segments (TensorRT-Model-Connect #2207 "Implementation": the
+  chunk form's carry, with a whole segment as the chunk); the pieces of
+  sequence-parallel state passing.
 
 Parity unpinned: none (see tests/test_oracle.py for the pins).
 """
@@ -80,6 +85,10 @@ def open_library(path: str):
     for name in ("oracle_ssd_sequential", "oracle_ssd_chunked"):
         getattr(lib, name).restype = ctypes.c_int
     lib.oracle_decode_step.restype = ctypes.c_int
+    lib.oracle_segment_decay.restype = None
+    lib.oracle_segment_decay.argtypes = [ctypes.c_int] * 3 + [ctypes.c_uint] + [dp] * 4
+    lib.oracle_state_combine.restype = None
+    lib.oracle_state_combine.argtypes = [ctypes.c_int, ctypes.c_long] + [dp] * 4
     lib.oracle_gated_group_rmsnorm.restype = None
     lib.oracle_gated_group_rmsnorm.argtypes = [ctypes.c_long, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_double] + [dp] * 4
@@ -286,3 +295,29 @@ def gated_group_rmsnorm(y, z, w, eps, G):
     _load().oracle_gated_group_rmsnorm(rows, C, G, float(eps), _dp(y), _dp(z), _dp(w), _dp(out))
     return out
 
+
+
+def segment_decay(dt_raw, A, *, dt_bias=None, dt_softplus=True):
+    """gamma[b,h] = sum_t dt[b,t,h] * A[h] over the rows of dt_raw [B,S,H]."""
+    dt_raw = _f64(dt_raw)
+    B, S, H = dt_raw.shape
+    A_ = _f64(A)
+    dtb = _f64(dt_bias)
+    out = np.empty((B, H), np.float64)
+    _load().oracle_segment_decay(B, S, H, DT_SOFTPLUS if dt_softplus else 0, _dp(dt_raw),
+                                 _dp(dtb), _dp(A_), _dp(out))
+    return out
+
+
+def state_combine(gamma, h_prev, h_seg):
+    """exp(min(gamma, 0)) * h_prev + h_seg per (sequence, head); gamma [B,H],
+    states [B,H,P,N]; h_prev None means zeros."""
+    g = _f64(gamma)
+    hs = _f64(h_seg)
+    hp = _f64(h_prev)
+    B, H = g.shape
+    assert hs.shape[:2] == (B, H) and (hp is None or hp.shape == hs.shape)
+    out = np.empty_like(hs)
+    _load().oracle_state_combine(B * H, hs.shape[2] * hs.shape[3], _dp(g), _dp(hp), _dp(hs),
+                                 _dp(out))
+    return out

@@ -59,7 +59,8 @@
  * that prove the pins can see it; a normal build never defines it.  In the
  * chunk form: 10 drops every clamp, 11 takes gamma_L from a separate
  * reduction (fp32, rows in reverse) with the state exponent unclamped, 12
- * clamps gamma_t and gamma_s one by one instead of their difference. */
+ * clamps gamma_t and gamma_s one by one instead of their difference; 13
+ * combines two segments' states without the second segment's decay. */
 #ifndef ORACLE_MUTANT
 #define ORACLE_MUTANT 0
 #endif
@@ -450,6 +451,57 @@ void oracle_gated_group_rmsnorm(long rows, int C, int G, double eps, const doubl
             const double inv = ORACLE_MUTANT == 8 ? 1.0 / (sqrt(ms) + eps) : 1.0 / sqrt(ms + eps);
             for (int c = g * gs; c < (g + 1) * gs; ++c)
                 o[c] = oracle_silu(zr[c]) * (yr[c] * inv) * w[c];
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sequence-parallel state passing: the rows of a sequence split into       */
+/* consecutive segments, each scanned from a zero state, then chained.      */
+
+/*
+ * The total decay of a segment, per (sequence, head): the last element of
+ * the cumulative sum gamma_t = sum_{i<=t} dt_i A_h over the segment's rows
+ * ([TRT] Implementation, where gamma of a chunk is that cumulative sum and
+ * its last element carries the state to the next chunk).
+ *   gamma[b,h] = sum_{t=0}^{S-1} dt[b,t,h] * A[h]
+ * with dt = softplus(dt_raw + dt_bias) under ORACLE_DT_SOFTPLUS, else dt_raw.
+ */
+void oracle_segment_decay(int B, int S, int H, unsigned flags, const double* dt_raw,
+                          const double* dt_bias, const double* A, double* gamma)
+{
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            double g = 0.0;
+            for (int t = 0; t < S; ++t) {
+                double v = dt_raw[((size_t)b * S + t) * H + h];
+                if (flags & ORACLE_DT_SOFTPLUS) {
+                    if (dt_bias && ORACLE_MUTANT != 5) v += dt_bias[h];
+                    v = oracle_softplus(v);
+                }
+                g += v * A[h];
+            }
+            gamma[(size_t)b * H + h] = g;
+        }
+}
+
+/*
+ * The state after two consecutive segments: the first one's final state
+ * h_prev decays through the second segment, whose own contribution h_seg is
+ * its final state from a zero start ([TRT] Implementation: the chunk form's
+ * carry h <- exp(min(gamma_L, 0)) h + (the chunk's terms), applied with the
+ * second segment as the chunk).
+ *   out[b,h,:,:] = exp(min(gamma[b,h], 0)) * h_prev[b,h,:,:] + h_seg[b,h,:,:]
+ * h_prev NULL means zeros.
+ */
+void oracle_state_combine(int BH, long PN, const double* gamma, const double* h_prev,
+                          const double* h_seg, double* out)
+{
+    for (int i = 0; i < BH; ++i) {
+        const double e = ORACLE_MUTANT == 13 ? 1.0 : exp(gamma[i] < 0.0 ? gamma[i] : 0.0);
+        for (long k = 0; k < PN; ++k) {
+            const size_t j = (size_t)i * PN + k;
+            out[j] = (h_prev ? e * h_prev[j] : 0.0) + h_seg[j];
         }
     }
 }

@@ -12,6 +12,7 @@ gate applied before the norm.  Mutants 10-12 are in the chunk form's clamp
 of the cumulative sum, not a separate reduction, and every exponent is
 clamped at 0): no clamp at all, gamma_L from a separate fp32 reduction with
 its state exponent unclamped, and gamma_t, gamma_s clamped one by one.
+Mutant 13 chains two segments' states without the second segment's decay.
 """
 import pytest
 
@@ -38,10 +39,12 @@ PINS = [
     pins.test_chunk_form_clamp_hand_values,
     pins.test_chunk_form_clamp_carries_across_chunks,
     lambda: pins.test_huge_decay_limit("chunked"),
+    pins.test_state_combine_hand_values,
+    lambda: pins.test_segments_chained_by_combine_equal_one_call([3, 8]),
 ]
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13])
 def test_pins_catch_mutant(mutant, tmp_path, monkeypatch):
     lib = oracle.open_library(oracle.build(out_path=str(tmp_path / f"m{mutant}.so"),
                                            mutant=mutant))

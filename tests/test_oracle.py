@@ -518,3 +518,52 @@ def test_varlen_of_equal_lengths_equals_the_batched_call():
         z=z.reshape(3, 4, -1), h0=spool)
     assert np.array_equal(y.reshape(yb.shape), yb)
     assert np.array_equal(sp, hb) and np.array_equal(cp, cb)
+
+
+
+# --------------------------------------------------------------------------
+# sequence-parallel state passing: segments scanned from a zero state, then
+# chained by the decay of each segment (TensorRT-Model-Connect #2207
+# "Implementation": the chunk form's carry with a segment as the chunk)
+
+def test_segment_decay_hand_values():
+    # dt as given: gamma = (0.5 + 1.5) * -2 = -4 ; with softplus and bias 0:
+    # softplus(0) = ln 2, softplus(ln 3) = ln 4 -> gamma = (ln 2 + ln 4) * -1 = -ln 8
+    g = oracle.segment_decay(np.array([[[0.5], [1.5]]]), np.array([-2.0]), dt_softplus=False)
+    assert g.shape == (1, 1) and g[0, 0] == -4.0
+    g = oracle.segment_decay(np.array([[[0.0], [math.log(3.0)]]]), np.array([-1.0]),
+                             dt_bias=np.array([0.0]))
+    assert abs(g[0, 0] + math.log(8.0)) < 1e-15
+
+
+def test_state_combine_hand_values():
+    hp = np.arange(8, dtype=np.float64).reshape(1, 2, 2, 2)
+    hs = np.ones((1, 2, 2, 2))
+    out = oracle.state_combine(np.array([[0.0, -math.log(2.0)]]), hp, hs)
+    assert np.array_equal(out[0, 0], hp[0, 0] + 1.0)
+    assert np.allclose(out[0, 1], 0.5 * hp[0, 1] + 1.0, rtol=0, atol=1e-15)
+    assert np.array_equal(oracle.state_combine(np.array([[-3.0, -1.0]]), None, hs), hs)
+
+
+@pytest.mark.parametrize("cuts", [[5], [3, 8], [1, 2, 9]])
+def test_segments_chained_by_combine_equal_one_call(cuts):
+    """Split the 11 rows at ``cuts``; scan every segment from a zero state;
+    chain: h <- state_combine(gamma_k, h, h_k) from h0.  The result is the
+    final state of one row-by-row call over all rows, and rescanning each
+    segment from the chained state gives that call's y."""
+    prob = _tiny_problem(h0=True)
+    kw = dict(dt_bias=prob["dt_bias"], D=prob["D"])
+    y, hS = oracle.ssd_sequential(prob["xbc"], prob["dt_raw"], prob["A"], **_dims(TINY),
+                                  h0=prob["h0"], **kw)
+    edges = [0] + list(cuts) + [11]
+    h = prob["h0"]
+    ys = []
+    for a, b in zip(edges[:-1], edges[1:]):
+        xs, ds = prob["xbc"][:, a:b], prob["dt_raw"][:, a:b]
+        _, h_k = oracle.ssd_sequential(xs, ds, prob["A"], **_dims(TINY), **kw)  # zero start
+        g_k = oracle.segment_decay(ds, prob["A"], dt_bias=prob["dt_bias"])
+        y_k, _ = oracle.ssd_sequential(xs, ds, prob["A"], **_dims(TINY), h0=h, **kw)
+        ys.append(y_k)
+        h = oracle.state_combine(g_k, h, h_k)
+    assert _relerr(h, hS) < 1e-13
+    assert _relerr(np.concatenate(ys, axis=1), y) < 1e-13
