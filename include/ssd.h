@@ -318,6 +318,48 @@ SSD_API ssd_status ssd_gated_group_rmsnorm(const ssd_dims* dims, ssd_dtype act, 
                                            void* out, cudaStream_t stream);
 
 /*
+ * Sequence-parallel state passing: the rows of one sequence split into
+ * consecutive segments (one per GPU), each scanned with ssd_chunk_scan.
+ * (TensorRT-Model-Connect #2207 "Implementation": the chunk form, where
+ * gamma of a chunk is the cumulative sum of a = dt A, its last element
+ * carries the state to the next chunk, h <- exp(min(gamma_S, 0)) h + the
+ * chunk's own terms, and every exponent is clamped at <= 0 -- applied here
+ * with a whole segment in the role of the chunk.)
+ *
+ * Segment k scanned from a zero state (ssm_state_in NULL) ends in its own
+ * contribution h_k; its total decay is Gamma_k = ssd_segment_decay over its
+ * rows.  With h_in_0 the sequence's initial state,
+ *   h_in_{k+1} = exp(min(Gamma_k, 0)) h_in_k + h_k      (ssd_state_combine)
+ * is the state at the start of segment k+1, and h_in_K the final state.
+ * Rescanning segment k from h_in_k (its conv state: the last W-1 raw rows
+ * before it) gives exactly the y of one call over all rows.  The exchange
+ * of (Gamma_k, h_k) between GPUs is the caller's (an all-gather);
+ * ssd_scan_gb300.seqpar drives the whole sequence with torch.distributed.
+ */
+
+/*
+ * ssd_segment_decay -- gamma[b,h] = sum_{t<S} dt[b,t,h] * A[h], with
+ * dt = softplus(dt_raw + dt_bias) under SSD_DT_SOFTPLUS (else dt_raw), the
+ * per-row products in fp32 and their sum in fp64, stored as fp32.
+ * Uses batch, seqlen and nheads of `dims`; flags: SSD_DT_SOFTPLUS only.
+ * dt [B,S,H] fp32, dt_bias [H] or NULL, A [H], gamma [B,H] fp32 (written).
+ * S = 0 gives gamma = 0.
+ */
+SSD_API ssd_status ssd_segment_decay(const ssd_dims* dims, unsigned flags, const float* dt,
+                                     const float* dt_bias, const float* A, float* gamma,
+                                     cudaStream_t stream);
+
+/*
+ * ssd_state_combine -- h_out = exp(min(gamma, 0)) * h_prev + h_seg for every
+ * (sequence, head): gamma [B,H] fp32, h_prev / h_seg / h_out [B,H,P,N] fp32
+ * (16-byte aligned; P*N a multiple of 4).  h_prev NULL means zeros; h_out may
+ * alias h_prev or h_seg exactly.  Uses batch, nheads, headdim, dstate.
+ */
+SSD_API ssd_status ssd_state_combine(const ssd_dims* dims, const float* gamma,
+                                     const float* h_prev, const float* h_seg, float* h_out,
+                                     cudaStream_t stream);
+
+/*
  * Kernel-launch counters, for observability (which path ran, how many
  * kernels a call launched).  Host-side, process-wide, monotonically
  * increasing; one counter per kernel kind below.  Copies min(n,
@@ -332,7 +374,9 @@ enum {
     SSD_KERNEL_DECODE_STEP = 5,    /* slot-indexed decode step              */
     SSD_KERNEL_DECODE_CONV = 6,    /* conv-pool roll of the decode step     */
     SSD_KERNEL_GATED_NORM = 7,     /* group RMSNorm + SiLU(z) gate          */
-    SSD_KERNEL_KINDS = 8
+    SSD_KERNEL_SEGMENT_DECAY = 8,  /* a segment's total decay               */
+    SSD_KERNEL_STATE_COMBINE = 9,  /* state after two consecutive segments  */
+    SSD_KERNEL_KINDS = 10
 };
 SSD_API int ssd_launch_counts(uint64_t* out, int n);
 

@@ -41,10 +41,11 @@ SSD_STATIC_SCRATCH_BYTES = 16 << 20
 EXPORTED = ("ssd_conv1d_rows", "ssd_chunk_scan", "ssd_chunk_scan_workspace_size",
             "ssd_decode_step", "ssd_status_string", "ssd_read_device_error",
             "ssd_launch_counts", "ssd_chunk_scan_static_ws", "ssd_gated_group_rmsnorm",
-            "ssd_chunk_scan_varlen", "ssd_set_debug_checks", "ssd_set_wait_limit_ns")
+            "ssd_chunk_scan_varlen", "ssd_set_debug_checks", "ssd_set_wait_limit_ns",
+            "ssd_segment_decay", "ssd_state_combine")
 
 KERNEL_KINDS = ("conv_rows", "conv_state", "scan_simt", "scan_tc", "bc_conv", "decode_step",
-                "decode_conv", "gated_norm")
+                "decode_conv", "gated_norm", "segment_decay", "state_combine")
 
 
 class SsdError(RuntimeError):
@@ -96,6 +97,8 @@ def load_library():
             lib.ssd_status_string.restype = ctypes.c_char_p
             lib.ssd_read_device_error.argtypes = [_vp]
             lib.ssd_launch_counts.argtypes = [ctypes.POINTER(ctypes.c_uint64), ci]
+            lib.ssd_segment_decay.argtypes = [P, cu, _vp, _vp, _vp, _vp, _vp]
+            lib.ssd_state_combine.argtypes = [P, _vp, _vp, _vp, _vp, _vp]
             lib.ssd_set_debug_checks.argtypes = [cu]
             lib.ssd_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             for n in EXPORTED:
@@ -116,6 +119,20 @@ def ssd_set_wait_limit_ns(ns: int) -> int:
     """Bound on each wait inside the tensor-core scan kernel (0: the default
     2 s); returns the old bound."""
     return int(load_library().ssd_set_wait_limit_ns(int(ns)))
+
+
+def ssd_segment_decay(d: ssd_dims, flags: int, dt, dt_bias, A, gamma, stream=None) -> None:
+    f = torch.float32
+    _check(load_library().ssd_segment_decay(
+        ctypes.byref(d), flags, _ptr(dt, f, "dt"), _ptr(dt_bias, f, "dt_bias"), _ptr(A, f, "A"),
+        _ptr(gamma, f, "gamma"), _stream(stream)), "ssd_segment_decay")
+
+
+def ssd_state_combine(d: ssd_dims, gamma, h_prev, h_seg, h_out, stream=None) -> None:
+    f = torch.float32
+    _check(load_library().ssd_state_combine(
+        ctypes.byref(d), _ptr(gamma, f, "gamma"), _ptr(h_prev, f, "h_prev"),
+        _ptr(h_seg, f, "h_seg"), _ptr(h_out, f, "h_out"), _stream(stream)), "ssd_state_combine")
 
 
 def ssd_status_string(status: int) -> str:

@@ -407,4 +407,39 @@ ssd_status ssd_gated_group_rmsnorm(const ssd_dims* dims, ssd_dtype act, const vo
     return counted(launch_gated_norm(p, bf16, stream), SSD_KERNEL_GATED_NORM);
 }
 
+ssd_status ssd_segment_decay(const ssd_dims* dims, unsigned flags, const float* dt,
+                             const float* dt_bias, const float* A, float* gamma,
+                             cudaStream_t stream)
+{
+    if (dims == nullptr || dims->batch < 0 || dims->seqlen < 0 || dims->nheads <= 0)
+        return SSD_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)SSD_DT_SOFTPLUS) return SSD_ERR_INVALID_ARG;
+    if ((long long)dims->batch * dims->seqlen * dims->nheads > (1LL << 62)) return SSD_ERR_INVALID_ARG;
+    if (A == nullptr || gamma == nullptr || !aligned4(A) || !aligned4(gamma) ||
+        (dt_bias && !aligned4(dt_bias)))
+        return SSD_ERR_INVALID_ARG;
+    if (dims->batch > 0 && dims->seqlen > 0 && (dt == nullptr || !aligned4(dt)))
+        return SSD_ERR_INVALID_ARG;
+    if (dims->batch == 0) return SSD_OK;
+    SegmentParams p{dims->batch, dims->seqlen, dims->nheads, flags, dt, dt_bias, A, gamma};
+    return counted(launch_segment_decay(p, stream), SSD_KERNEL_SEGMENT_DECAY);
+}
+
+ssd_status ssd_state_combine(const ssd_dims* dims, const float* gamma, const float* h_prev,
+                             const float* h_seg, float* h_out, cudaStream_t stream)
+{
+    if (dims == nullptr || dims->batch < 0 || dims->nheads <= 0 || dims->headdim <= 0 ||
+        dims->dstate <= 0)
+        return SSD_ERR_INVALID_ARG;
+    const long long pn = (long long)dims->headdim * dims->dstate;
+    if (pn % 4 != 0 || (long long)dims->batch * dims->nheads > (1LL << 30) || pn > (1LL << 30))
+        return SSD_ERR_INVALID_ARG;
+    if (gamma == nullptr || h_seg == nullptr || h_out == nullptr || !aligned4(gamma) ||
+        !aligned16(h_seg) || !aligned16(h_out) || (h_prev && !aligned16(h_prev)))
+        return SSD_ERR_INVALID_ARG;
+    if (dims->batch == 0) return SSD_OK;
+    CombineParams p{dims->batch * dims->nheads, pn, gamma, h_prev, h_seg, h_out};
+    return counted(launch_state_combine(p, stream), SSD_KERNEL_STATE_COMBINE);
+}
+
 }  // extern "C"

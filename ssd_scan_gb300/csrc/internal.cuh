@@ -155,6 +155,26 @@ struct GatedNormParams {
     const float* w;   // [C]
     void* out;        // [rows, C] act, may alias y
 };
+// Sequence-parallel state passing (state_pass.cu).
+struct SegmentParams {
+    int B, S, H;
+    unsigned flags;
+    const float* dt;       // [B,S,H]
+    const float* dt_bias;  // [H] or null
+    const float* A;        // [H]
+    float* gamma;          // [B,H]: sum over the rows of dt * A
+};
+struct CombineParams {
+    int BH;                // sequences x heads
+    long long PN;          // state elements per head (a multiple of 4)
+    const float* gamma;    // [BH]
+    const float* h_prev;   // [BH, PN] or null (zeros)
+    const float* h_seg;    // [BH, PN]
+    float* h_out;          // [BH, PN]; may alias h_prev or h_seg
+};
+cudaError_t launch_segment_decay(const SegmentParams& p, cudaStream_t st);
+cudaError_t launch_state_combine(const CombineParams& p, cudaStream_t st);
+
 bool gated_norm_supports(int C, int G, bool bf16);
 cudaError_t launch_gated_norm(const GatedNormParams& p, bool bf16, cudaStream_t st);
 cudaError_t launch_decode_conv_roll(const DecodeParams& p, bool bf16, cudaStream_t st);
