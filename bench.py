@@ -375,7 +375,7 @@ def bench_ours(args):
     extra = e2e = dec = p2048 = None
     if args.only == "all":
         p2048, _ = bench_prefill_2048(ssd, dev, stream, world, rank, args)
-        if args.extra:
+        if not args.no_extra:
             extra = bench_extra(ssd, dev, stream, args)
         # ---- end to end through the C-ABI from pinned host buffers
         e2e = bench_e2e_long(ssd, dev, stream, rank, args)
@@ -589,17 +589,15 @@ def chained_calls(ssd, shape, prm, inp, splits, device):
 
 
 def bench_extra(ssd, dev, stream, args):
-    """The other prefill workloads, timed like the headline one: long (8
-    sequences x 8192 rows, then a chained second call of 8192 rows each) and
-    decay stress (4 x 4096 rows with decays up to ~1e4 per row, fed as calls of
-    U{1..128} rows), tokens/s over all calls of one pass; and the gated group
-    RMSNorm at the prefill width, GB/s against the HBM peak."""
+    """The other workloads, timed like the headline one: decay stress (4 x
+    4096 rows with decays up to ~1e4 per row, fed as calls of U{1..128} rows),
+    tokens/s over all calls of one pass; 16 packed sequences at pool slots
+    (one ssd_chunk_scan_varlen call); and the gated group RMSNorm at the
+    prefill width, GB/s against the HBM peak."""
     out = {}
     for name, shape, splits, stress in (
-            ("long_8x8192_plus_8192", si.LONG.with_(seqlen=2 * si.LONG.seqlen),
-             [si.LONG.seqlen, si.LONG.seqlen], False),
             ("stress_4x4096_calls_1_to_128", si.STRESS, si.random_splits(si.STRESS.seqlen, 5),
-             True)):
+             True),):
         prm = {k: v.to(dev) for k, v in si.params(shape, seed=11, stress=stress).items()}
         inp = si.prefill_inputs(shape, seed=12, device=dev, stress=stress)
         run, ncalls = chained_calls(ssd, shape, prm, inp, splits, dev)
@@ -739,12 +737,49 @@ def bench_decode(ssd, dev, stream, world, args):
     sb = decode_state_bytes(R, shape)
     gbs = sb / (ms / 1e3) / 1e9
     total = (sb + decode_other_bytes(R, shape)) / (ms / 1e3) / 1e9
+    # K tokens of every row in one call (multi-token decode): the state moves
+    # once per call, so tokens/s grows with K while the call stays HBM-bound
+    multi = {}
+    for K in (2, 4, 8):
+        g = torch.Generator(device=dev).manual_seed(100 + K)
+        mins = [{"xbc": torch.randn((R, K, shape.cdim), generator=g, device=dev).to(torch.bfloat16),
+                 "dt_raw": torch.randn((R, K, shape.nheads), generator=g, device=dev),
+                 "z": torch.randn((R, K, shape.nheads * shape.headdim), generator=g,
+                                  device=dev).to(torch.bfloat16)} for _ in range(2)]
+        yk = torch.empty((R, K, shape.nheads, shape.headdim), dtype=torch.bfloat16, device=dev)
+        dk = ssd.dims(R, K, shape.nheads, shape.headdim, shape.dstate, shape.ngroups,
+                      shape.conv_width)
+
+        def kstep(t, mins=mins, yk=yk, dk=dk):
+            inp = mins[t % 2]
+            ssd.ssd_decode_step(dk, ssd.SSD_BF16, flags, inp["xbc"], prm["conv_w"], prm["conv_b"],
+                                pools["conv_pool"], inp["dt_raw"], prm["dt_bias"], prm["A"],
+                                prm["D"], inp["z"], pools["slot_ids"], nslots, pools["ssm_pool"],
+                                yk, stream)
+        for t in range(3):
+            kstep(t)
+        torch.cuda.synchronize()
+        n = 16
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        queue_ahead(statistics.median(host_s[1:]), n)
+        e0.record(stream)
+        for t in range(n):
+            kstep(t)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        kms = ev_ms = e0.elapsed_time(e1) / n
+        multi[f"K{K}"] = {"ms_per_call": round(kms, 5), "tokens_per_s": round(R * K / (kms / 1e3), 1),
+                          "state_gbs": round(sb / (kms / 1e3) / 1e9, 1),
+                          "vs_K_single_steps": round(K * ms / ev_ms, 2)}
+        del mins, yk
     assert ssd.ssd_read_device_error(stream) == ssd.SSD_OK
     return {"metric": "decode-step state GB/s", "value": round(gbs * world, 1), "unit": "GB/s",
             "per_gpu_gbs": round(gbs, 1), "ms_per_step": round(ms, 5), "steps": steps,
             "rows": R, "slots": nslots, "state_bytes_per_step": sb,
             "all_bytes_gbs": round(total, 1), "peak": hbm, "peak_source": src,
-            "frac": round(gbs / hbm, 4), "traffic": ncu_traffic("decode")}
+            "frac": round(gbs / hbm, 4), "traffic": ncu_traffic("decode"),
+            "tokens_per_s": round(R / (ms / 1e3), 1),
+            "multi_token": multi}
 
 
 # ---------------------------------------------------------------------------
@@ -834,8 +869,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--extra", action="store_true",
-                    help="also time the long (8 x 8192 + 8192) and decay-stress prefill workloads")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the decay-stress, packed-sequence and gated-norm workloads")
     ap.add_argument("--only", choices=["all", "long", "prefill", "decode"], default="all",
                     help="time only the long-prefill steps, the 2048-row prefill calls or "
                          "the decode steps (profiler runs)")

@@ -5,8 +5,8 @@
  *   ssd_conv1d_rows  causal depthwise conv1d + SiLU over [conv state ; rows]
  *   ssd_chunk_scan   the chunked SSD scan over S prefill rows (optionally with
  *                    the conv fused in front), with carried conv/SSM state
- *   ssd_decode_step  one recurrent step for R rows at slot-indexed states,
- *                    updated in place
+ *   ssd_decode_step  K recurrent steps (tokens) for R rows at slot-indexed
+ *                    states, updated in place
  * and ssd_chunk_scan_varlen (the scan over packed sequences of different
  * lengths with slot-indexed states) and ssd_gated_group_rmsnorm (the group
  * RMSNorm + SiLU(z) gate that follows the scan in the mixer).
@@ -262,28 +262,34 @@ SSD_API ssd_status ssd_chunk_scan_varlen(const ssd_dims* dims, ssd_dtype act, un
                                  size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * ssd_decode_step -- one recurrent step for R rows at slot-indexed states.
+ * ssd_decode_step -- K recurrent steps (K = 1 .. 16 tokens of each request)
+ * for R rows at slot-indexed states, in place.
  * (TensorSharp nemotron.md 4.1 and section 11 "Batched / paged forward":
  *  per-slot conv + SSM state pool; vllm.cpp #1362: the update runs in place
  *  at the state slot, no gather/scatter copies.)
  *
- * dims->batch = R rows, dims->seqlen must be 1.  For row i, s = slot_ids[i]:
- *   if conv_w != NULL:  u = [conv_pool[s] ; xbc[i]],  x|B|C = silu(conv(u)),
+ * dims->batch = R rows, dims->seqlen = K tokens per row (1 <= K <= 16; more
+ * gives SSD_ERR_UNSUPPORTED).  For row i, s = slot_ids[i], tokens t = 0..K-1
+ * in order (each exactly one step of the recurrence):
+ *   if conv_w != NULL:  u = [conv_pool[s] ; xbc[i,t]],  x|B|C = silu(conv(u)),
  *                       conv_pool[s] = last W-1 rows of u        (in place)
- *   else                x|B|C = xbc[i]
+ *   else                x|B|C = xbc[i,t]
  *   ssm_pool[s,h] = exp(dt A[h]) ssm_pool[s,h] + dt x_h B_g^T     (in place)
- *   y[i,h,:] = ssm_pool[s,h] C_g + D[h] x_h   (times silu(z) with SSD_HAS_Z)
+ *   y[i,t,h,:] = ssm_pool[s,h] C_g + D[h] x_h   (times silu(z) with SSD_HAS_Z)
+ * The state is read once and written once per call however many tokens it
+ * carries: K tokens in one call cost about one step's memory traffic, and
+ * give the same values as K calls of one token.
  *
- * xbc        [R,Cdim] act (raw when conv_w != NULL)
+ * xbc        [R,K,Cdim] act (raw when conv_w != NULL)
  * conv_pool  [num_slots,W-1,Cdim] act; required iff conv_w != NULL
- * dt         [R,H] fp32;  dt_bias, A, D, z as in ssd_chunk_scan ([R,H*P] for z)
+ * dt         [R,K,H] fp32;  dt_bias, A, D as in ssd_chunk_scan; z [R,K,H*P]
  * slot_ids   [R] int32, DEVICE memory.  Ids must be distinct (checked only
  *            with SSD_CHECK_DISTINCT_SLOTS on; else duplicate ids race).
  *            An id outside [0, num_slots) sets the device error word to
  *            SSD_ERR_BAD_SLOT and that row writes nothing (neither pool nor
  *            y); other rows are unaffected.
  * ssm_pool   [num_slots,H,P,N] fp32, updated in place
- * y          [R,H,P] act
+ * y          [R,K,H,P] act
  */
 SSD_API ssd_status ssd_decode_step(const ssd_dims* dims, ssd_dtype act, unsigned flags,
                            const void* xbc, const float* conv_w, const float* conv_b,

@@ -276,7 +276,8 @@ ssd_status ssd_decode_step(const ssd_dims* dims, ssd_dtype act, unsigned flags, 
     long long cdim = 0;
     ssd_status s = check_dims(dims, act, &cdim);
     if (s != SSD_OK) return s;
-    if (dims->seqlen != 1) return SSD_ERR_INVALID_ARG;
+    if (dims->seqlen < 1) return SSD_ERR_INVALID_ARG;
+    if (dims->seqlen > kDecodeMaxTokens) return SSD_ERR_UNSUPPORTED;
     if (flags & ~(unsigned)(SSD_DT_SOFTPLUS | SSD_HAS_Z)) return SSD_ERR_INVALID_ARG;
     const bool rows = dims->batch > 0;
     const bool has_z = (flags & SSD_HAS_Z) != 0;
@@ -291,7 +292,7 @@ ssd_status ssd_decode_step(const ssd_dims* dims, ssd_dtype act, unsigned flags, 
     if (conv_w == nullptr && (conv_pool || conv_b)) return SSD_ERR_INVALID_ARG;
     if (conv_w && (!aligned4(conv_w) || conv_pool == nullptr || !aligned16(conv_pool)))
         return SSD_ERR_INVALID_ARG;
-    if (!decode_supports(dims->nheads, dims->headdim, dims->dstate, dims->ngroups))
+    if (!decode_supports(dims->nheads, dims->headdim, dims->dstate, dims->ngroups, dims->seqlen))
         return SSD_ERR_UNSUPPORTED;
     if (!rows) return SSD_OK;
 
@@ -303,6 +304,7 @@ ssd_status ssd_decode_step(const ssd_dims* dims, ssd_dtype act, unsigned flags, 
                    dims->conv_width, flags, xbc, conv_w, conv_b, conv_pool, dt, dt_bias, A, D,
                    has_z ? z : nullptr, slot_ids, num_slots, ssm_pool, y, err};
     p.check_dups = (g_debug_checks.load(std::memory_order_relaxed) & SSD_CHECK_DISTINCT_SLOTS) != 0;
+    p.K = dims->seqlen;
     s = counted(launch_decode_step(p, bf16, stream), SSD_KERNEL_DECODE_STEP);
     if (s != SSD_OK) return s;
     return counted(launch_decode_conv_roll(p, bf16, stream), SSD_KERNEL_DECODE_CONV,

@@ -52,6 +52,9 @@ struct ScanParams {
     unsigned* err;              // device error word
 };
 
+// Tokens one decode call may carry per row (consecutive steps of a request).
+constexpr int kDecodeMaxTokens = 16;
+
 struct DecodeParams {
     int R, H, P, N, G, W;
     unsigned flags;
@@ -70,6 +73,7 @@ struct DecodeParams {
     void* y;                // [R,H,P] act
     unsigned* err;
     int check_dups = 0;     // a row whose slot id appeared at an earlier row: report, skip
+    int K = 1;              // tokens per row: xbc [R,K,Cdim], dt [R,K,H], z, y [R,K,..]
 };
 
 // Has slot id `s` already appeared among ids[0 .. i-1]?  (debug check)
@@ -143,7 +147,7 @@ bool scan_tc_supports(int P, int N);
 // dependent launch) and waits for it before its first read of p.bc.
 cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st, bool after_prepass);
 
-bool decode_supports(int H, int P, int N, int G);
+bool decode_supports(int H, int P, int N, int G, int K);
 cudaError_t launch_decode_step(const DecodeParams& p, bool bf16, cudaStream_t st);
 
 struct GatedNormParams {

@@ -110,12 +110,13 @@ def test_bf16_rejects_other_chunk_sizes(lib):
 
 
 def test_decode_rejects_bad_arguments_on_host(lib):
-    d = _d(batch=4, seqlen=2)
     P = ctypes.c_void_p
-    st = lib.ssd_decode_step(ctypes.byref(d), 1, 1, P(0x10000), None, None, None, P(0x20000),
-                             None, P(0x30000), None, None, P(0x40000), 8, P(0x50000),
-                             P(0x60000), None)
-    assert st == ssd.SSD_ERR_INVALID_ARG  # seqlen must be 1
+    for K, want in ((0, ssd.SSD_ERR_INVALID_ARG), (17, ssd.SSD_ERR_UNSUPPORTED)):
+        d = _d(batch=4, seqlen=K)  # tokens per row: 1 .. 16
+        st = lib.ssd_decode_step(ctypes.byref(d), 1, 1, P(0x10000), None, None, None,
+                                 P(0x20000), None, P(0x30000), None, None, P(0x40000), 8,
+                                 P(0x50000), P(0x60000), None)
+        assert st == want, K
     d = _d(batch=4, seqlen=1)
     st = lib.ssd_decode_step(ctypes.byref(d), 1, 1, P(0x10000), None, None, None, P(0x20000),
                              None, P(0x30000), None, None, None, 8, P(0x50000), P(0x60000),

@@ -177,3 +177,84 @@ def test_decode_full_size_every_row():
         assert np.array_equal(f64(pools["conv_pool"][sl[rr]]), c_o)
     ey.check(TOL[torch.bfloat16], R * si.DECODE_STEPS * H * P)
     eh.check(TOL[torch.bfloat16], R * H * P * N)
+
+
+# ---------------------------------------------------------------------------
+# K tokens per row in one call (multi-token decode): the state read once,
+# stepped K times, written once
+
+def _multi_inputs(shape, K, seed, act):
+    g = torch.Generator().manual_seed(seed)
+    R, H, P, C = shape.batch, shape.nheads, shape.headdim, shape.cdim
+    return {"xbc": torch.randn((R, K, C), generator=g).to(act).cuda(),
+            "dt_raw": torch.randn((R, K, H), generator=g).cuda(),
+            "z": torch.randn((R, K, H * P), generator=g).to(act).cuda()}
+
+
+def _multi_step(shape, prm, inp, slots, pool, cpool, conv=True, K=None):
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    R = inp["xbc"].shape[0]
+    K = inp["xbc"].shape[1] if K is None else K
+    d = ssd.dims(R, K, H, P, N, G, shape.conv_width)
+    y = torch.full((R, K, H, P), float("nan"), dtype=inp["xbc"].dtype, device="cuda")
+    ssd.ssd_decode_step(d, ssd.act_of(inp["xbc"]), ssd.SSD_DT_SOFTPLUS | ssd.SSD_HAS_Z,
+                        inp["xbc"], prm["conv_w"] if conv else None,
+                        prm["conv_b"] if conv else None, cpool if conv else None, inp["dt_raw"],
+                        prm["dt_bias"], prm["A"], prm["D"], inp["z"], slots, pool.shape[0], pool, y)
+    return y
+
+
+@pytest.mark.parametrize("K", [2, 3, 4, 7, 16])
+@pytest.mark.parametrize("act,conv", [(torch.bfloat16, True), (torch.float32, True),
+                                      (torch.bfloat16, False)])
+def test_multi_token_decode_equals_single_steps_and_oracle(K, act, conv):
+    """One call with K tokens per row == K calls of one token, bit for bit
+    (the same arithmetic, the state kept in registers between the tokens
+    instead of in the pool), and == the oracle's K steps from the slots'
+    states, within the tolerance; slots no row names stay untouched."""
+    shape = si.Shape(batch=12, seqlen=1, nheads=8, headdim=64, dstate=128, ngroups=2)
+    prm, pools = _setup(shape, 40, act=act)
+    slots = pools["slot_ids"]
+    inp = _multi_inputs(shape, K, seed=K, act=act)
+    pool0, cpool0 = pools["ssm_pool"].clone(), pools["conv_pool"].clone()
+    pa, ca = pool0.clone(), cpool0.clone()
+    y = _multi_step(shape, prm, inp, slots, pa, ca, conv=conv)
+    pb, cb = pool0.clone(), cpool0.clone()
+    ys = []
+    for t in range(K):
+        one = {k: v[:, t:t + 1].contiguous() for k, v in inp.items()}
+        ys.append(_multi_step(shape, prm, one, slots, pb, cb, conv=conv))
+    assert torch.equal(y, torch.cat(ys, dim=1))
+    assert torch.equal(pa, pb) and torch.equal(ca, cb)
+    sl = slots.long()
+    H, P, N, G = shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    y_o, h_o, c_o = oracle.mixer_prefill(
+        f64(inp["xbc"]), f64(prm["conv_w"]) if conv else None, f64(inp["dt_raw"]),
+        f64(prm["A"]), H=H, P=P, N=N, G=G, conv_b=f64(prm["conv_b"]) if conv else None,
+        conv_state=f64(cpool0[sl]) if conv else None, dt_bias=f64(prm["dt_bias"]),
+        D=f64(prm["D"]), z=f64(inp["z"]), h0=f64(pool0[sl]))
+    R = shape.batch
+    assert_close(y, y_o, TOL[act], count=R * K * H * P, what="y")
+    assert_close(pa[sl], h_o, TOL[act], count=R * H * P * N, what="pool")
+    if conv:
+        assert np.array_equal(f64(ca[sl]), c_o)
+    untouched = [s for s in range(40) if s not in set(slots.tolist())]
+    assert torch.equal(pa[untouched], pool0[untouched])
+    assert torch.equal(ca[untouched], cpool0[untouched])
+
+
+def test_multi_token_decode_bad_slot_and_token_limit():
+    shape = si.Shape(batch=3, seqlen=1, nheads=4, headdim=64, dstate=128, ngroups=1)
+    prm, pools = _setup(shape, 8)
+    slots = torch.tensor([1, 9, 4], dtype=torch.int32, device="cuda")
+    pool0, cpool0 = pools["ssm_pool"].clone(), pools["conv_pool"].clone()
+    inp = _multi_inputs(shape, 5, seed=2, act=torch.bfloat16)
+    assert ssd.ssd_read_device_error() == ssd.SSD_OK
+    _multi_step(shape, prm, inp, slots, pools["ssm_pool"], pools["conv_pool"])
+    assert ssd.ssd_read_device_error() == ssd.SSD_ERR_BAD_SLOT
+    changed = [bool((pools["ssm_pool"][s] != pool0[s]).any()) for s in range(8)]
+    assert changed == [s in (1, 4) for s in range(8)]
+    inp17 = _multi_inputs(shape, 17, seed=3, act=torch.bfloat16)
+    with pytest.raises(ssd.SsdError) as e:
+        _multi_step(shape, prm, inp17, slots, pools["ssm_pool"], pools["conv_pool"])
+    assert e.value.status == ssd.SSD_ERR_UNSUPPORTED
