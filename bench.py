@@ -253,11 +253,11 @@ LONG_STEP = si.LONG.with_(seqlen=2 * si.LONG.seqlen)  # two chained calls of 819
 LONG_SPLITS = [si.LONG.seqlen, si.LONG.seqlen]
 
 
-def long_step_bytes() -> dict:
-    """Algorithmic bytes of one long step: two calls of 8 x 8192 rows, each
-    with its per-row bytes and its per-sequence state bytes."""
-    per_call = prefill_bytes(si.LONG)["per_launch"]
-    pb = prefill_bytes(si.LONG)
+def long_step_bytes(batch: int = si.LONG.batch) -> dict:
+    """Algorithmic bytes of one long step: two calls of batch x 8192 rows,
+    each with its per-row bytes and its per-sequence state bytes."""
+    pb = prefill_bytes(si.LONG.with_(batch=batch))
+    per_call = pb["per_launch"]
     return {"per_row": pb["per_row"], "per_seq_per_call": pb["per_seq"], "per_call": per_call,
             "per_step": len(LONG_SPLITS) * per_call}
 
@@ -266,7 +266,7 @@ def bench_long(ssd, dev, stream, world, rank, args):
     """The headline: K steps of the long workload (two chained calls each),
     queued behind a spin so that none waits on the host, timed with CUDA
     events on the launching stream; clocks sampled during the timed loop."""
-    shape = LONG_STEP
+    shape = LONG_STEP.with_(batch=args.long_batch)
     prm = {k: v.to(dev) for k, v in si.params(shape, seed=rank_seed(rank)).items()}
     inp = si.prefill_inputs(shape, seed=rank_seed(rank) + 1, device=dev)
     run, ncalls = chained_calls(ssd, shape, prm, inp, LONG_SPLITS, dev)
@@ -295,7 +295,7 @@ def bench_long(ssd, dev, stream, world, rank, args):
     launches1 = ssd.ssd_launch_counts()
     assert ssd.ssd_read_device_error(stream) == ssd.SSD_OK
     ms = _max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
-    nb = long_step_bytes()
+    nb = long_step_bytes(args.long_batch)
     hbm, hbm_src = measured_peaks()
     achieved = nb["per_step"] / (ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
@@ -394,7 +394,7 @@ def bench_ours(args):
                                    "per GPU in one call, then a second 8192-row call of each fed "
                                    "with the final conv/ssm states; chunk 128, H=128 P=64 N=128 "
                                    "G=8 W=4, conv+SiLU and z-gate fused",
-                       "batch_per_gpu": si.LONG.batch, "seq_len": shape.seqlen,
+                       "batch_per_gpu": args.long_batch, "seq_len": shape.seqlen,
                        "calls_per_step": len(LONG_SPLITS),
                        "parallelism": f"replicas x{world} (independent sequences)",
                        "l2": "inputs of one step 7.2 GB > 129 MB L2"},
@@ -874,6 +874,9 @@ def main():
     ap.add_argument("--only", choices=["all", "long", "prefill", "decode"], default="all",
                     help="time only the long-prefill steps, the 2048-row prefill calls or "
                          "the decode steps (profiler runs)")
+    ap.add_argument("--long-batch", type=int, default=si.LONG.batch,
+                    help="sequences of the long workload (8; fewer only to keep profiler "
+                         "captures small)")
     ap.add_argument("--decode-slots", type=int, default=si.DECODE_SLOTS,
                     help="slots in the decode pool (the 256 rows touch the same bytes "
                          "whatever the pool size; a smaller pool keeps profiler captures small)")
