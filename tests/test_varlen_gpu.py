@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import ssd_inputs as si
-from tests.helpers import TOL, assert_close, f64
+from tests.helpers import TOL, MaxRel, assert_close, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -103,33 +103,39 @@ def test_varlen_equal_lengths_reproduce_the_batched_call():
     assert torch.equal(sp, hb) and torch.equal(cp, cb)
 
 
-def test_varlen_full_width_sampled_heads():
+def test_varlen_full_width_every_element():
     """The Nemotron-H-8B heads (128 heads, 8 groups): a long, a medium, a short
-    and a one-row sequence; four heads checked."""
+    and a one-row sequence at permuted slots, fresh and continuing; every y
+    element and every touched slot against the oracle, one group of 16 heads
+    (with its own B|C columns) at a time."""
     lens = [2048, 600, 77, 1]
     slots = [2, 0, 3, 1]
     init = [1, 0, 1, 1]
     shape, prm, rows, spool, cpool, cu = _problem(lens, nslots=4, H=128, G=8, seed=6)
     y, sp, cp = _run_gpu(shape, prm, rows, spool, cpool, cu, slots, init)
-    heads = [0, 45, 64, 127]
-    # the oracle on those heads only: each head with its own group's B|C columns
     H, P, N, G = 128, 64, 128, 8
-    cols = np.concatenate([np.arange(h * P, (h + 1) * P) for h in heads] +
-                          [np.arange(H * P + (h // 16) * N, H * P + (h // 16 + 1) * N) for h in heads] +
-                          [np.arange(H * P + G * N + (h // 16) * N, H * P + G * N + (h // 16 + 1) * N)
-                           for h in heads])
-    zc = np.concatenate([np.arange(h * P, (h + 1) * P) for h in heads])
-    sub_rows = {"xbc": rows["xbc"][:, cols], "dt_raw": rows["dt_raw"][:, heads],
-                "z": rows["z"][:, zc]}
-    sub_prm = {"conv_w": prm["conv_w"][cols], "conv_b": prm["conv_b"][cols],
-               "dt_bias": prm["dt_bias"][heads], "A": prm["A"][heads], "D": prm["D"][heads]}
-    sub_shape = si.Shape(batch=1, seqlen=sum(lens), nheads=4, headdim=P, dstate=N, ngroups=4)
-    yo, spo, cpo = _run_oracle(sub_shape, sub_prm, sub_rows, spool[:, heads], cpool[:, :, cols],
-                               cu, slots, init)
-    assert_close(y[:, heads], yo, TOL[torch.bfloat16], count=sum(lens) * 4 * P, what="y")
-    for s in slots:
-        assert_close(sp[s, heads], spo[s], TOL[torch.bfloat16], count=4 * P * N, what=f"slot {s}")
-        assert np.array_equal(f64(cp[s])[:, cols], cpo[s])
+    hpg = H // G
+    ey, eh = MaxRel("y"), MaxRel("slots")
+    for g in range(G):
+        heads = list(range(g * hpg, (g + 1) * hpg))
+        cols = np.concatenate([np.arange(g * hpg * P, (g + 1) * hpg * P),
+                               np.arange(H * P + g * N, H * P + (g + 1) * N),
+                               np.arange(H * P + G * N + g * N, H * P + G * N + (g + 1) * N)])
+        zc = np.arange(g * hpg * P, (g + 1) * hpg * P)
+        sub_rows = {"xbc": rows["xbc"][:, cols], "dt_raw": rows["dt_raw"][:, heads],
+                    "z": rows["z"][:, zc]}
+        sub_prm = {"conv_w": prm["conv_w"][cols], "conv_b": prm["conv_b"][cols],
+                   "dt_bias": prm["dt_bias"][heads], "A": prm["A"][heads], "D": prm["D"][heads]}
+        sub_shape = si.Shape(batch=1, seqlen=sum(lens), nheads=hpg, headdim=P, dstate=N,
+                             ngroups=1)
+        yo, spo, cpo = _run_oracle(sub_shape, sub_prm, sub_rows, spool[:, heads],
+                                   cpool[:, :, cols], cu, slots, init)
+        ey.add(y[:, g * hpg:(g + 1) * hpg], yo)
+        for s in slots:
+            eh.add(sp[s, g * hpg:(g + 1) * hpg], spo[s])
+            assert np.array_equal(f64(cp[s])[:, cols], cpo[s])
+    ey.check(TOL[torch.bfloat16], sum(lens) * H * P)
+    eh.check(TOL[torch.bfloat16], len(slots) * H * P * N)
 
 
 def test_varlen_bad_slot_sets_error_and_writes_nothing_for_it():
