@@ -693,8 +693,67 @@ def bench_extra(ssd, dev, stream, args):
         "us_per_call": round(ms * 1e3, 2), "bytes_per_call": nbytes,
         "gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
         "frac_of_hbm": round(nbytes / (ms / 1e3) / 1e9 / hbm, 4)}
+    out["mixer_tail_2048"] = bench_mixer_tail(ssd, dev, stream, si.PREFILL, steps=30)
+    out["mixer_tail_8x8192"] = bench_mixer_tail(ssd, dev, stream, si.LONG, steps=6)
     assert ssd.ssd_read_device_error(stream) == ssd.SSD_OK
     return out
+
+
+def bench_mixer_tail(ssd, dev, stream, shape, steps):
+    """The scan with the gated group RMSNorm after it: one
+    ssd_chunk_scan_gated_norm call (the gate and the per-head sums of squares
+    in the scan's epilogue, a scale pass after it) against ssd_chunk_scan
+    without the gate followed by ssd_gated_group_rmsnorm in place, on the
+    same inputs rotating over resident sets larger than the L2."""
+    pb = prefill_bytes(shape)
+    nsets = max(3, -(-2 * L2_BYTES // pb["per_launch"]))
+    prm, sets, d, _ = make_prefill_sets(shape, nsets, 41, dev)
+    H, C, S = shape.nheads, shape.nheads * shape.headdim, shape.batch * shape.seqlen
+    w = torch.rand((C,), generator=torch.Generator(device=dev).manual_seed(42), device=dev) + 0.5
+    fl = ssd.SSD_DT_SOFTPLUS
+    wsn = [ssd.workspace_for(d, ssd.SSD_BF16, fl | ssd.SSD_GATED_NORM, True, dev) for _ in sets]
+
+    def fused(i):
+        inp, out, _ = sets[i % nsets]
+        ssd.ssd_chunk_scan_gated_norm(
+            d, ssd.SSD_BF16, fl, inp["xbc"], prm["conv_w"], prm["conv_b"], inp["conv_state"],
+            out["cs"], inp["dt_raw"], prm["dt_bias"], prm["A"], prm["D"], inp["z"], w, 1e-5,
+            inp["ssm_state"], out["y"], out["hS"], wsn[i % nsets], stream)
+
+    def unfused(i):
+        inp, out, ws = sets[i % nsets]
+        ssd.ssd_chunk_scan(d, ssd.SSD_BF16, fl, inp["xbc"], prm["conv_w"], prm["conv_b"],
+                           inp["conv_state"], out["cs"], inp["dt_raw"], prm["dt_bias"], prm["A"],
+                           prm["D"], None, inp["ssm_state"], out["y"], out["hS"], ws, stream)
+        ssd.ssd_gated_group_rmsnorm(d, ssd.SSD_BF16, out["y"], inp["z"], w, 1e-5, out["y"],
+                                    stream)
+
+    def timed(fn):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        queue_ahead(60e-6, steps)
+        ev0.record(stream)
+        for i in range(steps):
+            fn(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1) / steps
+
+    ms_f, ms_u = timed(fused), timed(unfused)
+    # the fused call moves the scan's bytes, y once more in and out (the scale
+    # pass) and the per-head sums of squares out and in
+    nbytes = pb["per_launch"] + 2 * S * C * 2 + 2 * S * H * 4
+    hbm, _ = measured_peaks()
+    del sets, wsn
+    return {"workload": f"B={shape.batch} x S={shape.seqlen} rows, one call per step",
+            "fused_us_per_call": round(ms_f * 1e3, 2),
+            "scan_then_norm_us_per_call": round(ms_u * 1e3, 2),
+            "speedup": round(ms_u / ms_f, 3),
+            "fused_tokens_per_s": round(S / (ms_f / 1e3), 1),
+            "fused_algorithmic_bytes": nbytes,
+            "fused_frac_of_hbm": round(nbytes / (ms_f / 1e3) / 1e9 / hbm, 4)}
 
 
 def bench_decode(ssd, dev, stream, world, args):

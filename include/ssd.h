@@ -46,8 +46,9 @@
  *     W-1 most recent raw (pre-conv) rows, oldest first, in the activation
  *     dtype.
  *   - The SSM state is always fp32, layout [.., H, P, N] (N fastest).
- *   - With SSD_HAS_Z, y is multiplied by silu(z) (the gate alone).  For the
- *     mixer's gated group RMSNorm, run the scan without SSD_HAS_Z and then
+ *   - With SSD_HAS_Z, y is multiplied by silu(z) (the gate alone).  The
+ *     mixer's gated group RMSNorm is ssd_chunk_scan_gated_norm (scan, gate
+ *     and norm in one call), or the scan without SSD_HAS_Z followed by
  *     ssd_gated_group_rmsnorm.
  */
 #ifndef SSD_GB300_SSD_H
@@ -83,7 +84,8 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype; /* activation dtype */
 
 enum {
     SSD_DT_SOFTPLUS = 1u,  /* dt = softplus(dt_raw + dt_bias)                    */
-    SSD_HAS_Z = 2u         /* multiply y by silu(z)                              */
+    SSD_HAS_Z = 2u,        /* multiply y by silu(z)                              */
+    SSD_GATED_NORM = 4u    /* workspace query of ssd_chunk_scan_gated_norm       */
 };
 
 /*
@@ -168,11 +170,51 @@ SSD_API ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned 
 
 /*
  * Scratch bytes ssd_chunk_scan needs for these dims, activation dtype and
- * whether the conv is fused (conv_fused != 0 <=> conv_w != NULL).  Writes the
- * size to *bytes.  Returns SSD_ERR_INVALID_ARG for invalid dims.
+ * whether the conv is fused (conv_fused != 0 <=> conv_w != NULL).  With
+ * SSD_GATED_NORM in flags: the scratch of ssd_chunk_scan_gated_norm instead.
+ * Writes the size to *bytes.  Returns SSD_ERR_INVALID_ARG for invalid dims.
  */
 SSD_API ssd_status ssd_chunk_scan_workspace_size(const ssd_dims* dims, ssd_dtype act, unsigned flags,
                                          int conv_fused, size_t* bytes);
+
+/*
+ * ssd_chunk_scan_gated_norm -- the mixer's tail in one call: the scan of
+ * ssd_chunk_scan, then the gated group RMSNorm of ssd_gated_group_rmsnorm
+ * over its output.
+ * (TensorSharp nemotron.md section 3, Mamba2 branch: out = SiLU(z) *
+ *  GroupRMSNorm(y, ssm_norm.weight); section 4.1: y is normalised per group
+ *  before the gate; section 6: one weight per channel of H*P.)
+ *
+ *   y_ssm  = ssd_chunk_scan's y without the gate
+ *   y[r,c] = silu(z[r,c]) * y_ssm[r,c] / sqrt(mean_{c' in group} y_ssm[r,c']^2
+ *            + eps) * norm_w[c]
+ * with G = dims->ngroups groups of H*P/G contiguous channels (the scan's
+ * groups; each a whole number of heads).
+ *
+ * Arguments as ssd_chunk_scan's, and
+ *   flags     SSD_DT_SOFTPLUS; SSD_HAS_Z and SSD_GATED_NORM are implied
+ *   z         [B,S,H*P] act, required (rows > 0)
+ *   norm_w    [H*P] fp32, 16-byte aligned, required
+ *   eps       finite, >= 0
+ *   workspace at least ssd_chunk_scan_workspace_size(dims, act,
+ *             flags | SSD_GATED_NORM, conv_fused) bytes
+ * On the tensor-core path the scan's epilogue applies the gate and leaves
+ * each row's sum of y_ssm^2 per head in the workspace (fp32, before y is
+ * rounded); a second kernel scales y in place by the weight and the group's
+ * inverse norm.  Elsewhere (fp32, calls of <= 4 rows, norm groups whose
+ * head count is not a multiple of 4) the scan runs without the gate and
+ * ssd_gated_group_rmsnorm follows it in place.  Group channel count as in
+ * ssd_gated_group_rmsnorm, else SSD_ERR_UNSUPPORTED; errors as
+ * ssd_chunk_scan's.
+ */
+SSD_API ssd_status ssd_chunk_scan_gated_norm(const ssd_dims* dims, ssd_dtype act, unsigned flags,
+                                     const void* xbc, const float* conv_w, const float* conv_b,
+                                     const void* conv_state_in, void* conv_state_out,
+                                     const float* dt, const float* dt_bias, const float* A,
+                                     const float* D, const void* z, const float* norm_w,
+                                     float eps, const float* ssm_state_in, void* y,
+                                     float* ssm_state_out, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * ssd_chunk_scan_static_ws -- ssd_chunk_scan for callers that cannot
@@ -382,7 +424,8 @@ enum {
     SSD_KERNEL_GATED_NORM = 7,     /* group RMSNorm + SiLU(z) gate          */
     SSD_KERNEL_SEGMENT_DECAY = 8,  /* a segment's total decay               */
     SSD_KERNEL_STATE_COMBINE = 9,  /* state after two consecutive segments  */
-    SSD_KERNEL_KINDS = 10
+    SSD_KERNEL_NORM_SCALE = 10,    /* fused gated norm: y times 1/rms       */
+    SSD_KERNEL_KINDS = 11
 };
 SSD_API int ssd_launch_counts(uint64_t* out, int n);
 

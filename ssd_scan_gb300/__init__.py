@@ -33,6 +33,7 @@ SSD_BF16 = 1
 
 SSD_DT_SOFTPLUS = 1
 SSD_HAS_Z = 2
+SSD_GATED_NORM = 4
 
 # size of the fixed per-GPU scratch array behind ssd_chunk_scan_static_ws
 SSD_STATIC_SCRATCH_BYTES = 16 << 20
@@ -42,10 +43,10 @@ EXPORTED = ("ssd_conv1d_rows", "ssd_chunk_scan", "ssd_chunk_scan_workspace_size"
             "ssd_decode_step", "ssd_status_string", "ssd_read_device_error",
             "ssd_launch_counts", "ssd_chunk_scan_static_ws", "ssd_gated_group_rmsnorm",
             "ssd_chunk_scan_varlen", "ssd_set_debug_checks", "ssd_set_wait_limit_ns",
-            "ssd_segment_decay", "ssd_state_combine")
+            "ssd_segment_decay", "ssd_state_combine", "ssd_chunk_scan_gated_norm")
 
 KERNEL_KINDS = ("conv_rows", "conv_state", "scan_simt", "scan_tc", "bc_conv", "decode_step",
-                "decode_conv", "gated_norm", "segment_decay", "state_combine")
+                "decode_conv", "gated_norm", "segment_decay", "state_combine", "norm_scale")
 
 
 class SsdError(RuntimeError):
@@ -87,6 +88,8 @@ def load_library():
             lib.ssd_conv1d_rows.argtypes = [P, ci, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
             lib.ssd_chunk_scan.argtypes = [P, ci, cu] + [_vp] * 14 + [sz, _vp]
             lib.ssd_chunk_scan_static_ws.argtypes = [P, ci, cu] + [_vp] * 13 + [_vp]
+            lib.ssd_chunk_scan_gated_norm.argtypes = [P, ci, cu] + [_vp] * 11 + \
+                [ctypes.c_float] + [_vp] * 4 + [sz, _vp]
             lib.ssd_chunk_scan_workspace_size.argtypes = [P, ci, cu, ci, ctypes.POINTER(sz)]
             lib.ssd_decode_step.argtypes = [P, ci, cu] + [_vp] * 10 + [ci, _vp, _vp, _vp]
             lib.ssd_gated_group_rmsnorm.argtypes = [P, ci, _vp, _vp, _vp, ctypes.c_float, _vp,
@@ -213,6 +216,26 @@ def ssd_chunk_scan(d: ssd_dims, act: int, flags: int, xbc, conv_w, conv_b, conv_
         ws_bytes, _stream(stream)), "ssd_chunk_scan")
 
 
+def ssd_chunk_scan_gated_norm(d: ssd_dims, act: int, flags: int, xbc, conv_w, conv_b,
+                              conv_state_in, conv_state_out, dt, dt_bias, A, D, z, norm_w,
+                              eps: float, ssm_state_in, y, ssm_state_out, workspace=None,
+                              stream=None) -> None:
+    """The scan, then silu(z) * GroupRMSNorm(y; norm_w, eps) over its output,
+    in one call (workspace: ssd_chunk_scan_workspace_size with SSD_GATED_NORM)."""
+    a = _ACT[act]
+    f = torch.float32
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().ssd_chunk_scan_gated_norm(
+        ctypes.byref(d), act, flags, _ptr(xbc, a, "xbc"), _ptr(conv_w, f, "conv_w"),
+        _ptr(conv_b, f, "conv_b"), _ptr(conv_state_in, a, "conv_state_in"),
+        _ptr(conv_state_out, a, "conv_state_out"), _ptr(dt, f, "dt"),
+        _ptr(dt_bias, f, "dt_bias"), _ptr(A, f, "A"), _ptr(D, f, "D"), _ptr(z, a, "z"),
+        _ptr(norm_w, f, "norm_w"), ctypes.c_float(eps), _ptr(ssm_state_in, f, "ssm_state_in"),
+        _ptr(y, a, "y"), _ptr(ssm_state_out, f, "ssm_state_out"),
+        _ptr(workspace, None, "workspace"), ws_bytes, _stream(stream)),
+        "ssd_chunk_scan_gated_norm")
+
+
 def ssd_chunk_scan_static_ws(d: ssd_dims, act: int, flags: int, xbc, conv_w, conv_b,
                              conv_state_in, conv_state_out, dt, dt_bias, A, D, z, ssm_state_in,
                              y, ssm_state_out, stream=None) -> None:
@@ -298,14 +321,20 @@ def workspace_for(d: ssd_dims, act: int, flags: int, conv_fused: bool, device) -
 
 def chunk_scan(xbc, dt, A, *, nheads, headdim, dstate, ngroups, conv_w=None, conv_b=None,
                conv_state=None, dt_bias=None, D=None, z=None, ssm_state=None,
-               dt_softplus=True, out=None, workspace=None, stream=None):
-    """Allocate outputs and call ssd_chunk_scan.  Returns (y, ssm_state_out,
+               dt_softplus=True, out=None, workspace=None, stream=None, norm_w=None,
+               norm_eps=1e-5):
+    """Allocate outputs and call ssd_chunk_scan (with ``norm_w``:
+    ssd_chunk_scan_gated_norm, z required).  Returns (y, ssm_state_out,
     conv_state_out or None)."""
     B, S, _ = xbc.shape
     W = conv_w.shape[1] if conv_w is not None else 4
     d = dims(B, S, nheads, headdim, dstate, ngroups, W, 128)
     act = act_of(xbc)
     flags = (SSD_DT_SOFTPLUS if dt_softplus else 0) | (SSD_HAS_Z if z is not None else 0)
+    if norm_w is not None:
+        if z is None:
+            raise ValueError("the gated norm needs z")
+        flags = (flags & SSD_DT_SOFTPLUS) | SSD_GATED_NORM
     if out is None:
         y = torch.empty((B, S, nheads, headdim), dtype=xbc.dtype, device=xbc.device)
         hs = torch.empty((B, nheads, headdim, dstate), dtype=torch.float32, device=xbc.device)
@@ -315,8 +344,13 @@ def chunk_scan(xbc, dt, A, *, nheads, headdim, dstate, ngroups, conv_w=None, con
         y, hs, cs = out
     if workspace is None:
         workspace = workspace_for(d, act, flags, conv_w is not None, xbc.device)
-    ssd_chunk_scan(d, act, flags, xbc, conv_w, conv_b, conv_state, cs, dt, dt_bias, A, D, z,
-                   ssm_state, y, hs, workspace, stream)
+    if norm_w is not None:
+        ssd_chunk_scan_gated_norm(d, act, flags, xbc, conv_w, conv_b, conv_state, cs, dt,
+                                  dt_bias, A, D, z, norm_w, norm_eps, ssm_state, y, hs,
+                                  workspace, stream)
+    else:
+        ssd_chunk_scan(d, act, flags, xbc, conv_w, conv_b, conv_state, cs, dt, dt_bias, A, D,
+                       z, ssm_state, y, hs, workspace, stream)
     return y, hs, cs
 
 

@@ -91,6 +91,14 @@ size_t tc_workspace_bytes(const ssd_dims* d)
     return (n + 255) & ~(size_t)255;
 }
 
+// Scratch of the fused gated norm on the tensor-core path: each row's sum of
+// y^2 per head, [B, H, S] fp32, after the B|C scratch.
+size_t norm_ss_bytes(const ssd_dims* d)
+{
+    const size_t n = (size_t)d->batch * d->nheads * d->seqlen * 4;
+    return (n + 255) & ~(size_t)255;
+}
+
 std::atomic<uint64_t> g_launches[SSD_KERNEL_KINDS];
 
 // Records one launch of `kind` when it succeeded (kernels that a launcher
@@ -183,24 +191,35 @@ ssd_status ssd_chunk_scan_workspace_size(const ssd_dims* dims, ssd_dtype act, un
     if (bytes == nullptr) return SSD_ERR_INVALID_ARG;
     ssd_status s = check_dims(dims, act, &cdim);
     if (s != SSD_OK) return s;
-    if (flags & ~(unsigned)(SSD_DT_SOFTPLUS | SSD_HAS_Z)) return SSD_ERR_INVALID_ARG;
-    *bytes = (conv_fused && use_tensor_cores(dims, act)) ? tc_workspace_bytes(dims) : 0;
+    if (flags & ~(unsigned)(SSD_DT_SOFTPLUS | SSD_HAS_Z | SSD_GATED_NORM)) return SSD_ERR_INVALID_ARG;
+    const bool tc = use_tensor_cores(dims, act);
+    *bytes = (conv_fused && tc) ? tc_workspace_bytes(dims) : 0;
+    if ((flags & SSD_GATED_NORM) && tc && norm_scale_supports(dims->nheads, dims->ngroups))
+        *bytes += norm_ss_bytes(dims);
     return SSD_OK;
 }
 
-ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned flags, const void* xbc,
-                          const float* conv_w, const float* conv_b, const void* conv_state_in,
-                          void* conv_state_out, const float* dt, const float* dt_bias,
-                          const float* A, const float* D, const void* z,
-                          const float* ssm_state_in, void* y, float* ssm_state_out,
-                          void* workspace, size_t workspace_bytes, cudaStream_t stream)
+}  // extern "C"
+
+namespace {
+
+// ssd_chunk_scan, and with norm_w != NULL ssd_chunk_scan_gated_norm (the
+// gate implied; flags then without SSD_HAS_Z and SSD_GATED_NORM).
+ssd_status chunk_scan_impl(const ssd_dims* dims, ssd_dtype act, unsigned flags, const void* xbc,
+                           const float* conv_w, const float* conv_b, const void* conv_state_in,
+                           void* conv_state_out, const float* dt, const float* dt_bias,
+                           const float* A, const float* D, const void* z,
+                           const float* ssm_state_in, void* y, float* ssm_state_out,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                           const float* norm_w, float eps)
 {
     long long cdim = 0;
     ssd_status s = check_dims(dims, act, &cdim);
     if (s != SSD_OK) return s;
     if (flags & ~(unsigned)(SSD_DT_SOFTPLUS | SSD_HAS_Z)) return SSD_ERR_INVALID_ARG;
+    const bool norm = norm_w != nullptr;
     const bool rows = dims->batch > 0 && dims->seqlen > 0;
-    const bool has_z = (flags & SSD_HAS_Z) != 0;
+    const bool has_z = norm || (flags & SSD_HAS_Z) != 0;
     if (rows && (xbc == nullptr || dt == nullptr || y == nullptr || !aligned16(xbc) ||
                  !aligned16(y) || !aligned4(dt)))
         return SSD_ERR_INVALID_ARG;
@@ -216,8 +235,14 @@ ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned flags, c
     if ((conv_state_in && !aligned16(conv_state_in)) ||
         (conv_state_out && !aligned16(conv_state_out)))
         return SSD_ERR_INVALID_ARG;
+    if (norm) {
+        if (!aligned16(norm_w) || !(eps >= 0.0f) || eps > 3.4e38f) return SSD_ERR_INVALID_ARG;
+        const long long C = (long long)dims->nheads * dims->headdim;
+        if (!gated_norm_supports((int)C, dims->ngroups, act == SSD_BF16)) return SSD_ERR_UNSUPPORTED;
+    }
     size_t need = 0;
-    s = ssd_chunk_scan_workspace_size(dims, act, flags, conv_w != nullptr, &need);
+    s = ssd_chunk_scan_workspace_size(dims, act, flags | (norm ? (unsigned)SSD_GATED_NORM : 0u),
+                                      conv_w != nullptr, &need);
     if (s != SSD_OK) return s;
     if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned16(workspace))))
         return SSD_ERR_INVALID_ARG;
@@ -226,6 +251,15 @@ ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned flags, c
     const bool tc = use_tensor_cores(dims, act);
     if (!tc && !scan_simt_supports(dims->headdim, dims->dstate)) return SSD_ERR_UNSUPPORTED;
     if (dims->batch == 0) return SSD_OK;
+    if (norm && !(tc && norm_scale_supports(dims->nheads, dims->ngroups))) {
+        // the row-exact kernels: the scan without the gate, then the norm in place
+        s = chunk_scan_impl(dims, act, flags & ~(unsigned)SSD_HAS_Z, xbc, conv_w, conv_b,
+                            conv_state_in, conv_state_out, dt, dt_bias, A, D, nullptr,
+                            ssm_state_in, y, ssm_state_out, workspace, workspace_bytes, stream,
+                            nullptr, 0.0f);
+        if (s != SSD_OK) return s;
+        return ssd_gated_group_rmsnorm(dims, act, y, z, norm_w, eps, y, stream);
+    }
 
     unsigned* err = nullptr;
     s = error_word_address(&err);
@@ -235,11 +269,16 @@ ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned flags, c
         const int H = dims->nheads, P = dims->headdim, N = dims->dstate, G = dims->ngroups;
         // the scan kernel also writes the new conv state (each CTA its head's x
         // columns, one CTA per group its B|C columns)
-        TcScanParams tp{dims->batch, dims->seqlen, H, G, dims->conv_width, flags,
+        TcScanParams tp{dims->batch, dims->seqlen, H, G, dims->conv_width,
+                        has_z ? flags | (unsigned)SSD_HAS_Z : flags,
                         conv_w != nullptr, xbc, xbc, (int)cdim, H * P, conv_w, conv_b,
                         conv_state_in, conv_w != nullptr ? conv_state_out : nullptr, dt, dt_bias,
                         A, D, has_z ? z : nullptr, ssm_state_in, y, ssm_state_out, err};
         tp.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+        if (norm) {
+            tp.norm_ss = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                  (conv_w != nullptr ? tc_workspace_bytes(dims) : 0));
+        }
         if (conv_w != nullptr) {
             // B|C columns: conv + SiLU once per group into the workspace
             ConvParams bp{dims->batch, dims->seqlen, (int)cdim, dims->conv_width, xbc, conv_w,
@@ -251,6 +290,10 @@ ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned flags, c
             tp.bc_col0 = 0;
         }
         s = counted(launch_scan_tc(tp, stream, conv_w != nullptr), SSD_KERNEL_SCAN_TC);
+        if (s == SSD_OK && norm) {
+            NormScaleParams np{dims->batch, dims->seqlen, H, P, G, eps, tp.norm_ss, norm_w, y};
+            s = counted(launch_norm_scale(np, stream), SSD_KERNEL_NORM_SCALE, dims->seqlen > 0);
+        }
     } else {
         ScanParams p{dims->batch, dims->seqlen, dims->nheads, dims->headdim, dims->dstate,
                      dims->ngroups, dims->conv_width, flags, xbc, conv_w, conv_b, conv_state_in,
@@ -265,6 +308,38 @@ ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned flags, c
                     dims->conv_width > 1);
     }
     return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+ssd_status ssd_chunk_scan(const ssd_dims* dims, ssd_dtype act, unsigned flags, const void* xbc,
+                          const float* conv_w, const float* conv_b, const void* conv_state_in,
+                          void* conv_state_out, const float* dt, const float* dt_bias,
+                          const float* A, const float* D, const void* z,
+                          const float* ssm_state_in, void* y, float* ssm_state_out,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    return chunk_scan_impl(dims, act, flags, xbc, conv_w, conv_b, conv_state_in, conv_state_out,
+                           dt, dt_bias, A, D, z, ssm_state_in, y, ssm_state_out, workspace,
+                           workspace_bytes, stream, nullptr, 0.0f);
+}
+
+ssd_status ssd_chunk_scan_gated_norm(const ssd_dims* dims, ssd_dtype act, unsigned flags,
+                                     const void* xbc, const float* conv_w, const float* conv_b,
+                                     const void* conv_state_in, void* conv_state_out,
+                                     const float* dt, const float* dt_bias, const float* A,
+                                     const float* D, const void* z, const float* norm_w,
+                                     float eps, const float* ssm_state_in, void* y,
+                                     float* ssm_state_out, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream)
+{
+    if (flags & ~(unsigned)(SSD_DT_SOFTPLUS | SSD_HAS_Z | SSD_GATED_NORM)) return SSD_ERR_INVALID_ARG;
+    if (norm_w == nullptr) return SSD_ERR_INVALID_ARG;
+    return chunk_scan_impl(dims, act, flags & (unsigned)SSD_DT_SOFTPLUS, xbc, conv_w, conv_b,
+                           conv_state_in, conv_state_out, dt, dt_bias, A, D, z, ssm_state_in, y,
+                           ssm_state_out, workspace, workspace_bytes, stream, norm_w, eps);
 }
 
 ssd_status ssd_decode_step(const ssd_dims* dims, ssd_dtype act, unsigned flags, const void* xbc,

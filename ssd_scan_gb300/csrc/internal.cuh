@@ -140,6 +140,10 @@ struct TcScanParams {
     int num_slots = 0;
     int check_dups = 0;             // packed sequences: report and skip a repeated slot id
     unsigned long long wait_ns = 0; // bound on each wait between the kernel's warps
+    // The gated group RMSNorm's epilogue share (fixed-length calls with z):
+    // besides y silu(z), each row's sum of y^2 over the head's channels (y
+    // before the gate) into norm_ss [B,H,S]; null: the plain gate.
+    float* norm_ss = nullptr;
 };
 bool scan_tc_supports(int P, int N);
 // after_prepass: the kernel just before it on `st` is the B|C conv writing p.bc;
@@ -178,6 +182,19 @@ struct CombineParams {
 };
 cudaError_t launch_segment_decay(const SegmentParams& p, cudaStream_t st);
 cudaError_t launch_state_combine(const CombineParams& p, cudaStream_t st);
+
+// y[r, c] *= w[c] / sqrt(sum_{h in group(c)} ss[b, h, s] / gs + eps), in
+// place: the second step of the gated group RMSNorm after a scan that applied
+// the gate and left the per-head sums of squares (bf16 y).
+struct NormScaleParams {
+    int B, S, H, P, G;
+    float eps;
+    const float* ss;  // [B,H,S]
+    const float* w;   // [H*P]
+    void* y;          // [B,S,H,P] bf16, scaled in place
+};
+bool norm_scale_supports(int H, int G);
+cudaError_t launch_norm_scale(const NormScaleParams& p, cudaStream_t st);
 
 bool gated_norm_supports(int C, int G, bool bf16);
 cudaError_t launch_gated_norm(const GatedNormParams& p, bool bf16, cudaStream_t st);

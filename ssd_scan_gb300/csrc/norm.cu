@@ -144,7 +144,115 @@ __global__ void __launch_bounds__(1024) gated_norm_block_kernel(GatedNormParams 
     NormVec<T>::store(static_cast<T*>(p.out) + off, o);
 }
 
+// The scale step of the gated group RMSNorm fused into the scan: the scan
+// wrote y' = y silu(z) (bf16) and each row's sum of y^2 per head into ss.
+// A group of the norm is H/G whole heads, so its mean square is the sum of
+// those heads' partial sums over gs channels, and out = y' w / sqrt(ms + eps).
+// kScaleRows rows per CTA; a thread owns the same 16-byte column vectors in
+// each of them.  A warp's 32 vectors of one pass lie in one group, so each
+// warp sums that group's partials itself (lane = head x row, shuffles) and
+// needs no barrier.  Every load (y', the weights, the partial sums) is issued
+// before the first wait, so their latencies overlap.
+constexpr int kScaleRows = 2;
+constexpr int kScaleThreads = 256;
+constexpr int kScaleU = 1;  // column vectors per thread and row in one pass
+constexpr int kScaleSs = kScaleRows > 1 ? kScaleRows / 2 : 1;  // partial-sum rows per lane
+
+__global__ void __launch_bounds__(kScaleThreads) norm_scale_kernel(NormScaleParams p)
+{
+    const int tid = threadIdx.x, lane = tid & 31;
+    const long long rows = (long long)p.B * p.S;
+    const long long r0 = (long long)blockIdx.x * kScaleRows;
+    const int nrows = (int)min((long long)kScaleRows, rows - r0);
+    const int hg = p.H / p.G;
+    const int vpr = p.H * p.P / 8;  // 16-byte vectors per row
+    const int vpg = hg * p.P / 8;   // per group (a multiple of 32)
+    const float inv_gs = 1.0f / (float)(hg * p.P);
+    uint4* y = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + (size_t)r0 * p.H * p.P);
+    const float4* w4 = reinterpret_cast<const float4*>(p.w);
+    // this lane's share of the partial sums: head k0 (+16, +32, ..) of rows
+    // 2i + (lane >> 4); the two half-warps' sums meet in lanes 0 and 16
+    const int k0 = lane & 15;
+    const float* ssrow[kScaleSs];
+#pragma unroll
+    for (int i = 0; i < kScaleSs; ++i) {
+        const int rl = 2 * i + (lane >> 4);
+        const long long rr = r0 + rl;
+        ssrow[i] = rl < nrows ? p.ss + (size_t)(rr / p.S) * p.H * p.S + rr % p.S : nullptr;
+    }
+
+    for (int cb = 0; cb < vpr; cb += kScaleU * kScaleThreads) {
+        uint4 buf[kScaleRows][kScaleU];
+        float4 wa[kScaleU], wb[kScaleU];
+        float ssv[kScaleU][kScaleSs];
+#pragma unroll
+        for (int u = 0; u < kScaleU; ++u) {
+            const int cv = cb + tid + u * kScaleThreads;
+            if (cv < vpr) {
+#pragma unroll
+                for (int rl = 0; rl < kScaleRows; ++rl)
+                    if (rl < nrows) buf[rl][u] = y[(size_t)rl * vpr + cv];
+                wa[u] = __ldg(w4 + 2 * cv);
+                wb[u] = __ldg(w4 + 2 * cv + 1);
+            }
+            const int cw = cb + (tid & ~31) + u * kScaleThreads;  // the warp's first vector
+#pragma unroll
+            for (int i = 0; i < kScaleSs; ++i) {
+                float acc = 0.0f;
+                if (cw < vpr && ssrow[i] != nullptr) {
+                    const float* ss = ssrow[i] + (size_t)(cw / vpg) * hg * p.S;
+                    for (int k = k0; k < hg; k += 16) acc += ss[(size_t)k * p.S];
+                }
+                ssv[u][i] = acc;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kScaleU; ++u)
+#pragma unroll
+            for (int i = 0; i < kScaleSs; ++i)
+#pragma unroll
+                for (int d = 1; d < 16; d <<= 1) ssv[u][i] += __shfl_xor_sync(0xffffffffu, ssv[u][i], d);
+#pragma unroll
+        for (int u = 0; u < kScaleU; ++u) {
+            const int cv = cb + tid + u * kScaleThreads;
+#pragma unroll
+            for (int rl = 0; rl < kScaleRows; ++rl) {
+                const float f = rsqrtf(__shfl_sync(0xffffffffu, ssv[u][rl >> 1], 16 * (rl & 1)) * inv_gs + p.eps);
+                if (cv >= vpr || rl >= nrows) continue;
+                const float2 ff = make_float2(f, f);
+                const float2 wf[4] = {__fmul2_rn(make_float2(wa[u].x, wa[u].y), ff),
+                                      __fmul2_rn(make_float2(wa[u].z, wa[u].w), ff),
+                                      __fmul2_rn(make_float2(wb[u].x, wb[u].y), ff),
+                                      __fmul2_rn(make_float2(wb[u].z, wb[u].w), ff)};
+                __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&buf[rl][u]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    hv[k] = __float22bfloat162_rn(__fmul2_rn(__bfloat1622float2(hv[k]), wf[k]));
+                y[(size_t)rl * vpr + cv] = buf[rl][u];
+            }
+        }
+    }
+}
+
 }  // namespace
+
+bool norm_scale_supports(int H, int G)
+{
+    // a warp's 32 vectors in one group: a group of a multiple of 256 channels
+    // (P = 64: a multiple of 4 heads)
+    return G > 0 && H % G == 0 && (H / G) * 64 % 256 == 0;
+}
+
+cudaError_t launch_norm_scale(const NormScaleParams& p, cudaStream_t st)
+{
+    const long long rows = (long long)p.B * p.S;
+    if (rows == 0) return cudaSuccess;
+    const long long blocks = (rows + kScaleRows - 1) / kScaleRows;
+    if (blocks > 0x7fffffffLL || p.P != 64 || !norm_scale_supports(p.H, p.G))
+        return cudaErrorInvalidValue;
+    norm_scale_kernel<<<(unsigned)blocks, kScaleThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
 
 bool gated_norm_supports(int C, int G, bool bf16)
 {

@@ -142,6 +142,8 @@ struct __align__(1024) TcSmem {
     uint64_t cvready[kCv], epidone[kCv];                 // gamma warp <-> compute
     uint32_t tmem_base;
     int abort;
+    // gated group RMSNorm share of the epilogue (the kNorm instantiation)
+    float nsum[2][4][Q];  // by chunk parity, column group j, row: sum of y^2 over 16 channels
 };
 
 constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;
@@ -279,7 +281,7 @@ __device__ __forceinline__ bool wait_or_abort(TcSmem& s, uint64_t* bar, uint32_t
     }
 }
 
-template <bool kVarlen>
+template <bool kVarlen, bool kNorm>
 __global__ void __launch_bounds__(kThreads, 1)
     scan_tc_kernel(const __grid_constant__ CUtensorMap map_bc, const __grid_constant__ CUtensorMap map_z,
                    const __grid_constant__ CUtensorMap map_y, const TcScanParams p)
@@ -859,6 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const float dec = ex2_fast(fminf(cv.g2h[t] + cv.g2l[t], 0.0f));  // exp(min(gamma_t, 0))
                 const float2 dd = make_float2(dec, dec);
+                float2 ss2 = make_float2(0.0f, 0.0f);  // (kNorm) sum of y^2 over this thread's columns
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {  // 8 columns at a time
                     float yv[8];
@@ -889,6 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         float2 v = make_float2(yv[2 * e], yv[2 * e + 1]);
+                        if constexpr (kNorm) ss2 = __ffma2_rn(v, v, ss2);  // the norm's sum of y^2
                         if (has_z) v = __fmul2_rn(v, silu2(zv[e]));
                         out[e] = v;
                     }
@@ -903,6 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         at<uint4>(s.Yt, off) = pack4x2(out);
                     }
                 }
+                if constexpr (kNorm) s.nsum[c & 1][j][t] = ss2.x + ss2.y;
             } else {
                 ok = false;
             }
@@ -910,6 +915,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&s.epidone[c % kCv]);
             named_bar_sync(1 + q, 128);  // the quarter's four warps
+            if constexpr (kNorm) {
+                // the row's sum over the head's 64 channels, in a fixed order.  The
+                // quarter's other warps write this parity's slots again at chunk
+                // c + 2, after the quarter's barrier of chunk c + 1, which this
+                // warp reaches only after these reads.
+                if (j == 0 && ok && t < rows) {
+                    const float ns = (s.nsum[c & 1][0][t] + s.nsum[c & 1][1][t]) +
+                                     (s.nsum[c & 1][2][t] + s.nsum[c & 1][3][t]);
+                    p.norm_ss[((size_t)b * H + h) * S + (size_t)c * Q + t] = ns;
+                }
+            }
             // a quarter with rows left (packed sequences: a whole quarter of them)
             if (j == 0 && lane == 0 && ok && (kVarlen ? c * Q + 32 * q + 32 <= S : c * Q + 32 * q < S)) {
                 tma_store_3d(&map_y, reinterpret_cast<const char*>(s.Yt) + q * 32 * 128, h * P,
@@ -1013,7 +1029,9 @@ cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st, bool after_pr
     if ((p.flags & kHasZ) && !make_map(&mz, p.S > 0 ? p.z : stand_in, p.H * P, mS, mB))
         return cudaErrorInvalidValue;
     if (!make_map(&my, p.S > 0 ? p.y : stand_in, p.H * P, mS, mB, 32)) return cudaErrorInvalidValue;
-    auto kernel = varlen ? scan_tc_kernel<true> : scan_tc_kernel<false>;
+    if (p.norm_ss != nullptr && (varlen || !(p.flags & kHasZ))) return cudaErrorInvalidValue;
+    auto kernel = varlen ? scan_tc_kernel<true, false>
+                         : (p.norm_ss ? scan_tc_kernel<false, true> : scan_tc_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
