@@ -368,6 +368,9 @@ def bench_ours(args):
     if args.only == "decode":
         dec = bench_decode(ssd, dev, stream, world, args)
         return {"metric": "decode-step state GB/s", "decode": dec} if rank == 0 else None
+    if args.only == "tail":  # profiling runs: the scan + gated norm calls alone
+        tail = {"mixer_tail_2048": bench_mixer_tail(ssd, dev, stream, si.PREFILL, steps=args.steps)}
+        return {"metric": "mixer_tail", **tail} if rank == 0 else None
     if args.only == "prefill":  # profiling runs: the 2048-row calls alone
         p2048, _ = bench_prefill_2048(ssd, dev, stream, world, rank, args)
         return {"metric": "prefill_2048", "prefill_2048": p2048} if rank == 0 else None
@@ -930,9 +933,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the decay-stress, packed-sequence and gated-norm workloads")
-    ap.add_argument("--only", choices=["all", "long", "prefill", "decode"], default="all",
-                    help="time only the long-prefill steps, the 2048-row prefill calls or "
-                         "the decode steps (profiler runs)")
+    ap.add_argument("--only", choices=["all", "long", "prefill", "decode", "tail"], default="all",
+                    help="time only the long-prefill steps, the 2048-row prefill calls, "
+                         "the decode steps or the scan + gated norm calls (profiler runs)")
     ap.add_argument("--long-batch", type=int, default=si.LONG.batch,
                     help="sequences of the long workload (8; fewer only to keep profiler "
                          "captures small)")
