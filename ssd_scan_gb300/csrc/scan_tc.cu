@@ -48,16 +48,18 @@
 //  - control warp (one thread): every TMA load (the C tile of the next chunk
 //    into the one C buffer once G4 of this chunk -- and so G1, G3, issued
 //    before it -- is done; B tiles two chunks ahead, double-buffered; the z
-//    tile of a chunk once the epilogue before it is done) and every MMA, each
-//    as soon as its operands are ready (mbarriers from the compute warps).
+//    tile of the next chunk, double-buffered, once the mask of this chunk is
+//    done) and every MMA, each as soon as its operands are ready (mbarriers
+//    from the compute warps).
 //  - compute warps, phase by phase on every chunk: mask (one 32x32 block of a
 //    TMEM lane quarter per warp, warp % 4 = quarter), state update (16 state
 //    columns per warp, h in fp32 registers, its bf16 copy into shared memory
 //    for G3), conv of the next chunk (4 rows x 4 channels per thread: causal
 //    taps over raw rows prefetched a chunk ahead in registers, SiLU, the x and
 //    scaled-x tiles), epilogue (16 columns of a lane quarter per warp: z from
-//    its TMA tile, y through a staging tile that each quarter stores with one
-//    TMA store).  At the end they write the final state and the new conv state.
+//    its TMA tile, y written over it in place, each quarter's rows leaving
+//    with one TMA store).  At the end they write the final state and the new
+//    conv state.
 // Per-thread global accesses that would scatter a warp over 32 rows (z, y)
 // go through TMA tiles instead: the load/store unit would otherwise spend 32
 // requests on every such instruction.  Every wait is bounded in time; a wait
@@ -128,15 +130,14 @@ struct __align__(1024) TcSmem {
     __nv_bfloat16 XS[2][Q * 64];    // scaled x rows [s][p] (SW128): v o x or w o x, by parity
     __nv_bfloat16 XR[2][Q * 64];    // x rows [s][p] (exact chunks), by parity
     __nv_bfloat16 Hs[N * 64];       // bf16 state rows [n][p] of the previous chunk: G3's B
-    __nv_bfloat16 Zt[Q * 64];       // z rows [t][p] of the epilogue's chunk (TMA, SW128)
-    __nv_bfloat16 Yt[Q * 64];       // y rows [t][p] on their way out (TMA store by 32-row
-                                    // quarters, SW128)
+    __nv_bfloat16 Zt[2][Q * 64];    // z rows [t][p] by chunk parity (TMA, SW128); y written
+                                    // over them in place, stored by 32-row quarters
     ChunkVals cv[kCv];              // ring of per-chunk values
     // taps by [tap][channel pair] (front-padded with zeros): a thread reads its two
     // pairs of a tap as one 16-byte vector, a half-warp a contiguous 256 bytes
     alignas(16) float2 wconv[kMaxW][P / 2];
     alignas(16) float2 bconv[P / 2];
-    uint64_t full_c, full_b[2], full_z;  // TMA landed
+    uint64_t full_c, full_b[2], full_z[2];  // TMA landed
     uint64_t g1, g3, g4, g2, fin;   // MMA commits
     uint64_t xready, mready, hsready;                    // compute -> control
     uint64_t cvready[kCv], epidone[kCv];                 // gamma warp <-> compute
@@ -159,7 +160,7 @@ static_assert(sizeof(ChunkVals) % 16 == 0 && offsetof(TcSmem, cv) % 16 == 0, "fl
 static_assert(offsetof(ChunkVals, g2l) % 16 == 0 && offsetof(ChunkVals, dts) % 16 == 0, "float4");
 static_assert(offsetof(ChunkVals, sc) % 16 == 0 && offsetof(ChunkVals, vb) % 16 == 0, "float4");
 static_assert(offsetof(TcSmem, wconv) % 16 == 0 && offsetof(TcSmem, bconv) % 16 == 0, "float4");
-static_assert(offsetof(TcSmem, Zt) % 1024 == 0 && offsetof(TcSmem, Yt) % 1024 == 0, "tile");
+static_assert(offsetof(TcSmem, Zt) % 1024 == 0, "tile");
 static_assert(offsetof(TcSmem, full_c) % 8 == 0, "mbarriers");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
@@ -330,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         mbar_init(&s.full_c, 1);
-        mbar_init(&s.full_z, 1);
+        mbar_init(&s.full_z[0], 1);
+        mbar_init(&s.full_z[1], 1);
         for (int i = 0; i < 2; ++i) mbar_init(&s.full_b[i], 1);
         mbar_init(&s.g1, 1);
         mbar_init(&s.g3, 1);
@@ -433,15 +435,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&s.g3);
                 return true;
             };
-            // z tile of chunk c (one buffer: the epilogue of chunk c-1 is done with it)
+            // z tile of chunk c into buffer c & 1
             auto load_z = [&](int c) {
-                mbar_arrive_expect_tx(&s.full_z, Q * 64 * 2);
-                tma_load_3d(s.Zt, &map_z, &s.full_z, h * P, trow(c), tz);
+                mbar_arrive_expect_tx(&s.full_z[c & 1], Q * 64 * 2);
+                tma_load_3d(s.Zt[c & 1], &map_z, &s.full_z[c & 1], h * P, trow(c), tz);
                 loaded_z = c + 1;
             };
             if (has_z) {
                 prefetch_tmap(&map_z);
                 load_z(0);
+                if (nchunks > 1) load_z(1);
             }
             load_c(0);
             load_b(0);
@@ -475,14 +478,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // z of chunk c once the epilogue of chunk c-1 is done (it comes before
                 // the mask of chunk c, so this does not hold up G2(c))
-                if (has_z && c > 0) {
-                    ok = wait_or_abort(s, &s.epidone[(c - 1) % kCv], ((c - 1) / kCv) & 1, wlim);
-                    if (!ok) break;
-                    load_z(c);
-                }
                 // G2(c): M(c) in TMEM (CB(c) consumed); onto G3(c) (factored) or fresh
                 ok = wait_or_abort(s, &s.mready, c & 1, wlim);
                 if (!ok) break;
+                // z of chunk c+1 into the buffer of chunk c-1: its epilogue read the z
+                // rows and its y store read the tile before these arrivals
+                if (has_z && c >= 1 && c + 1 < nchunks) load_z(c + 1);
                 tc_fence_after();
                 {
                     const bool fac = s.cv[c % kCv].factored != 0;
@@ -516,10 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = max(0, loaded_b - 2); k < loaded_b; ++k)
                 while (!mbar_test(&s.full_b[k & 1], (k >> 1) & 1) && globaltimer_ns() - t0 < kWaitNs)
                     __nanosleep(64);
-            if (loaded_z > 0) {  // z tiles are requested in order, each after the last was used
-                const int k = loaded_z - 1;
-                while (!mbar_test(&s.full_z, k & 1) && globaltimer_ns() - t0 < kWaitNs) __nanosleep(64);
-            }
+            for (int k = max(0, loaded_z - 2); k < loaded_z; ++k)  // the last load into each buffer
+                while (!mbar_test(&s.full_z[k & 1], (k >> 1) & 1) && globaltimer_ns() - t0 < kWaitNs)
+                    __nanosleep(64);
         }
     } else if (warp == kGammaWarp) {
         // ===================== gamma: per-chunk row values (one warp) =====================
@@ -817,6 +817,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 ok = false;
             }
+            // the last y store of this quarter has read its tile before this
+            // arrival: the control thread loads z of chunk c+1 into that buffer
+            // only after it
+            if (j == 0 && lane == 0 && c > 0) bulk_wait_read_all();
             tc_fence_before();
             mbar_arrive(&s.mready);
 
@@ -851,12 +855,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             // ---- epilogue(c): factored y = u Y; exact y = Y + u Yo; times silu(z).
-            // z comes from its TMA tile; y goes to the staging tile, and each quarter's
-            // 32 rows leave with one TMA store (rows past the end are not written).
-            // The staging tile's last store finished reading it before its issuer's
-            // mask(c) arrival, which G2(c), waited on below, comes after. ----
+            // z comes from its TMA tile and y is written over it in place; each
+            // quarter's 32 rows leave with one TMA store (rows past the end are not
+            // written).  The store of chunk c-2 from this buffer finished reading it
+            // before its issuer's mask(c-1) arrival. ----
             if (ok) ok = wait_or_abort(s, &s.g2, c & 1, wlim);
-            if (ok && has_z) ok = wait_or_abort(s, &s.full_z, c & 1, wlim);
+            if (ok && has_z) ok = wait_or_abort(s, &s.full_z[kb], (c >> 1) & 1, wlim);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
                 const float dec = ex2_fast(fminf(cv.g2h[t] + cv.g2l[t], 0.0f));  // exp(min(gamma_t, 0))
@@ -888,7 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     float2 out[4], zv[4];
                     const uint32_t off = chunk_off(t, 2 * j + hh);  // row t, 8 columns (SW128)
-                    if (has_z) unpack4x2(at<uint4>(s.Zt, off), zv);
+                    if (has_z) unpack4x2(at<uint4>(s.Zt[kb], off), zv);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         float2 v = make_float2(yv[2 * e], yv[2 * e + 1]);
@@ -904,14 +908,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                       ((size_t)(row0 + c * Q + t) * H + h) * P +
                                                       16 * j + 8 * hh) = pack4x2(out);
                     } else {
-                        at<uint4>(s.Yt, off) = pack4x2(out);
+                        at<uint4>(s.Zt[kb], off) = pack4x2(out);
                     }
                 }
                 if constexpr (kNorm) s.nsum[c & 1][j][t] = ss2.x + ss2.y;
             } else {
                 ok = false;
             }
-            fence_proxy_async_smem();   // the staging tile is read by the TMA store
+            fence_proxy_async_smem();   // the tile is read by the TMA store
             tc_fence_before();
             mbar_arrive(&s.epidone[c % kCv]);
             named_bar_sync(1 + q, 128);  // the quarter's four warps
@@ -928,10 +932,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // a quarter with rows left (packed sequences: a whole quarter of them)
             if (j == 0 && lane == 0 && ok && (kVarlen ? c * Q + 32 * q + 32 <= S : c * Q + 32 * q < S)) {
-                tma_store_3d(&map_y, reinterpret_cast<const char*>(s.Yt) + q * 32 * 128, h * P,
+                tma_store_3d(&map_y, reinterpret_cast<const char*>(s.Zt[kb]) + q * 32 * 128, h * P,
                              trow(c) + 32 * q, tz);
                 bulk_commit();
-                bulk_wait_read_all();
             }
         }
         if (j == 0 && lane == 0) bulk_wait_all();  // y of the last chunks written
