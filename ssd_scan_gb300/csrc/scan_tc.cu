@@ -45,24 +45,27 @@
 //  - gamma warp: for up to four chunks ahead, dt (softplus + bias), the
 //    double-float cumulative sum of a = dt A, the form of the chunk and the
 //    per-row factors, into a ring of per-chunk value sets in shared memory.
-//  - control warp (one thread): every TMA load (the C tile of the next chunk
-//    into the one C buffer once G4 of this chunk -- and so G1, G3, issued
-//    before it -- is done; B tiles two chunks ahead, double-buffered; the z
-//    tile of the next chunk, double-buffered, once the mask of this chunk is
-//    done) and every MMA, each as soon as its operands are ready (mbarriers
-//    from the compute warps).
+//  - control warp (one thread): every TMA load (the C and B tiles of the next
+//    chunk into the one C and B buffers once G4 of this chunk -- and so G1,
+//    G3, issued before it -- is done; the raw x rows of the chunk after next,
+//    with the 4 rows before them, double-buffered, once the conv of this chunk
+//    is done; the z tile of the next chunk, double-buffered, once the mask of
+//    this chunk is done) and every MMA, each as soon as its operands are ready
+//    (mbarriers from the compute warps).
 //  - compute warps, phase by phase on every chunk: mask (one 32x32 block of a
 //    TMEM lane quarter per warp, warp % 4 = quarter), state update (16 state
 //    columns per warp, h in fp32 registers, its bf16 copy into shared memory
 //    for G3), conv of the next chunk (4 rows x 4 channels per thread: causal
-//    taps over raw rows prefetched a chunk ahead in registers, SiLU, the x and
-//    scaled-x tiles), epilogue (16 columns of a lane quarter per warp: z from
+//    taps over the raw rows of its TMA tiles, SiLU, the x and scaled-x
+//    tiles), epilogue (16 columns of a lane quarter per warp: z from
 //    its TMA tile, y written over it in place, each quarter's rows leaving
 //    with one TMA store).  At the end they write the final state and the new
 //    conv state.
 // Per-thread global accesses that would scatter a warp over 32 rows (z, y)
 // go through TMA tiles instead: the load/store unit would otherwise spend 32
-// requests on every such instruction.  Every wait is bounded in time; a wait
+// requests on every such instruction.  The raw x rows come by TMA too: per-
+// thread loads of them a chunk ahead cost the compute warps ~0.5 us per chunk
+// in issue and held 14 registers through every phase.  Every wait is bounded in time; a wait
 // that runs out aborts the CTA (the other waits then fail fast) and sets the
 // device error word.
 #include "internal.cuh"
@@ -126,18 +129,20 @@ struct __align__(16) ChunkVals {  // per-chunk row values, written by the gamma 
 
 struct __align__(1024) TcSmem {
     __nv_bfloat16 C[2][Q * 64];     // C tile [t][n]: 2 panels of 64 n (TMA, SW128); one chunk
-    __nv_bfloat16 B[2][2][Q * 64];  // B tiles [s][n] by chunk parity
+    __nv_bfloat16 B[2][Q * 64];     // B tile [s][n]: 2 panels of 64 n (TMA, SW128); one chunk
     __nv_bfloat16 XS[2][Q * 64];    // scaled x rows [s][p] (SW128): v o x or w o x, by parity
     __nv_bfloat16 XR[2][Q * 64];    // x rows [s][p] (exact chunks), by parity
+    __nv_bfloat16 XRAW[2][Q * 64];  // raw x rows [t][p] of a chunk (TMA, SW128), by parity
     __nv_bfloat16 Hs[N * 64];       // bf16 state rows [n][p] of the previous chunk: G3's B
     __nv_bfloat16 Zt[2][Q * 64];    // z rows [t][p] by chunk parity (TMA, SW128); y written
                                     // over them in place, stored by 32-row quarters
+    __nv_bfloat16 XH[2][4 * 64];    // the 4 raw x rows before a chunk (TMA, unswizzled), by parity
     ChunkVals cv[kCv];              // ring of per-chunk values
     // taps by [tap][channel pair] (front-padded with zeros): a thread reads its two
     // pairs of a tap as one 16-byte vector, a half-warp a contiguous 256 bytes
     alignas(16) float2 wconv[kMaxW][P / 2];
     alignas(16) float2 bconv[P / 2];
-    uint64_t full_c, full_b[2], full_z[2];  // TMA landed
+    uint64_t full_c, full_b, full_z[2], full_x[2];  // TMA landed
     uint64_t g1, g3, g4, g2, fin;   // MMA commits
     uint64_t xready, mready, hsready;                    // compute -> control
     uint64_t cvready[kCv], epidone[kCv];                 // gamma warp <-> compute
@@ -155,7 +160,8 @@ static_assert(offsetof(TcSmem, C) % 1024 == 0 && offsetof(TcSmem, B) % 1024 == 0
 static_assert(offsetof(TcSmem, XS) % 1024 == 0 && offsetof(TcSmem, XR) % 1024 == 0, "tile");
 static_assert(sizeof(((TcSmem*)nullptr)->XS[0]) % 1024 == 0, "tile");
 static_assert(sizeof(((TcSmem*)nullptr)->XR[0]) % 1024 == 0, "tile");
-static_assert(offsetof(TcSmem, Hs) % 1024 == 0, "tile");
+static_assert(offsetof(TcSmem, Hs) % 1024 == 0 && offsetof(TcSmem, XRAW) % 1024 == 0, "tile");
+static_assert(offsetof(TcSmem, XH) % 128 == 0 && sizeof(((TcSmem*)nullptr)->XH[0]) % 128 == 0, "tile");
 static_assert(sizeof(ChunkVals) % 16 == 0 && offsetof(TcSmem, cv) % 16 == 0, "float4 rows");
 static_assert(offsetof(ChunkVals, g2l) % 16 == 0 && offsetof(ChunkVals, dts) % 16 == 0, "float4");
 static_assert(offsetof(ChunkVals, sc) % 16 == 0 && offsetof(ChunkVals, vb) % 16 == 0, "float4");
@@ -285,7 +291,8 @@ __device__ __forceinline__ bool wait_or_abort(TcSmem& s, uint64_t* bar, uint32_t
 template <bool kVarlen, bool kNorm>
 __global__ void __launch_bounds__(kThreads, 1)
     scan_tc_kernel(const __grid_constant__ CUtensorMap map_bc, const __grid_constant__ CUtensorMap map_z,
-                   const __grid_constant__ CUtensorMap map_y, const TcScanParams p)
+                   const __grid_constant__ CUtensorMap map_y, const __grid_constant__ CUtensorMap map_x,
+                   const __grid_constant__ CUtensorMap map_xh, const TcScanParams p)
 {
     // Align to the 1024-byte swizzle atom with pointer arithmetic on the
     // shared array itself, so the compiler keeps every access in the shared
@@ -333,7 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&s.full_c, 1);
         mbar_init(&s.full_z[0], 1);
         mbar_init(&s.full_z[1], 1);
-        for (int i = 0; i < 2; ++i) mbar_init(&s.full_b[i], 1);
+        mbar_init(&s.full_b, 1);
+        mbar_init(&s.full_x[0], 1);
+        mbar_init(&s.full_x[1], 1);
         mbar_init(&s.g1, 1);
         mbar_init(&s.g3, 1);
         mbar_init(&s.g4, 1);
@@ -379,6 +388,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // state update.
         if (lane == 0 && nchunks > 0) {
             prefetch_tmap(&map_bc);
+            // raw x rows: the B|C conv does not write them, so the first two chunks'
+            // are requested before waiting for it
+            prefetch_tmap(&map_x);
+            int loaded_x = 0;
+            auto load_x = [&](int c) {  // raw x tile of chunk c and the 4 rows before it
+                const int kx = c & 1;
+                mbar_arrive_expect_tx(&s.full_x[kx], Q * 64 * 2 + (c > 0 ? 4 * 64 * 2 : 0));
+                tma_load_3d(s.XRAW[kx], &map_x, &s.full_x[kx], h * P, trow(c), tz);
+                if (c > 0) tma_load_3d(s.XH[kx], &map_xh, &s.full_x[kx], h * P, trow(c) - 4, tz);
+                loaded_x = c + 1;
+            };
+            load_x(0);
+            if (nchunks > 1) load_x(1);
             // launched to overlap the B|C conv that writes the bc tiles (when there
             // is one): wait for it here, before the first tile load.  Every read of
             // the old conv state by that kernel is then done too, so the new conv
@@ -394,11 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(s.C[1], &map_bc, &s.full_c, xC + 64, trow(c), tz);
                 loaded_c = c + 1;
             };
-            auto load_b = [&](int c) {  // B tile of chunk c into buffer c & 1
-                const int kb = c & 1;
-                mbar_arrive_expect_tx(&s.full_b[kb], 2 * Q * 64 * 2);
-                tma_load_3d(s.B[kb][0], &map_bc, &s.full_b[kb], xB, trow(c), tz);
-                tma_load_3d(s.B[kb][1], &map_bc, &s.full_b[kb], xB + 64, trow(c), tz);
+            auto load_b = [&](int c) {  // B tile of chunk c (the one buffer)
+                mbar_arrive_expect_tx(&s.full_b, 2 * Q * 64 * 2);
+                tma_load_3d(s.B[0], &map_bc, &s.full_b, xB, trow(c), tz);
+                tma_load_3d(s.B[1], &map_bc, &s.full_b, xB + 64, trow(c), tz);
                 loaded_b = c + 1;
             };
             // K step k of a K-major operand: (k>>2)*16 KB + (k&3)*32 B; of an MN-major
@@ -413,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dC = sdesc_sw128(smem_u32(s.C), 16, 1024);
             auto g1 = [&](int c) {
                 const uint64_t dA = dC;
-                const uint64_t dB = sdesc_sw128(smem_u32(s.B[c & 1]), 16, 1024);
+                const uint64_t dB = sdesc_sw128(smem_u32(s.B), 16, 1024);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     mma_bf16_ss(tbase + kColCB, dA + kmaj(k), dB + kmaj(k), kIdCB, k > 0);
@@ -448,8 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             load_c(0);
             load_b(0);
-            if (nchunks > 1) load_b(1);
-            bool ok = wait_or_abort(s, &s.full_c, 0, wlim) && wait_or_abort(s, &s.full_b[0], 0, wlim);
+            bool ok = wait_or_abort(s, &s.full_c, 0, wlim) && wait_or_abort(s, &s.full_b, 0, wlim);
             if (ok) {
                 tc_fence_after();
                 g1(0);
@@ -460,21 +480,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // G4(c): x rows of chunk c in place; dH read by state(c-1)
                 ok = wait_or_abort(s, &s.xready, c & 1, wlim) && wait_or_abort(s, &s.hsready, c & 1, wlim);
                 if (!ok) break;
+                // the conv of chunk c is done with its raw tile: chunk c+2's goes there
+                if (c + 2 < nchunks) load_x(c + 2);
                 tc_fence_after();
                 {
-                    const uint64_t dA = sdesc_sw128(smem_u32(s.B[kb]), Q * 128, 1024);
+                    const uint64_t dA = sdesc_sw128(smem_u32(s.B), Q * 128, 1024);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
                         mma_bf16_ss(tbase + kColDH, dA + 128 * k, (kb ? dXS1 : dXS0) + 128 * k, kIdState, k > 0);
                     mma_commit(&s.g4);
                 }
-                // tiles: C of chunk c+1 (G1(c), G3(c) done), B of chunk c+2 into B[kb]
-                // (G1(c), G4(c) done)
+                // tiles of chunk c+1: C (G1(c), G3(c) done) and B (G1(c), G4(c) done)
                 if (c + 1 < nchunks) {
                     ok = wait_or_abort(s, &s.g4, c & 1, wlim);
                     if (!ok) break;
                     load_c(c + 1);
-                    if (c + 2 < nchunks) load_b(c + 2);
+                    load_b(c + 1);
                 }
                 // z of chunk c once the epilogue of chunk c-1 is done (it comes before
                 // the mask of chunk c, so this does not hold up G2(c))
@@ -497,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (c + 1 < nchunks) {
                     // G1(c+1): its tiles landed
                     ok = wait_or_abort(s, &s.full_c, (c + 1) & 1, wlim) &&
-                         wait_or_abort(s, &s.full_b[(c + 1) & 1], ((c + 1) >> 1) & 1, wlim);
+                         wait_or_abort(s, &s.full_b, (c + 1) & 1, wlim);
                     if (!ok) break;
                     tc_fence_after();
                     g1(c + 1);
@@ -514,8 +535,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int k = loaded_c - 1;
                 while (!mbar_test(&s.full_c, k & 1) && globaltimer_ns() - t0 < kWaitNs) __nanosleep(64);
             }
-            for (int k = max(0, loaded_b - 2); k < loaded_b; ++k)
-                while (!mbar_test(&s.full_b[k & 1], (k >> 1) & 1) && globaltimer_ns() - t0 < kWaitNs)
+            if (loaded_b > 0) {
+                const int k = loaded_b - 1;
+                while (!mbar_test(&s.full_b, k & 1) && globaltimer_ns() - t0 < kWaitNs) __nanosleep(64);
+            }
+            for (int k = max(0, loaded_x - 2); k < loaded_x; ++k)  // the last load into each buffer
+                while (!mbar_test(&s.full_x[k & 1], (k >> 1) & 1) && globaltimer_ns() - t0 < kWaitNs)
                     __nanosleep(64);
             for (int k = max(0, loaded_z - 2); k < loaded_z; ++k)  // the last load into each buffer
                 while (!mbar_test(&s.full_z[k & 1], (k >> 1) & 1) && globaltimer_ns() - t0 < kWaitNs)
@@ -641,26 +666,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // -- conv share: rows 4 rq .. 4 rq + 3, channels 4 jq .. 4 jq + 3 --
         const int rq = tid >> 4, jq = tid & 15;
-        const __nv_bfloat16* xrow =
-            static_cast<const __nv_bfloat16*>(p.xbc) + (size_t)row0 * Cdim + h * P + 4 * jq;
         const __nv_bfloat16* csb =
             cs_in ? static_cast<const __nv_bfloat16*>(cs_in) + (size_t)slot * (W - 1) * Cdim + h * P + 4 * jq
                   : nullptr;
-        uint2 raw[kRaw];  // raw rows 4rq-3 .. 4rq+3 of a chunk, loaded one chunk ahead
-        auto load_raw = [&](int c) {
-            const int g0 = c * Q + 4 * rq - (kMaxW - 1);
+        // the raw rows before chunk 0 (the conv state's x columns; rq == 0 only):
+        // later chunks find theirs in the 4-row tile loaded with their own rows
+        uint2 halo0[kMaxW - 1];
 #pragma unroll
-            for (int i = 0; i < kRaw; ++i) {
-                const int gr = g0 + i;
-                uint2 v = make_uint2(0u, 0u);
-                if (gr >= 0) {
-                    if (gr < S) v = ldg_u2(xrow + (size_t)gr * Cdim);
-                } else if (csb != nullptr && gr + W - 1 >= 0) {
-                    v = ldg_u2(csb + (size_t)(gr + W - 1) * Cdim);
-                }
-                raw[i] = v;
-            }
-        };
+        for (int i = 0; i < kMaxW - 1; ++i) {
+            const int gr = i - (kMaxW - 1);
+            halo0[i] = make_uint2(0u, 0u);
+            if (rq == 0 && csb != nullptr && gr + W - 1 >= 0) halo0[i] = ldg_u2(csb + (size_t)(gr + W - 1) * Cdim);
+        }
         // conv(c): x rows and scaled x rows of chunk c (this thread's 4 x 4 share)
         auto conv = [&](int c) {
             const int rows = min(Q, S - c * Q);
@@ -668,6 +685,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool need_x = cv.factored == 0;  // x rows feed G2 in the exact form
             const float4 sc4 = *reinterpret_cast<const float4*>(&cv.sc[4 * rq]);
             const float scs[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+            // raw rows 4rq-3 .. 4rq+3: this chunk's tile, the 4-row tile before it
+            // (later chunks) or the conv state (chunk 0)
+            uint2 raw[kRaw];
+#pragma unroll
+            for (int i = 0; i < kRaw; ++i) {
+                const int r = 4 * rq - (kMaxW - 1) + i;
+                if (r >= 0)
+                    raw[i] = at<uint2>(s.XRAW[c & 1], chunk_off(r, jq >> 1) + ((jq & 1) << 3));
+                else if (c > 0)
+                    raw[i] = at<uint2>(s.XH[c & 1], (uint32_t)((r + 4) * 128 + jq * 8));
+                else
+                    raw[i] = i < kMaxW - 1 ? halo0[i < kMaxW - 1 ? i : 0] : make_uint2(0u, 0u);
+            }
             // out[i] = b + sum_k w[k] u[i+k] over raw rows i .. i+3, tap by tap (only
             // one tap's weights live at a time: registers are scarce with 18 warps)
             float2 acc[4][2];
@@ -740,12 +770,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
         }
         if (nchunks > 0) {
-            load_raw(0);
-            ok = wait_or_abort(s, &s.cvready[0], 0, wlim);
+            ok = wait_or_abort(s, &s.cvready[0], 0, wlim) && wait_or_abort(s, &s.full_x[0], 0, wlim);
             if (ok) conv(0);
             fence_proxy_async_smem();  // XR / XS are read by G4 / G2
             mbar_arrive(&s.xready);
-            if (nchunks > 1) load_raw(1);
         }
 
         for (int c = 0; c < nchunks; ++c) {
@@ -847,11 +875,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- conv(c+1): XS[(c+1)&1] and XR[(c+1)&1] were read by G4(c-1) and
             // G2(c-1), which this thread saw done in the epilogue of chunk c-1 ----
             if (c + 1 < nchunks) {
-                if (ok) ok = wait_or_abort(s, &s.cvready[(c + 1) % kCv], ((c + 1) / kCv) & 1, wlim);
+                if (ok)
+                    ok = wait_or_abort(s, &s.cvready[(c + 1) % kCv], ((c + 1) / kCv) & 1, wlim) &&
+                         wait_or_abort(s, &s.full_x[(c + 1) & 1], ((c + 1) >> 1) & 1, wlim);
                 if (ok) conv(c + 1);
                 fence_proxy_async_smem();  // XR / XS are read by G4 / G2
                 mbar_arrive(&s.xready);
-                if (c + 2 < nchunks) load_raw(c + 2);
             }
 
             // ---- epilogue(c): factored y = u Y; exact y = Y + u Yo; times silu(z).
@@ -998,15 +1027,18 @@ bool encode_fn()
     return g_encode != nullptr;
 }
 
-// 3-D map over rows of `cols` bf16: dims {cols, S, B}, box {64, box_rows, 1}, SW128.
-bool make_map(CUtensorMap* m, const void* base, int cols, int S, int B, int box_rows = Q)
+// 3-D map over rows of `cols` bf16: dims {cols, S, B}, box {64, box_rows, 1}, SW128
+// (or unswizzled).
+bool make_map(CUtensorMap* m, const void* base, int cols, int S, int B, int box_rows = Q,
+              bool swizzle = true)
 {
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)S, (cuuint64_t)B};
     cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * 2 * (cuuint64_t)S};
     cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1025,8 +1057,13 @@ cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st, bool after_pr
     // rows; with no rows, any 16-byte aligned array stands in (no tile is read)
     const int mS = p.S > 0 ? p.S : 1, mB = varlen ? 1 : p.B;
     const void* stand_in = p.h0;
-    CUtensorMap mbc, mz, my;
+    CUtensorMap mbc, mz, my, mx, mxh;
     if (!make_map(&mbc, p.S > 0 ? p.bc : stand_in, p.bc_stride, mS, mB)) return cudaErrorInvalidValue;
+    // raw x rows of a head (128-row tiles) and the 4 rows before a tile, [B, S, Cdim]
+    const int Cdim = p.H * P + 2 * p.G * N;
+    if (!make_map(&mx, p.S > 0 ? p.xbc : stand_in, Cdim, mS, mB) ||
+        !make_map(&mxh, p.S > 0 ? p.xbc : stand_in, Cdim, mS, mB, 4, false))
+        return cudaErrorInvalidValue;
     // z tiles in (128 rows), y leaves in 32-row quarters; both [B, S, H*P]
     memset(&mz, 0, sizeof(mz));
     if ((p.flags & kHasZ) && !make_map(&mz, p.S > 0 ? p.z : stand_in, p.H * P, mS, mB))
@@ -1048,7 +1085,7 @@ cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st, bool after_pr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = after_prepass ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kernel, mbc, mz, my, p);
+    return cudaLaunchKernelEx(&cfg, kernel, mbc, mz, my, mx, mxh, p);
 }
 
 }  // namespace ssd
