@@ -336,13 +336,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool has_z = (p.flags & kHasZ) != 0;
     const uint64_t wlim = p.wait_ns ? p.wait_ns : kWaitNs;  // pipeline waits
 
+    // Work that needs nothing from the setup starts before its barrier: the
+    // control thread's raw x tiles of the first two chunks (it initialises their
+    // barriers itself) and the gamma warp's first dt rows.
+    int loaded_x = 0;  // raw x tiles requested (control thread)
+    auto load_x = [&](int c) {  // raw x tile of chunk c and the 4 rows before it
+        const int kx = c & 1;
+        mbar_arrive_expect_tx(&s.full_x[kx], Q * 64 * 2 + (c > 0 ? 4 * 64 * 2 : 0));
+        tma_load_3d(s.XRAW[kx], &map_x, &s.full_x[kx], h * P, trow(c), tz);
+        if (c > 0) tma_load_3d(s.XH[kx], &map_xh, &s.full_x[kx], h * P, trow(c) - 4, tz);
+        loaded_x = c + 1;
+    };
+    if (warp == kControlWarp && lane == 0) {
+        mbar_init(&s.full_x[0], 1);
+        mbar_init(&s.full_x[1], 1);
+        fence_mbar_init();
+        if (nchunks > 0) {
+            prefetch_tmap(&map_x);
+            load_x(0);
+            if (nchunks > 1) load_x(1);
+        }
+    }
+    float dt0[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (warp == kGammaWarp) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = 4 * lane + i;
+            if (r < S) dt0[i] = p.dt[((size_t)row0 + r) * H + h];
+        }
+    }
     if (tid == 0) {
         mbar_init(&s.full_c, 1);
         mbar_init(&s.full_z[0], 1);
         mbar_init(&s.full_z[1], 1);
         mbar_init(&s.full_b, 1);
-        mbar_init(&s.full_x[0], 1);
-        mbar_init(&s.full_x[1], 1);
         mbar_init(&s.g1, 1);
         mbar_init(&s.g3, 1);
         mbar_init(&s.g4, 1);
@@ -362,17 +389,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(&s.tmem_base, 512);
         tmem_relinquish();
     }
-    if (p.conv) {
-        for (int i = tid; i < P / 2; i += kThreads) {
-            float w4[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            for (int e = 0; e < 2; ++e)
-                for (int k = 0; k < W; ++k)
-                    w4[e][kMaxW - W + k] = p.conv_w[(size_t)(h * P + 2 * i + e) * W + k];
-            for (int k = 0; k < kMaxW; ++k) s.wconv[k][i] = make_float2(w4[0][k], w4[1][k]);
-            s.bconv[i] = p.conv_b ? make_float2(p.conv_b[h * P + 2 * i], p.conv_b[h * P + 2 * i + 1])
-                                  : make_float2(0.f, 0.f);
-        }
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -388,19 +404,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // state update.
         if (lane == 0 && nchunks > 0) {
             prefetch_tmap(&map_bc);
-            // raw x rows: the B|C conv does not write them, so the first two chunks'
-            // are requested before waiting for it
-            prefetch_tmap(&map_x);
-            int loaded_x = 0;
-            auto load_x = [&](int c) {  // raw x tile of chunk c and the 4 rows before it
-                const int kx = c & 1;
-                mbar_arrive_expect_tx(&s.full_x[kx], Q * 64 * 2 + (c > 0 ? 4 * 64 * 2 : 0));
-                tma_load_3d(s.XRAW[kx], &map_x, &s.full_x[kx], h * P, trow(c), tz);
-                if (c > 0) tma_load_3d(s.XH[kx], &map_xh, &s.full_x[kx], h * P, trow(c) - 4, tz);
-                loaded_x = c + 1;
-            };
-            load_x(0);
-            if (nchunks > 1) load_x(1);
             // launched to overlap the B|C conv that writes the bc tiles (when there
             // is one): wait for it here, before the first tile load.  Every read of
             // the old conv state by that kernel is then done too, so the new conv
@@ -553,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
         const float Dabs = p.D ? fabsf(p.D[h]) : 0.0f;
         const bool softplus = (p.flags & kDtSoftplus) != 0;
-        float dtn[4];
+        float dtn[4] = {dt0[0], dt0[1], dt0[2], dt0[3]};
         auto load_dt = [&](int c) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -561,7 +564,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dtn[i] = r < S ? p.dt[((size_t)row0 + r) * H + h] : 0.0f;
             }
         };
-        if (nchunks > 0) load_dt(0);
         for (int c = 0; c < nchunks; ++c) {
             const int rows = min(Q, S - c * Q);
             ChunkVals& cv = s.cv[c % kCv];
@@ -663,6 +665,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t sbase = ((size_t)slot * H + h) * P * N;
         const float Dh = p.D ? p.D[h] : 0.0f;
         bool ok = true;  // false after any failed wait: the thread then only walks the loop
+        // conv taps by [tap][channel pair] and bias into shared memory (read by the
+        // first conv, after the compute warps' barrier below)
+        if (p.conv && tid < P / 2) {
+            float w4[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            for (int e = 0; e < 2; ++e)
+                for (int k = 0; k < W; ++k)
+                    w4[e][kMaxW - W + k] = p.conv_w[(size_t)(h * P + 2 * tid + e) * W + k];
+            for (int k = 0; k < kMaxW; ++k) s.wconv[k][tid] = make_float2(w4[0][k], w4[1][k]);
+            s.bconv[tid] = p.conv_b ? make_float2(p.conv_b[h * P + 2 * tid], p.conv_b[h * P + 2 * tid + 1])
+                                    : make_float2(0.f, 0.f);
+        }
 
         // -- conv share: rows 4 rq .. 4 rq + 3, channels 4 jq .. 4 jq + 3 --
         const int rq = tid >> 4, jq = tid & 15;
@@ -769,6 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st16(tbase + lane_off + kColM + 16 * j, zero);
             tmem_st_wait();
         }
+        named_bar_sync(5, kCompute);  // the conv weights
         if (nchunks > 0) {
             ok = wait_or_abort(s, &s.cvready[0], 0, wlim) && wait_or_abort(s, &s.full_x[0], 0, wlim);
             if (ok) conv(0);
