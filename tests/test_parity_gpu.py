@@ -149,6 +149,19 @@ def test_prefill_137_rows_every_element():
     check_prefill_every_element(shape, cpu, y, h, cs, torch.bfloat16)
 
 
+@pytest.mark.parametrize("splits", [[129, 130, 258], [1, 128, 2, 386]])
+def test_calls_whose_last_chunk_is_short_chain_their_conv_state(splits):
+    """Calls whose last chunk holds 1 or 2 rows: the new conv state (the last
+    W-1 raw rows) then reaches back into the chunk before.  Chained calls over
+    517 rows, every element of y and of the final states against one oracle
+    pass over all rows (a wrong conv state would also corrupt the next call's
+    first rows); the final conv state bit for bit."""
+    shape = si.Shape(batch=2, seqlen=sum(splits), nheads=16, headdim=64, dstate=128, ngroups=2)
+    cpu, dev = make_problem(shape, act=torch.bfloat16, seed=13)
+    y, h, cs = gpu_prefill(shape, dev, splits)
+    check_prefill_every_element(shape, cpu, y, h, cs, torch.bfloat16)
+
+
 # ---------------------------------------------------------------------------
 # the other workloads at full size, in the calls the benchmark makes.  Inputs
 # are drawn on the GPU; the checked sequences are copied to the host and the
