@@ -134,8 +134,7 @@ SSD_API ssd_status ssd_conv1d_rows(const ssd_dims* dims, ssd_dtype act,
  *   state = exp(dt_t A[h]) state + dt_t x_t B_t^T       state [P,N]
  *   y[b,t,h,:] = state C_t + D[h] x_t   (times silu(z) with SSD_HAS_Z)
  * computed in 128-row chunks on the tensor cores (bf16, P=64, N=128, W<=4,
- * calls of more than 4 rows) or exactly row by row (fp32, other shapes, and
- * bf16 calls of at most 4 rows, where the row kernel is faster).
+ * any row count) or exactly row by row (fp32 and other shapes).
  *
  * xbc             [B,S,Cdim] act: raw rows when conv_w != NULL (the conv of
  *                 ssd_conv1d_rows runs first), else already post-conv rows.
@@ -201,7 +200,7 @@ SSD_API ssd_status ssd_chunk_scan_workspace_size(const ssd_dims* dims, ssd_dtype
  * On the tensor-core path the scan's epilogue applies the gate and leaves
  * each row's sum of y_ssm^2 per head in the workspace (fp32, before y is
  * rounded); a second kernel scales y in place by the weight and the group's
- * inverse norm.  Elsewhere (fp32, calls of <= 4 rows, norm groups whose
+ * inverse norm.  Elsewhere (fp32, other shapes, norm groups whose
  * head count is not a multiple of 4) the scan runs without the gate and
  * ssd_gated_group_rmsnorm follows it in place.  Group channel count as in
  * ssd_gated_group_rmsnorm, else SSD_ERR_UNSUPPORTED; errors as

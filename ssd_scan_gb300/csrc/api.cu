@@ -67,13 +67,14 @@ ssd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR
 
 // The tensor-core chunk scan serves bf16 with P = 64, N = 128, W <= 4 and
 // 128-row chunks; everything else runs on the row-exact fp32-pipe kernel.
-// Calls of at most this many rows per sequence take the row-exact kernel even
-// in bf16 (one CTA per (sequence, head), the state in registers, no chunk
-// pipeline to fill).  Measured at 4 sequences x 128 heads: the tensor-core
-// path costs ~37 us for any call of up to 128 rows, the row kernel ~25 us for
-// one row and ~2.7 us more per row, so the row kernel wins up to 4 rows.
+// Calls of at most SSD_SHORT_CALL_ROWS rows per sequence would take the
+// row-exact kernel even in bf16.  Measured (us per call, tensor cores / row
+// kernel): 4 sequences x 128 heads, 1 row 26.7 / 24.6, 2 rows 26.7 / 26.7,
+// 4 rows 26.6 / 32.8; 1 sequence, 1 row 12.4 / 16.5.  Calls of up to 128
+// rows walk several units per CTA on the tensor cores, so none goes to the
+// row kernel.
 #ifndef SSD_SHORT_CALL_ROWS
-#define SSD_SHORT_CALL_ROWS 4
+#define SSD_SHORT_CALL_ROWS 0
 #endif
 
 bool use_tensor_cores(const ssd_dims* d, ssd_dtype act)
@@ -289,7 +290,9 @@ ssd_status chunk_scan_impl(const ssd_dims* dims, ssd_dtype act, unsigned flags, 
             tp.bc_stride = 2 * G * N;
             tp.bc_col0 = 0;
         }
-        s = counted(launch_scan_tc(tp, stream, conv_w != nullptr), SSD_KERNEL_SCAN_TC);
+        s = counted(scan_units_supports(tp) ? launch_scan_units(tp, stream, conv_w != nullptr)
+                                            : launch_scan_tc(tp, stream, conv_w != nullptr),
+                    SSD_KERNEL_SCAN_TC);
         if (s == SSD_OK && norm) {
             NormScaleParams np{dims->batch, dims->seqlen, H, P, G, eps, tp.norm_ss, norm_w, y};
             s = counted(launch_norm_scale(np, stream), SSD_KERNEL_NORM_SCALE, dims->seqlen > 0);

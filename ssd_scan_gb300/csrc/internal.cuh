@@ -146,6 +146,10 @@ struct TcScanParams {
     float* norm_ss = nullptr;
 };
 bool scan_tc_supports(int P, int N);
+// Calls of at most 128 rows per sequence (fixed length, no fused norm): one CTA
+// per SM walking several one-chunk (sequence, head) units.
+bool scan_units_supports(const TcScanParams& p);
+cudaError_t launch_scan_units(const TcScanParams& p, cudaStream_t st, bool after_prepass);
 // after_prepass: the kernel just before it on `st` is the B|C conv writing p.bc;
 // the scan is then launched to overlap that kernel's tail (programmatic
 // dependent launch) and waits for it before its first read of p.bc.

@@ -260,12 +260,14 @@ __device__ __forceinline__ T& at(void* base, uint32_t off)
     return *reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(base) + off);
 }
 
-__device__ __forceinline__ bool aborted(TcSmem& s)
+template <typename SM>
+__device__ __forceinline__ bool aborted(SM& s)
 {
     return *reinterpret_cast<volatile int*>(&s.abort) != 0;
 }
 
-__device__ __forceinline__ void set_abort(TcSmem& s)
+template <typename SM>
+__device__ __forceinline__ void set_abort(SM& s)
 {
     *reinterpret_cast<volatile int*>(&s.abort) = 1;
 }
@@ -273,7 +275,8 @@ __device__ __forceinline__ void set_abort(TcSmem& s)
 // Bounded wait that also gives up as soon as another thread has aborted.
 // The hinted try_wait suspends the thread until the phase completes (or
 // about a microsecond passes), so a waiting warp takes no issue slots.
-__device__ __forceinline__ bool wait_or_abort(TcSmem& s, uint64_t* bar, uint32_t parity,
+template <typename SM>
+__device__ __forceinline__ bool wait_or_abort(SM& s, uint64_t* bar, uint32_t parity,
                                               uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
@@ -1033,6 +1036,682 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ---- short calls: several one-chunk units per CTA --------------------------------
+//
+// A call of at most Q rows per sequence has one chunk per (sequence, head), and
+// one CTA per unit spends more on its prologue (barriers, TMEM, the first
+// tiles and row values) and its tail than on the chunk.  scan_units_kernel
+// keeps one CTA per SM and walks the units blockIdx.x, blockIdx.x + gridDim.x,
+// ... through the same chunk pipeline as scan_tc_kernel, each unit in the
+// place of a chunk: its tiles, row values, conv taps and conv halo are
+// requested while the unit before it is processed.  The state does not carry
+// from unit to unit: the state update of unit c writes unit c's final state
+// and puts unit c+1's initial state in the state tile (the arrival that G3 and
+// G4 of unit c+1 wait for, as for the next chunk of one sequence).  The x
+// columns of a unit's new conv state are written from the raw rows its conv
+// reads.  Bit for bit the arithmetic of scan_tc_kernel.
+
+constexpr int kUv = 2;  // per-unit value sets in flight
+
+struct __align__(16) UnitVals {
+    ChunkVals cv;                                   // the unit's row values
+    alignas(16) float2 wconv[kMaxW][P / 2];         // its head's conv taps (front-padded)
+    alignas(16) float2 bconv[P / 2];
+    alignas(16) __nv_bfloat16 halo[kMaxW - 1][P];   // raw x rows -3 .. -1: its conv state
+    float Dh;                                       // its head's D
+    int pad[3];
+};
+
+struct __align__(1024) UnitSmem {
+    __nv_bfloat16 C[2][Q * 64];
+    __nv_bfloat16 B[2][Q * 64];
+    __nv_bfloat16 XS[2][Q * 64];
+    __nv_bfloat16 XR[2][Q * 64];
+    __nv_bfloat16 XRAW[2][Q * 64];
+    __nv_bfloat16 Hs[N * 64];
+    __nv_bfloat16 Zt[2][Q * 64];
+    UnitVals uv[kUv];
+    uint64_t full_c, full_b, full_z[2], full_x[2];
+    uint64_t g1, g3, g4, g2, fin;
+    uint64_t xready, mready, hsready;
+    uint64_t cvready[kUv], epidone[kUv];
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t kUnitSmemBytes = sizeof(UnitSmem) + 1024;
+static_assert(offsetof(UnitSmem, B) % 1024 == 0 && offsetof(UnitSmem, XS) % 1024 == 0, "tile");
+static_assert(offsetof(UnitSmem, XR) % 1024 == 0 && offsetof(UnitSmem, XRAW) % 1024 == 0, "tile");
+static_assert(offsetof(UnitSmem, Hs) % 1024 == 0 && offsetof(UnitSmem, Zt) % 1024 == 0, "tile");
+static_assert(sizeof(UnitVals) % 16 == 0 && offsetof(UnitSmem, uv) % 16 == 0, "float4 rows");
+static_assert(offsetof(UnitVals, wconv) % 16 == 0 && offsetof(UnitVals, halo) % 16 == 0, "vectors");
+static_assert(offsetof(UnitSmem, full_c) % 8 == 0, "mbarriers");
+static_assert(kUnitSmemBytes <= 232448, "shared memory per CTA");
+
+__global__ void __launch_bounds__(kThreads, 1)
+    scan_units_kernel(const __grid_constant__ CUtensorMap map_bc, const __grid_constant__ CUtensorMap map_z,
+                      const __grid_constant__ CUtensorMap map_y, const __grid_constant__ CUtensorMap map_x,
+                      const TcScanParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    UnitSmem& s = *reinterpret_cast<UnitSmem*>(smem_raw + ((1024u - (sm100::smem_u32(smem_raw) & 1023u)) & 1023u));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = p.H, G = p.G, W = p.W, S = p.S;  // S <= Q: one chunk per unit
+    const int hpg = H / G;
+    const int Cdim = H * P + 2 * G * N;
+    // this CTA's units: c-th = (sequence, head) number blockIdx.x + c gridDim.x
+    const int nu = (p.B * H - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    auto unit_b = [&](int c) { return ((int)blockIdx.x + c * (int)gridDim.x) / H; };
+    auto unit_h = [&](int c) { return ((int)blockIdx.x + c * (int)gridDim.x) % H; };
+    const bool has_z = (p.flags & kHasZ) != 0;
+    const uint64_t wlim = p.wait_ns ? p.wait_ns : kWaitNs;
+
+    // the raw x tiles of the first two units before the setup barrier
+    int loaded_x = 0;
+    auto load_x = [&](int c) {
+        const int kx = c & 1;
+        mbar_arrive_expect_tx(&s.full_x[kx], Q * 64 * 2);
+        tma_load_3d(s.XRAW[kx], &map_x, &s.full_x[kx], unit_h(c) * P, 0, unit_b(c));
+        loaded_x = c + 1;
+    };
+    if (warp == kControlWarp && lane == 0) {
+        mbar_init(&s.full_x[0], 1);
+        mbar_init(&s.full_x[1], 1);
+        fence_mbar_init();
+        if (nu > 0) {
+            prefetch_tmap(&map_x);
+            load_x(0);
+            if (nu > 1) load_x(1);
+        }
+    }
+    if (tid == 0) {
+        mbar_init(&s.full_c, 1);
+        mbar_init(&s.full_z[0], 1);
+        mbar_init(&s.full_z[1], 1);
+        mbar_init(&s.full_b, 1);
+        mbar_init(&s.g1, 1);
+        mbar_init(&s.g3, 1);
+        mbar_init(&s.g4, 1);
+        mbar_init(&s.g2, 1);
+        mbar_init(&s.fin, 1);
+        mbar_init(&s.xready, kCompute);
+        mbar_init(&s.mready, kCompute);
+        mbar_init(&s.hsready, kCompute);
+        for (int i = 0; i < kUv; ++i) {
+            mbar_init(&s.cvready[i], 32);
+            mbar_init(&s.epidone[i], kCompute);
+        }
+        s.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&s.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = s.tmem_base;
+
+    if (warp == kControlWarp) {
+        // ===================== control: TMA + MMA (one thread) =====================
+        // scan_tc_kernel's order, unit c in the place of chunk c
+        if (lane == 0 && nu > 0) {
+            prefetch_tmap(&map_bc);
+            griddep_wait();  // the B|C pre-pass (see scan_tc_kernel)
+            int loaded_c = 0, loaded_b = 0, loaded_z = 0;
+            auto load_c = [&](int c) {
+                const int xC = p.bc_col0 + G * N + (unit_h(c) / hpg) * N;
+                mbar_arrive_expect_tx(&s.full_c, 2 * Q * 64 * 2);
+                tma_load_3d(s.C[0], &map_bc, &s.full_c, xC, 0, unit_b(c));
+                tma_load_3d(s.C[1], &map_bc, &s.full_c, xC + 64, 0, unit_b(c));
+                loaded_c = c + 1;
+            };
+            auto load_b = [&](int c) {
+                const int xB = p.bc_col0 + (unit_h(c) / hpg) * N;
+                mbar_arrive_expect_tx(&s.full_b, 2 * Q * 64 * 2);
+                tma_load_3d(s.B[0], &map_bc, &s.full_b, xB, 0, unit_b(c));
+                tma_load_3d(s.B[1], &map_bc, &s.full_b, xB + 64, 0, unit_b(c));
+                loaded_b = c + 1;
+            };
+            auto kmaj = [](int k) { return (uint64_t)(((k >> 2) << 10) + ((k & 3) << 1)); };
+            const uint64_t dHs = sdesc_sw128(smem_u32(s.Hs), 8192, 1024);
+            const uint64_t dXS0 = sdesc_sw128(smem_u32(s.XS[0]), 8192, 1024);
+            const uint64_t dXS1 = sdesc_sw128(smem_u32(s.XS[1]), 8192, 1024);
+            const uint64_t dXR0 = sdesc_sw128(smem_u32(s.XR[0]), 8192, 1024);
+            const uint64_t dXR1 = sdesc_sw128(smem_u32(s.XR[1]), 8192, 1024);
+            const uint64_t dC = sdesc_sw128(smem_u32(s.C), 16, 1024);
+            auto g1 = [&]() {
+                const uint64_t dB = sdesc_sw128(smem_u32(s.B), 16, 1024);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16_ss(tbase + kColCB, dC + kmaj(k), dB + kmaj(k), kIdCB, k > 0);
+                mma_commit(&s.g1);
+            };
+            // G3(c): unit c's initial state in the state tile; Y / Yo [c&1] read by
+            // the epilogue of unit c-2
+            auto g3 = [&](int c) -> bool {
+                bool r = wait_or_abort(s, &s.hsready, c & 1, wlim) &&
+                         wait_or_abort(s, &s.cvready[c % kUv], (c / kUv) & 1, wlim);
+                if (r && c >= 2) r = wait_or_abort(s, &s.epidone[(c - 2) % kUv], ((c - 2) / kUv) & 1, wlim);
+                if (!r) return false;
+                tc_fence_after();
+                const uint32_t dY = (s.uv[c % kUv].cv.factored ? kColY : kColYo) + 64 * (c & 1);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16_ss(tbase + dY, dC + kmaj(k), dHs + 128 * k, kIdY, k > 0);
+                mma_commit(&s.g3);
+                return true;
+            };
+            auto load_z = [&](int c) {
+                mbar_arrive_expect_tx(&s.full_z[c & 1], Q * 64 * 2);
+                tma_load_3d(s.Zt[c & 1], &map_z, &s.full_z[c & 1], unit_h(c) * P, 0, unit_b(c));
+                loaded_z = c + 1;
+            };
+            if (has_z) {
+                prefetch_tmap(&map_z);
+                load_z(0);
+                if (nu > 1) load_z(1);
+            }
+            load_c(0);
+            load_b(0);
+            bool ok = wait_or_abort(s, &s.full_c, 0, wlim) && wait_or_abort(s, &s.full_b, 0, wlim);
+            if (ok) {
+                tc_fence_after();
+                g1();
+                ok = g3(0);
+            }
+            for (int c = 0; c < nu && ok; ++c) {
+                const int kb = c & 1;
+                ok = wait_or_abort(s, &s.xready, c & 1, wlim) && wait_or_abort(s, &s.hsready, c & 1, wlim);
+                if (!ok) break;
+                if (c + 2 < nu) load_x(c + 2);
+                tc_fence_after();
+                {
+                    const uint64_t dA = sdesc_sw128(smem_u32(s.B), Q * 128, 1024);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mma_bf16_ss(tbase + kColDH, dA + 128 * k, (kb ? dXS1 : dXS0) + 128 * k, kIdState, k > 0);
+                    mma_commit(&s.g4);
+                }
+                if (c + 1 < nu) {
+                    ok = wait_or_abort(s, &s.g4, c & 1, wlim);
+                    if (!ok) break;
+                    load_c(c + 1);
+                    load_b(c + 1);
+                }
+                ok = wait_or_abort(s, &s.mready, c & 1, wlim);
+                if (!ok) break;
+                if (has_z && c >= 1 && c + 1 < nu) load_z(c + 1);
+                tc_fence_after();
+                {
+                    const bool fac = s.uv[c % kUv].cv.factored != 0;
+                    const uint64_t dB = fac ? (kb ? dXS1 : dXS0) : (kb ? dXR1 : dXR0);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mma_bf16_ts(tbase + kColY + 64 * kb, tbase + kColM + 8 * k, dB + 128 * k, kIdY,
+                                    fac || k > 0);
+                    mma_commit(&s.g2);
+                }
+                if (c + 1 < nu) {
+                    ok = wait_or_abort(s, &s.full_c, (c + 1) & 1, wlim) &&
+                         wait_or_abort(s, &s.full_b, (c + 1) & 1, wlim);
+                    if (!ok) break;
+                    tc_fence_after();
+                    g1();
+                    ok = g3(c + 1);
+                    if (!ok) break;
+                }
+            }
+            if (!ok) set_abort(s);
+            mma_commit(&s.fin);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_test(&s.fin, 0) && globaltimer_ns() - t0 < kWaitNs) __nanosleep(64);
+            if (loaded_c > 0) {
+                const int k = loaded_c - 1;
+                while (!mbar_test(&s.full_c, k & 1) && globaltimer_ns() - t0 < kWaitNs) __nanosleep(64);
+            }
+            if (loaded_b > 0) {
+                const int k = loaded_b - 1;
+                while (!mbar_test(&s.full_b, k & 1) && globaltimer_ns() - t0 < kWaitNs) __nanosleep(64);
+            }
+            for (int k = max(0, loaded_x - 2); k < loaded_x; ++k)
+                while (!mbar_test(&s.full_x[k & 1], (k >> 1) & 1) && globaltimer_ns() - t0 < kWaitNs)
+                    __nanosleep(64);
+            for (int k = max(0, loaded_z - 2); k < loaded_z; ++k)
+                while (!mbar_test(&s.full_z[k & 1], (k >> 1) & 1) && globaltimer_ns() - t0 < kWaitNs)
+                    __nanosleep(64);
+        } else if (lane == 0) {
+            griddep_wait();
+        }
+    } else if (warp == kGammaWarp) {
+        // ===================== gamma: per-unit values (one warp) =====================
+        // scan_tc_kernel's per-chunk values, and the unit's head scalars, conv
+        // taps (lane = channel pair) and conv halo; up to kUv units ahead
+        const bool softplus = (p.flags & kDtSoftplus) != 0;
+        const __nv_bfloat16* cs = static_cast<const __nv_bfloat16*>(p.conv_state_in);
+        for (int c = 0; c < nu; ++c) {
+            const int b = unit_b(c), h = unit_h(c);
+            const float Ah = p.A[h];
+            const float bias = p.dt_bias ? p.dt_bias[h] : 0.0f;
+            const float Dh = p.D ? p.D[h] : 0.0f;
+            const float Dabs = fabsf(Dh);
+            float dtn[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = 4 * lane + i;
+                dtn[i] = r < S ? p.dt[((size_t)b * S + r) * H + h] : 0.0f;
+            }
+            float w4[2][kMaxW] = {}, b2[2] = {};
+            if (p.conv) {
+                for (int e = 0; e < 2; ++e) {
+                    for (int k = 0; k < W; ++k) w4[e][kMaxW - W + k] = p.conv_w[(size_t)(h * P + 2 * lane + e) * W + k];
+                    if (p.conv_b) b2[e] = p.conv_b[h * P + 2 * lane + e];
+                }
+            }
+            uint32_t hal[kMaxW - 1];  // two channels of each halo row
+#pragma unroll
+            for (int i = 0; i < kMaxW - 1; ++i) {
+                const int sr = i - (kMaxW - 1) + W - 1;  // row of the conv state
+                hal[i] = (cs != nullptr && sr >= 0)
+                             ? *reinterpret_cast<const uint32_t*>(cs + ((size_t)b * (W - 1) + sr) * Cdim + h * P + 2 * lane)
+                             : 0u;
+            }
+            const int rows = S;
+            float dt[4];
+            bool dt_ok = true;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float d = softplus ? softplus_f32(dtn[i] + bias) : dtn[i];
+                const bool valid = 4 * lane + i < rows;
+                dt[i] = valid ? d : 0.0f;
+                dt_ok = dt_ok && (!valid || (dt[i] > 0.0f && Dabs < dt[i] * 1e30f));
+            }
+            float gh[4], gl[4];
+            gh[0] = dt[0] * Ah;
+            gl[0] = 0.0f;
+#pragma unroll
+            for (int i = 1; i < 4; ++i) {
+                gh[i] = gh[i - 1];
+                gl[i] = gl[i - 1];
+                df_add(gh[i], gl[i], dt[i] * Ah, 0.0f);
+            }
+            float th = gh[3], tl = gl[3];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const float oh = __shfl_up_sync(0xffffffffu, th, d);
+                const float ol = __shfl_up_sync(0xffffffffu, tl, d);
+                if (lane >= d) df_add(th, tl, oh, ol);
+            }
+            float eh = __shfl_up_sync(0xffffffffu, th, 1);
+            float el = __shfl_up_sync(0xffffffffu, tl, 1);
+            if (lane == 0) eh = el = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) df_add(gh[i], gl[i], eh, el);
+            float o_h[4], o_l[4], o_sc[4], o_vb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) df_to_log2(gh[i], gl[i], o_h[i], o_l[i]);
+            const float gLh = __shfl_sync(0xffffffffu, o_h[3], 31);
+            const float gLl = __shfl_sync(0xffffffffu, o_l[3], 31);
+            const bool factored = __all_sync(0xffffffffu, dt_ok) && Ah <= 0.0f && gLh + gLl >= kFactorMinLog2;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                o_sc[i] = factored ? ex2_fast(-(o_h[i] + o_l[i])) * dt[i]
+                                   : ex2_fast(fminf((gLh - o_h[i]) + (gLl - o_l[i]), 0.0f)) * dt[i];
+            }
+            int split_bits = 0;
+            if (!factored) {
+                const int l0 = lane & ~7;
+                const float gfh = __shfl_sync(0xffffffffu, o_h[0], l0), gfl = __shfl_sync(0xffffffffu, o_l[0], l0);
+                const float gmh = __shfl_sync(0xffffffffu, o_h[0], l0 + 4), gml = __shfl_sync(0xffffffffu, o_l[0], l0 + 4);
+                const float geh = __shfl_sync(0xffffffffu, o_h[3], l0 + 7), gel = __shfl_sync(0xffffffffu, o_l[3], l0 + 7);
+                bool lane_ok = Ah <= 0.0f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    lane_ok = lane_ok && (4 * lane + i >= rows || (dt[i] > 0.0f && Dabs < dt[i] * 0x1p60f));
+                lane_ok = lane_ok && (gfh - gmh) + (gfl - gml) <= kSplitMaxLog2 &&
+                          (gmh - geh) + (gml - gel) <= kSplitMaxLog2;
+                const bool mono = __all_sync(0xffffffffu, Ah <= 0.0f && dt[0] >= 0.0f && dt[1] >= 0.0f &&
+                                                              dt[2] >= 0.0f && dt[3] >= 0.0f);
+                const unsigned blk_ok = __ballot_sync(0xffffffffu, lane_ok);
+                const bool split = mono && ((blk_ok >> l0) & 0xffu) == 0xffu;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) split_bits |= (mono && ((blk_ok >> (8 * k)) & 0xffu) == 0xffu) << k;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o_vb[i] = split ? ex2_fast((gmh - o_h[i]) + (gml - o_l[i])) * dt[i] : 1.0f;
+            }
+            // the slot is free once the epilogue of unit c-kUv is done
+            const bool ok = c < kUv || wait_or_abort(s, &s.epidone[c % kUv], ((c / kUv) - 1) & 1, wlim);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            UnitVals& uv = s.uv[c % kUv];
+            ChunkVals& cv = uv.cv;
+            reinterpret_cast<float4*>(cv.g2h)[lane] = make_float4(o_h[0], o_h[1], o_h[2], o_h[3]);
+            reinterpret_cast<float4*>(cv.g2l)[lane] = make_float4(o_l[0], o_l[1], o_l[2], o_l[3]);
+            reinterpret_cast<float4*>(cv.dts)[lane] = make_float4(dt[0], dt[1], dt[2], dt[3]);
+            reinterpret_cast<float4*>(cv.sc)[lane] = make_float4(o_sc[0], o_sc[1], o_sc[2], o_sc[3]);
+            if (!factored)
+                reinterpret_cast<float4*>(cv.vb)[lane] = make_float4(o_vb[0], o_vb[1], o_vb[2], o_vb[3]);
+#pragma unroll
+            for (int k = 0; k < kMaxW; ++k) uv.wconv[k][lane] = make_float2(w4[0][k], w4[1][k]);
+            uv.bconv[lane] = make_float2(b2[0], b2[1]);
+#pragma unroll
+            for (int i = 0; i < kMaxW - 1; ++i) *reinterpret_cast<uint32_t*>(&uv.halo[i][2 * lane]) = hal[i];
+            if (lane == 0) {
+                cv.decS = ex2_fast(fminf(gLh + gLl, 0.0f));
+                cv.factored = factored;
+                cv.split = split_bits;
+                uv.Dh = Dh;
+            }
+            mbar_arrive(&s.cvready[c % kUv]);
+        }
+    } else {
+        // ===================== compute warps =====================
+        const int q = warp & 3;
+        const int j = warp >> 2;
+        const int t = 32 * q + lane;
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        bool ok = true;
+        const int rq = tid >> 4, jq = tid & 15;
+        auto state_base = [&](int c) { return ((size_t)unit_b(c) * H + unit_h(c)) * P * N; };
+        // conv(c): unit c's x rows and scaled x rows (this thread's 4 x 4 share);
+        // the thread holding rows S-3 .. S-1 also writes them as the x columns
+        // of the unit's new conv state
+        auto conv = [&](int c) {
+            const int rows = S;
+            const UnitVals& uv = s.uv[c % kUv];
+            const ChunkVals& cv = uv.cv;
+            const bool need_x = cv.factored == 0;
+            const float4 sc4 = *reinterpret_cast<const float4*>(&cv.sc[4 * rq]);
+            const float scs[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+            uint2 raw[kRaw];
+#pragma unroll
+            for (int i = 0; i < kRaw; ++i) {
+                const int r = 4 * rq - (kMaxW - 1) + i;
+                if (r >= 0)
+                    raw[i] = at<uint2>(s.XRAW[c & 1], chunk_off(r, jq >> 1) + ((jq & 1) << 3));
+                else
+                    raw[i] = *reinterpret_cast<const uint2*>(&uv.halo[i < kMaxW - 1 ? i : 0][4 * jq]);
+            }
+            if (p.conv_state_out != nullptr && W > 1 && rq == (S - 1) >> 2) {
+                __nv_bfloat16* so = static_cast<__nv_bfloat16*>(p.conv_state_out) +
+                                    (size_t)unit_b(c) * (W - 1) * Cdim + unit_h(c) * P + 4 * jq;
+#pragma unroll
+                for (int i = 0; i < kRaw; ++i) {
+                    const int jj = 4 * rq - (kMaxW - 1) + i - (S - (W - 1));  // row of the new state
+                    if (jj >= 0 && jj < W - 1) *reinterpret_cast<uint2*>(so + (size_t)jj * Cdim) = raw[i];
+                }
+            }
+            float2 acc[4][2];
+            {
+                const float4 bb = *reinterpret_cast<const float4*>(&uv.bconv[2 * jq]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[i][0] = make_float2(bb.x, bb.y);
+                    acc[i][1] = make_float2(bb.z, bb.w);
+                }
+            }
+            if (p.conv) {
+#pragma unroll
+                for (int k = 0; k < kMaxW; ++k) {
+                    const float4 wk = *reinterpret_cast<const float4*>(&uv.wconv[k][2 * jq]);
+                    const float2 w0 = make_float2(wk.x, wk.y), w1 = make_float2(wk.z, wk.w);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[i][0] = __ffma2_rn(w0, unpack2(raw[i + k].x), acc[i][0]);
+                        acc[i][1] = __ffma2_rn(w1, unpack2(raw[i + k].y), acc[i][1]);
+                    }
+                }
+            }
+            const uint32_t coff = (uint32_t)((jq & 1) << 3);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = 4 * rq + i;
+                float2 x0, x1;
+                if (p.conv) {
+                    x0 = silu2(acc[i][0]);
+                    x1 = silu2(acc[i][1]);
+                } else {
+                    x0 = unpack2(raw[kMaxW - 1 + i].x);
+                    x1 = unpack2(raw[kMaxW - 1 + i].y);
+                }
+                if (r >= rows) x0 = x1 = make_float2(0.f, 0.f);
+                const float2 sc2 = make_float2(scs[i], scs[i]);
+                const uint32_t off = chunk_off(r, jq >> 1) + coff;
+                if (need_x) {
+                    const float vbi = cv.vb[4 * rq + i];
+                    const float2 vb2 = make_float2(vbi, vbi);
+                    at<uint2>(s.XR[c & 1], off) = make_uint2(pack2(__fmul2_rn(vb2, x0)), pack2(__fmul2_rn(vb2, x1)));
+                }
+                at<uint2>(s.XS[c & 1], off) = make_uint2(pack2(__fmul2_rn(sc2, x0)), pack2(__fmul2_rn(sc2, x1)));
+            }
+        };
+
+        // -- state share: column n = t, p = 16 j .. 16 j + 15 --
+        float2 hreg[8];
+        auto load_h = [&](int c) {  // unit c's initial state (zeros without one)
+            const size_t sb = state_base(c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                hreg[i] = p.h0 ? make_float2(p.h0[sb + (size_t)(16 * j + 2 * i) * N + t],
+                                             p.h0[sb + (size_t)(16 * j + 2 * i + 1) * N + t])
+                               : make_float2(0.f, 0.f);
+        };
+        auto store_h = [&]() {
+            at<uint4>(s.Hs, chunk_off(t, 2 * j)) = pack4x2(&hreg[0]);
+            at<uint4>(s.Hs, chunk_off(t, 2 * j + 1)) = pack4x2(&hreg[4]);
+        };
+
+        if (nu > 0) load_h(0);
+        store_h();
+        fence_proxy_async_smem();
+        mbar_arrive(&s.hsready);
+        if (j > q) {
+            uint32_t zero[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) zero[i] = 0u;
+            tmem_st16(tbase + lane_off + kColM + 16 * j, zero);
+            tmem_st_wait();
+        }
+        if (nu > 0) {
+            ok = wait_or_abort(s, &s.cvready[0], 0, wlim) && wait_or_abort(s, &s.full_x[0], 0, wlim);
+            if (ok) conv(0);
+            fence_proxy_async_smem();
+            mbar_arrive(&s.xready);
+        }
+
+        for (int c = 0; c < nu; ++c) {
+            const int rows = S;
+            const int kb = c & 1;
+            const UnitVals& uv = s.uv[c % kUv];
+            const ChunkVals& cv = uv.cv;
+            const float Dh = uv.Dh;
+
+            // ---- mask(c) ----
+            const bool fac = cv.factored != 0;
+            if (ok) ok = wait_or_abort(s, &s.g1, c & 1, wlim);
+            if (__all_sync(0xffffffffu, ok)) {
+                if (j <= q) {
+                    tc_fence_after();
+                    const bool split = !fac && ((cv.split >> j) & 1);
+                    const float dts_t = cv.dts[t];
+                    float g2h_t = 0.0f, g2l_t = 0.0f, rt = 1.0f;
+                    if (!fac) {
+                        g2h_t = cv.g2h[t];
+                        g2l_t = cv.g2l[t];
+                        if (split)
+                            rt = ex2_fast((g2h_t - cv.g2h[32 * j + 16]) + (g2l_t - cv.g2l[32 * j + 16]));
+                    }
+                    const float diag = (j == q && t < rows)
+                                           ? (fac ? __fdividef(Dh, dts_t) : split ? __fdividef(Dh * rt, dts_t) : Dh)
+                                           : 0.0f;
+#pragma unroll 1
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int c0 = 32 * j + 16 * hf;
+                        float v[16];
+                        tmem_ld16(tbase + lane_off + kColCB + c0, v);
+                        tmem_ld_wait();
+                        if (split) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] *= rt;
+                        } else if (!fac) {
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const int sb = c0 + 4 * q4;
+                                const float4 gh = *reinterpret_cast<const float4*>(&cv.g2h[sb]);
+                                const float4 gl = *reinterpret_cast<const float4*>(&cv.g2l[sb]);
+                                const float4 ds = *reinterpret_cast<const float4*>(&cv.dts[sb]);
+                                const float ghs[4] = {gh.x, gh.y, gh.z, gh.w}, gls[4] = {gl.x, gl.y, gl.z, gl.w};
+                                const float dss[4] = {ds.x, ds.y, ds.z, ds.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float ex = (g2h_t - ghs[e]) + (g2l_t - gls[e]);
+                                    v[4 * q4 + e] = v[4 * q4 + e] * dss[e] * ex2_fast(fminf(ex, 0.0f));
+                                }
+                            }
+                        }
+                        if (j == q) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                v[e] = (c0 + e < t) ? v[e] : (c0 + e == t ? v[e] + diag : 0.0f);
+                        }
+                        uint32_t m[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) m[e] = pack2(make_float2(v[2 * e], v[2 * e + 1]));
+                        tmem_st8(tbase + lane_off + kColM + 16 * j + 8 * hf, m);
+                    }
+                    tmem_st_wait();
+                }
+            } else {
+                ok = false;
+            }
+            if (j == 0 && lane == 0 && c > 0) bulk_wait_read_all();
+            tc_fence_before();
+            mbar_arrive(&s.mready);
+
+            // ---- state(c): unit c's final state h = decS h0 + b dH to memory; unit
+            // c+1's initial state into the registers and the state tile ----
+            if (ok) ok = wait_or_abort(s, &s.g4, c & 1, wlim) && wait_or_abort(s, &s.g3, c & 1, wlim);
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+                const float2 dS = make_float2(cv.decS, cv.decS);
+                const float2 bS = fac ? dS : make_float2(1.0f, 1.0f);
+                float v[16];
+                tmem_ld16(tbase + kColDH + lane_off + 16 * j, v);
+                tmem_ld_wait();
+                const size_t sb = state_base(c);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 hf = __ffma2_rn(dS, hreg[i], __fmul2_rn(bS, make_float2(v[2 * i], v[2 * i + 1])));
+                    p.hS[sb + (size_t)(16 * j + 2 * i) * N + t] = hf.x;
+                    p.hS[sb + (size_t)(16 * j + 2 * i + 1) * N + t] = hf.y;
+                }
+                if (c + 1 < nu) {
+                    load_h(c + 1);
+                    store_h();
+                }
+                fence_proxy_async_smem();
+            } else {
+                ok = false;
+            }
+            tc_fence_before();
+            mbar_arrive(&s.hsready);
+
+            // ---- conv(c+1) ----
+            if (c + 1 < nu) {
+                if (ok)
+                    ok = wait_or_abort(s, &s.cvready[(c + 1) % kUv], ((c + 1) / kUv) & 1, wlim) &&
+                         wait_or_abort(s, &s.full_x[(c + 1) & 1], ((c + 1) >> 1) & 1, wlim);
+                if (ok) conv(c + 1);
+                fence_proxy_async_smem();
+                mbar_arrive(&s.xready);
+            }
+
+            // ---- epilogue(c) ----
+            if (ok) ok = wait_or_abort(s, &s.g2, c & 1, wlim);
+            if (ok && has_z) ok = wait_or_abort(s, &s.full_z[kb], (c >> 1) & 1, wlim);
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+                const float dec = ex2_fast(fminf(cv.g2h[t] + cv.g2l[t], 0.0f));
+                const float2 dd = make_float2(dec, dec);
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    float yv[8];
+                    tmem_ld8(tbase + kColY + 64 * kb + lane_off + 16 * j + 8 * hh, yv);
+                    if (!fac) {
+                        float yo[8];
+                        tmem_ld8(tbase + kColYo + 64 * kb + lane_off + 16 * j + 8 * hh, yo);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 8; k += 2) {
+                            const float2 r = __ffma2_rn(dd, make_float2(yo[k], yo[k + 1]),
+                                                        make_float2(yv[k], yv[k + 1]));
+                            yv[k] = r.x;
+                            yv[k + 1] = r.y;
+                        }
+                    } else {
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 8; k += 2) {
+                            const float2 r = __fmul2_rn(dd, make_float2(yv[k], yv[k + 1]));
+                            yv[k] = r.x;
+                            yv[k + 1] = r.y;
+                        }
+                    }
+                    float2 out[4], zv[4];
+                    const uint32_t off = chunk_off(t, 2 * j + hh);
+                    if (has_z) unpack4x2(at<uint4>(s.Zt[kb], off), zv);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float2 v = make_float2(yv[2 * e], yv[2 * e + 1]);
+                        if (has_z) v = __fmul2_rn(v, silu2(zv[e]));
+                        out[e] = v;
+                    }
+                    at<uint4>(s.Zt[kb], off) = pack4x2(out);
+                }
+            } else {
+                ok = false;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&s.epidone[c % kUv]);
+            named_bar_sync(1 + q, 128);
+            if (j == 0 && lane == 0 && ok && 32 * q < S) {
+                tma_store_3d(&map_y, reinterpret_cast<const char*>(s.Zt[kb]) + q * 32 * 128, unit_h(c) * P,
+                             32 * q, unit_b(c));
+                bulk_commit();
+            }
+            // the B|C columns of the new conv state, from the first head of a group
+            // (read from memory: these rows are not in shared memory)
+            if (p.conv_state_out != nullptr && W > 1 && unit_h(c) % hpg == 0 && tid < 2 * N) {
+                const int b = unit_b(c), g = unit_h(c) / hpg;
+                const int col = tid < N ? H * P + g * N + tid : H * P + G * N + g * N + (tid - N);
+                const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(p.xbc);
+                const __nv_bfloat16* si = static_cast<const __nv_bfloat16*>(p.conv_state_in);
+                __nv_bfloat16* so = static_cast<__nv_bfloat16*>(p.conv_state_out);
+                const int nh = W - 1;
+                for (int jj = 0; jj < nh; ++jj) {
+                    const int r = S + jj;
+                    __nv_bfloat16 v;
+                    if (r < nh) v = si ? si[((size_t)b * nh + r) * Cdim + col] : __float2bfloat16_rn(0.0f);
+                    else v = xs[((size_t)b * S + (r - nh)) * Cdim + col];
+                    so[((size_t)b * nh + jj) * Cdim + col] = v;
+                }
+            }
+        }
+        if (j == 0 && lane == 0) bulk_wait_read_all();
+        if (!ok) set_abort(s);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && s.abort) atomicOr(p.err, kErrTimeout);
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
 // ---- host side ------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -1070,6 +1749,42 @@ bool make_map(CUtensorMap* m, const void* base, int cols, int S, int B, int box_
 }  // namespace
 
 bool scan_tc_supports(int P_, int N_) { return P_ == P && N_ == N; }
+
+bool scan_units_supports(const TcScanParams& p)
+{
+    return p.cu_seqlens == nullptr && p.norm_ss == nullptr && p.S >= 1 && p.S <= Q && p.W <= kMaxW;
+}
+
+cudaError_t launch_scan_units(const TcScanParams& p, cudaStream_t st, bool after_prepass)
+{
+    if (p.B == 0) return cudaSuccess;
+    if (!scan_units_supports(p) || !encode_fn()) return cudaErrorNotSupported;
+    const int Cdim = p.H * P + 2 * p.G * N;
+    CUtensorMap mbc, mz, my, mx;
+    if (!make_map(&mbc, p.bc, p.bc_stride, p.S, p.B) || !make_map(&my, p.y, p.H * P, p.S, p.B, 32) ||
+        !make_map(&mx, p.xbc, Cdim, p.S, p.B))
+        return cudaErrorInvalidValue;
+    memset(&mz, 0, sizeof(mz));
+    if ((p.flags & kHasZ) && !make_map(&mz, p.z, p.H * P, p.S, p.B)) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(scan_units_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kUnitSmemBytes);
+    if (e != cudaSuccess) return e;
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const long long units = (long long)p.B * p.H;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(units < nsm ? units : nsm));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kUnitSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_prepass ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, scan_units_kernel, mbc, mz, my, mx, p);
+}
 
 cudaError_t launch_scan_tc(const TcScanParams& p, cudaStream_t st, bool after_prepass)
 {

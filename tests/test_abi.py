@@ -150,7 +150,7 @@ def test_workspace_size_query(lib):
 def test_workspace_size_follows_the_routing(lib):
     """Scratch is the post-conv B|C rows, [B, S, 2 G N] bf16 rounded up to 256
     bytes, and only where the call takes the tensor-core path with the conv
-    fused (bf16, P = 64, N = 128, W <= 4, more than 4 rows per call)."""
+    fused (bf16, P = 64, N = 128, W <= 4, rows in the call)."""
     flags = ssd.SSD_DT_SOFTPLUS | ssd.SSD_HAS_Z
     tc = dict(headdim=64, dstate=128)
     size = lambda act, fused, **kw: ssd.ssd_chunk_scan_workspace_size(_d(**{**tc, **kw}), act,
@@ -159,10 +159,10 @@ def test_workspace_size_follows_the_routing(lib):
     assert size(ssd.SSD_BF16, True, seqlen=2048, nheads=128, ngroups=8) == 2048 * 2 * 8 * 128 * 2
     # ragged sizes round up to 256 bytes
     assert size(ssd.SSD_BF16, True, batch=3, seqlen=5, ngroups=1) == (3 * 5 * 2 * 128 * 2 + 255) // 256 * 256
-    # no scratch: conv not fused, fp32 (row-exact kernel), short calls, other shapes
+    # no scratch: conv not fused, fp32 (row-exact kernel), no rows, other shapes
     assert size(ssd.SSD_BF16, False, seqlen=2048) == 0
     assert size(ssd.SSD_F32, True, seqlen=2048) == 0
-    assert size(ssd.SSD_BF16, True, seqlen=4) == 0
+    assert size(ssd.SSD_BF16, True, seqlen=0) == 0
     assert size(ssd.SSD_BF16, True, seqlen=2048, headdim=32) == 0
     assert size(ssd.SSD_BF16, True, seqlen=2048, conv_width=5) == 0
 

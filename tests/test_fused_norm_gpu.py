@@ -111,11 +111,11 @@ def test_fused_gated_norm_matches_oracle(B, S, splits, conv):
                  what="fused against scan, then norm")
 
 
-@pytest.mark.parametrize("act,S", [(torch.float32, 37), (torch.bfloat16, 3)])
-def test_fused_gated_norm_on_the_row_exact_kernel(act, S):
-    """fp32, and bf16 calls of at most 4 rows: the scan without the gate, then
-    the norm in place, behind the same call."""
-    shape = si.Shape(batch=2, seqlen=S, nheads=8, headdim=64, dstate=128, ngroups=2)
+@pytest.mark.parametrize("act,S,P", [(torch.float32, 37, 64), (torch.bfloat16, 3, 32)])
+def test_fused_gated_norm_on_the_row_exact_kernel(act, S, P):
+    """fp32, and bf16 heads of 32 channels (not the tensor-core shape): the
+    scan without the gate, then the norm in place, behind the same call."""
+    shape = si.Shape(batch=2, seqlen=S, nheads=8, headdim=P, dstate=128, ngroups=2)
     cpu, dev = make_problem(shape, act=act, seed=4, with_z=True)
     w = _weights(shape.nheads * shape.headdim, seed=6)
     before = ssd.ssd_launch_counts()

@@ -149,6 +149,21 @@ def test_prefill_137_rows_every_element():
     check_prefill_every_element(shape, cpu, y, h, cs, torch.bfloat16)
 
 
+@pytest.mark.parametrize("B,S", [(3, 100), (2, 5), (4, 128), (1, 77)])
+def test_short_calls_several_units_per_cta_every_element(B, S):
+    """Calls of at most 128 rows run on the kernel whose CTAs walk several
+    (sequence, head) units each: 128 heads x B sequences over the SMs, so most
+    CTAs take two or more units (one at B = 1).  Every element of y and of the
+    final states against the oracle, the conv state bit for bit."""
+    shape = si.PREFILL.with_(batch=B, seqlen=S)
+    cpu, dev = make_problem(shape, act=torch.bfloat16, seed=17 + S)
+    before = ssd.ssd_launch_counts()
+    y, h, cs = gpu_prefill(shape, dev)
+    after = ssd.ssd_launch_counts()
+    assert after["scan_tc"] - before["scan_tc"] == 1 and after["scan_simt"] == before["scan_simt"]
+    check_prefill_every_element(shape, cpu, y, h, cs, torch.bfloat16)
+
+
 @pytest.mark.parametrize("splits", [[129, 130, 258], [1, 128, 2, 386]])
 def test_calls_whose_last_chunk_is_short_chain_their_conv_state(splits):
     """Calls whose last chunk holds 1 or 2 rows: the new conv state (the last
@@ -262,16 +277,16 @@ def test_bf16_runs_on_tensor_cores():
     _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
 
 
-def test_bf16_short_calls_take_row_exact_kernel():
-    """Calls of up to 4 rows run the row-exact kernel (cheaper than filling the
-    chunk pipeline); 5 rows and more run on the tensor cores."""
-    shape = si.Shape(batch=2, seqlen=9, nheads=8, headdim=64, dstate=128, ngroups=2)
+def test_bf16_calls_of_a_few_rows_run_on_tensor_cores():
+    """Calls of 1 to 5 rows run on the tensor cores too (their units walk the
+    chunk pipeline several per CTA), chained into one sequence."""
+    shape = si.Shape(batch=2, seqlen=12, nheads=8, headdim=64, dstate=128, ngroups=2)
     cpu, dev = make_problem(shape, act=torch.bfloat16, seed=4)
     c0 = _counts()
-    y, h, cs = gpu_prefill(shape, dev, [4, 5])
+    y, h, cs = gpu_prefill(shape, dev, [1, 2, 4, 5])
     torch.cuda.synchronize()
     c1 = _counts()
-    assert c1["scan_simt"] - c0["scan_simt"] == 1 and c1["scan_tc"] - c0["scan_tc"] == 1
+    assert c1["scan_tc"] - c0["scan_tc"] == 4 and c1["scan_simt"] == c0["scan_simt"]
     _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
 
 
