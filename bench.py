@@ -371,6 +371,9 @@ def bench_ours(args):
     if args.only == "tail":  # profiling runs: the scan + gated norm calls alone
         tail = {"mixer_tail_2048": bench_mixer_tail(ssd, dev, stream, si.PREFILL, steps=args.steps)}
         return {"metric": "mixer_tail", **tail} if rank == 0 else None
+    if args.only == "stress":  # profiling runs: the decay-stress passes alone
+        st = {"stress_4x4096_calls_1_to_128": bench_stress(ssd, dev, stream, steps=args.steps)}
+        return {"metric": "stress", **st} if rank == 0 else None
     if args.only == "prefill":  # profiling runs: the 2048-row calls alone
         p2048, _ = bench_prefill_2048(ssd, dev, stream, world, rank, args)
         return {"metric": "prefill_2048", "prefill_2048": p2048} if rank == 0 else None
@@ -591,39 +594,41 @@ def chained_calls(ssd, shape, prm, inp, splits, device):
     return run, len(calls)
 
 
+def bench_stress(ssd, dev, stream, steps):
+    """The decay-stress workload: 4 x 4096 rows with decays up to ~1e4 per
+    row, fed as chained calls of U{1..128} rows (seeded splits); tokens/s
+    over all calls of one pass."""
+    shape, splits = si.STRESS, si.random_splits(si.STRESS.seqlen, 5)
+    prm = {k: v.to(dev) for k, v in si.params(shape, seed=11, stress=True).items()}
+    inp = si.prefill_inputs(shape, seed=12, device=dev, stress=True)
+    run, ncalls = chained_calls(ssd, shape, prm, inp, splits, dev)
+    host_s = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        run(stream)
+        host_s.append(time.perf_counter() - t0)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    queue_ahead(min(host_s), steps)
+    ev0.record(stream)
+    for _ in range(steps):
+        run(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    rows = shape.batch * shape.seqlen
+    return {"tokens_per_s": round(rows / (ms / 1e3), 1), "ms_per_pass": round(ms, 4),
+            "calls_per_pass": ncalls, "rows_per_pass": rows,
+            "host_ms_per_pass": round(min(host_s) * 1e3, 3)}
+
+
 def bench_extra(ssd, dev, stream, args):
     """The other workloads, timed like the headline one: decay stress (4 x
     4096 rows with decays up to ~1e4 per row, fed as calls of U{1..128} rows),
     tokens/s over all calls of one pass; 16 packed sequences at pool slots
     (one ssd_chunk_scan_varlen call); and the gated group RMSNorm at the
     prefill width, GB/s against the HBM peak."""
-    out = {}
-    for name, shape, splits, stress in (
-            ("stress_4x4096_calls_1_to_128", si.STRESS, si.random_splits(si.STRESS.seqlen, 5),
-             True),):
-        prm = {k: v.to(dev) for k, v in si.params(shape, seed=11, stress=stress).items()}
-        inp = si.prefill_inputs(shape, seed=12, device=dev, stress=stress)
-        run, ncalls = chained_calls(ssd, shape, prm, inp, splits, dev)
-        host_s = []
-        for _ in range(3):
-            t0 = time.perf_counter()
-            run(stream)
-            host_s.append(time.perf_counter() - t0)
-        torch.cuda.synchronize()
-        steps = 5
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        queue_ahead(min(host_s), steps)
-        ev0.record(stream)
-        for _ in range(steps):
-            run(stream)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        ms = ev0.elapsed_time(ev1) / steps
-        rows = shape.batch * shape.seqlen
-        out[name] = {"tokens_per_s": round(rows / (ms / 1e3), 1), "ms_per_pass": round(ms, 4),
-                     "calls_per_pass": ncalls, "rows_per_pass": rows,
-                     "host_ms_per_pass": round(min(host_s) * 1e3, 3)}
-        del inp, run
+    out = {"stress_4x4096_calls_1_to_128": bench_stress(ssd, dev, stream, steps=5)}
     # packed sequences with states at pool slots: 16 sequences of log-uniform
     # 1..2048 rows (seeded), at slots of a 64-slot pool, a quarter of them fresh
     sh = si.PREFILL
@@ -933,9 +938,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the decay-stress, packed-sequence and gated-norm workloads")
-    ap.add_argument("--only", choices=["all", "long", "prefill", "decode", "tail"], default="all",
+    ap.add_argument("--only", choices=["all", "long", "prefill", "decode", "tail", "stress"],
+                    default="all",
                     help="time only the long-prefill steps, the 2048-row prefill calls, "
-                         "the decode steps or the scan + gated norm calls (profiler runs)")
+                         "the decode steps, the scan + gated norm calls or the decay-stress "
+                         "passes (profiler runs)")
     ap.add_argument("--long-batch", type=int, default=si.LONG.batch,
                     help="sequences of the long workload (8; fewer only to keep profiler "
                          "captures small)")
