@@ -31,7 +31,8 @@ constexpr int kThreads = 512;
 template <typename T, int KT, int RF>
 __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
 {
-    extern __shared__ float sm[];  // x [K][hpg*P] | B [K][N] | C [K][N] | dt, dA [K][hpg]
+    // x [K][hpg*P] | B [K][N] | C [K][N] | dt, dA [K][hpg] | D [hpg] | silu(z) [K][hpg*P]
+    extern __shared__ float sm[];
     const int g = blockIdx.x, i = blockIdx.y;
     const int H = p.H, P = p.P, N = p.N, G = p.G, K = p.K;
     const int hpg = H / G;
@@ -56,6 +57,8 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
     float* Cs = Bs + K * N;         // [K][N]
     float* dts = Cs + K * N;        // [K][hpg]
     float* dAs = dts + K * hpg;     // [K][hpg]
+    float* Ds = dAs + K * hpg;      // [hpg]
+    float* zs = Ds + hpg;           // [K][XW] (with z)
     // conv + SiLU of the group's channels over u = [conv state ; the row's K
     // tokens]: output t reads u rows t .. t+W-1 (the first W-1 rows of u from
     // the slot's conv state, the rest from the row's raw tokens)
@@ -90,11 +93,21 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
         dts[jt] = dt;
         dAs[jt] = expf(dt * p.A[h]);
     }
+    // the skip weights and the gate, so that no global load waits in the
+    // state loop below
+    for (int j = threadIdx.x; j < hpg; j += blockDim.x) Ds[j] = p.D ? p.D[h0 + j] : 0.0f;
+    if (p.flags & kHasZ) {
+        const T* zz = static_cast<const T*>(p.z);
+        for (int e = threadIdx.x; e < K * XW; e += blockDim.x) {
+            const int t = e / XW, c = e % XW;
+            const float zv = to_f32(zz[((size_t)i * K + t) * H * P + h0 * P + c]);
+            zs[e] = zv / (1.0f + expf(-zv));
+        }
+    }
     __syncthreads();
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
     const int nv = N / 4;  // float4 per state row
-    const T* zz = static_cast<const T*>(p.z);
     T* y = static_cast<T*>(p.y);
     const int nrows = hpg * P;  // state rows of this group, head-major
     float4* st0 = reinterpret_cast<float4*>(p.pool + ((size_t)s * H + h0) * (size_t)P * N);
@@ -165,11 +178,8 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
         if ((lane & (32 / (RF * KT) - 1)) == 0 && tt < K) {
             const int row = r0 + rr;         // j * P + pp
             const int h = h0 + j, pp = row % P;
-            float yv = fmaf(p.D ? p.D[h] : 0.0f, xs[tt * XW + row], acc[0]);
-            if (p.flags & kHasZ) {
-                const float zv = to_f32(zz[((size_t)i * K + tt) * H * P + h * P + pp]);
-                yv *= zv / (1.0f + expf(-zv));
-            }
+            float yv = fmaf(Ds[j], xs[tt * XW + row], acc[0]);
+            if (p.flags & kHasZ) yv *= zs[tt * XW + row];
             y[(((size_t)i * K + tt) * H + h) * P + pp] = from_f32<T>(yv);
         }
     }
@@ -200,7 +210,8 @@ __global__ void decode_conv_roll_kernel(DecodeParams p)
 size_t decode_smem_bytes(const DecodeParams& p)
 {
     const int hpg = p.H / p.G;
-    return sizeof(float) * (size_t)p.K * ((size_t)hpg * p.P + 2 * (size_t)p.N + 2 * (size_t)hpg);
+    const size_t zb = (p.flags & kHasZ) ? (size_t)hpg * p.P : 0;
+    return sizeof(float) * ((size_t)p.K * ((size_t)hpg * p.P + 2 * (size_t)p.N + 2 * (size_t)hpg + zb) + hpg);
 }
 
 template <typename T, int KT, int RF>
