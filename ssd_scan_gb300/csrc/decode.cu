@@ -61,29 +61,30 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
     float* zs = Ds + hpg;           // [K][XW] (with z)
     // conv + SiLU of the group's channels over u = [conv state ; the row's K
     // tokens]: output t reads u rows t .. t+W-1 (the first W-1 rows of u from
-    // the slot's conv state, the rest from the row's raw tokens)
-    for (int c = threadIdx.x; c < CH; c += blockDim.x) {
+    // the slot's conv state, the rest from the row's raw tokens).  A thread per
+    // (channel, token) output, so a row's K tokens spread over the CTA.
+    for (int it = threadIdx.x; it < CH * K; it += blockDim.x) {
+        const int c = it % CH, t = it / CH;
         const int gc = c < XW ? h0 * P + c
                               : (c < XW + N ? H * P + g * N + (c - XW)
                                             : H * P + G * N + g * N + (c - XW - N));
         float* dst = c < XW ? xs + c : (c < XW + N ? Bs + (c - XW) : Cs + (c - XW - N));
         const int ld = c < XW ? XW : N;  // row stride of dst
-        for (int t = 0; t < K; ++t) {
-            float v;
-            if (p.conv_w) {
-                v = p.conv_b ? p.conv_b[gc] : 0.0f;
-                for (int k = 0; k < p.W; ++k) {
-                    const int u = t + k;
-                    const float xv = u < HW ? to_f32(cpool[((size_t)s * HW + u) * Cdim + gc])
-                                            : to_f32(xbc[((size_t)i * K + (u - HW)) * Cdim + gc]);
-                    v = fmaf(p.conv_w[(size_t)gc * p.W + k], xv, v);
-                }
-                v = v / (1.0f + expf(-v));
-            } else {
-                v = to_f32(xbc[((size_t)i * K + t) * Cdim + gc]);
+        float v;
+        if (p.conv_w) {
+            v = p.conv_b ? p.conv_b[gc] : 0.0f;
+#pragma unroll 4
+            for (int k = 0; k < p.W; ++k) {
+                const int u = t + k;
+                const float xv = u < HW ? to_f32(cpool[((size_t)s * HW + u) * Cdim + gc])
+                                        : to_f32(xbc[((size_t)i * K + (u - HW)) * Cdim + gc]);
+                v = fmaf(p.conv_w[(size_t)gc * p.W + k], xv, v);
             }
-            dst[t * ld] = v;
+            v = v / (1.0f + expf(-v));
+        } else {
+            v = to_f32(xbc[((size_t)i * K + t) * Cdim + gc]);
         }
+        dst[t * ld] = v;
     }
     for (int jt = threadIdx.x; jt < K * hpg; jt += blockDim.x) {
         const int t = jt / hpg, j = jt % hpg;
