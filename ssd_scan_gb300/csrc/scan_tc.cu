@@ -1302,12 +1302,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int r = 4 * lane + i;
                 dtn[i] = r < S ? p.dt[((size_t)b * S + r) * H + h] : 0.0f;
             }
-            float w4[2][kMaxW] = {}, b2[2] = {};
-            if (p.conv) {
-                for (int e = 0; e < 2; ++e) {
-                    for (int k = 0; k < W; ++k) w4[e][kMaxW - W + k] = p.conv_w[(size_t)(h * P + 2 * lane + e) * W + k];
-                    if (p.conv_b) b2[e] = p.conv_b[h * P + 2 * lane + e];
+            // taps front-padded to kMaxW (slot k holds tap k - (kMaxW - W)), indexed
+            // statically so that they stay in registers
+            float w4[2][kMaxW], b2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+#pragma unroll
+                for (int k = 0; k < kMaxW; ++k) {
+                    const int kk = k - (kMaxW - W);
+                    w4[e][k] = p.conv && kk >= 0 ? p.conv_w[(size_t)(h * P + 2 * lane + e) * W + kk] : 0.0f;
                 }
+                b2[e] = p.conv && p.conv_b ? p.conv_b[h * P + 2 * lane + e] : 0.0f;
             }
             uint32_t hal[kMaxW - 1];  // two channels of each halo row
 #pragma unroll
@@ -1690,13 +1695,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __nv_bfloat16* si = static_cast<const __nv_bfloat16*>(p.conv_state_in);
                 __nv_bfloat16* so = static_cast<__nv_bfloat16*>(p.conv_state_out);
                 const int nh = W - 1;
-                for (int jj = 0; jj < nh; ++jj) {
+                // every row read before any is written (one memory round trip; the
+                // state may be updated in place)
+                __nv_bfloat16 v[kMaxW - 1];
+#pragma unroll
+                for (int jj = 0; jj < kMaxW - 1; ++jj) {
                     const int r = S + jj;
-                    __nv_bfloat16 v;
-                    if (r < nh) v = si ? si[((size_t)b * nh + r) * Cdim + col] : __float2bfloat16_rn(0.0f);
-                    else v = xs[((size_t)b * S + (r - nh)) * Cdim + col];
-                    so[((size_t)b * nh + jj) * Cdim + col] = v;
+                    v[jj] = __float2bfloat16_rn(0.0f);
+                    if (jj < nh) {
+                        if (r >= nh) v[jj] = xs[((size_t)b * S + (r - nh)) * Cdim + col];
+                        else if (si) v[jj] = si[((size_t)b * nh + r) * Cdim + col];
+                    }
                 }
+#pragma unroll
+                for (int jj = 0; jj < kMaxW - 1; ++jj)
+                    if (jj < nh) so[((size_t)b * nh + jj) * Cdim + col] = v[jj];
             }
         }
         if (j == 0 && lane == 0) bulk_wait_read_all();
