@@ -1008,22 +1008,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             __nv_bfloat16* so = static_cast<__nv_bfloat16*>(p.conv_state_out);
             const int nh = W - 1;
             const int L = nchunks - 1;  // the last chunk: its raw x tile and the 4 rows before it
-            for (int jj = 0; jj < nh; ++jj) {
+            // every row read before any is written (one memory round trip)
+            __nv_bfloat16 v[kMaxW - 1];
+#pragma unroll
+            for (int jj = 0; jj < kMaxW - 1; ++jj) {
                 const int r = S + jj;  // row of [conv state ; rows]
                 const int rr = r - nh;  // the same row of this call's rows
-                __nv_bfloat16 v;
-                if (rr < 0) {
-                    v = si ? si[((size_t)slot * nh + r) * Cdim + col] : __float2bfloat16_rn(0.0f);
+                v[jj] = __float2bfloat16_rn(0.0f);
+                if (jj >= nh) {
+                } else if (rr < 0) {
+                    if (si) v[jj] = si[((size_t)slot * nh + r) * Cdim + col];
                 } else if (tid < P && L >= 0 && (rr >= L * Q || L > 0)) {
                     // this head's x columns: from the raw tiles still in shared memory
-                    v = rr >= L * Q
-                            ? at<__nv_bfloat16>(s.XRAW[L & 1], chunk_off(rr - L * Q, tid >> 3) + (uint32_t)(tid & 7) * 2)
-                            : at<__nv_bfloat16>(s.XH[L & 1], (uint32_t)((rr - L * Q + 4) * 128 + tid * 2));
+                    v[jj] = rr >= L * Q
+                                ? at<__nv_bfloat16>(s.XRAW[L & 1], chunk_off(rr - L * Q, tid >> 3) + (uint32_t)(tid & 7) * 2)
+                                : at<__nv_bfloat16>(s.XH[L & 1], (uint32_t)((rr - L * Q + 4) * 128 + tid * 2));
                 } else {
-                    v = xs[((size_t)row0 + rr) * Cdim + col];
+                    v[jj] = xs[((size_t)row0 + rr) * Cdim + col];
                 }
-                so[((size_t)slot * nh + jj) * Cdim + col] = v;
             }
+#pragma unroll
+            for (int jj = 0; jj < kMaxW - 1; ++jj)
+                if (jj < nh) so[((size_t)slot * nh + jj) * Cdim + col] = v[jj];
         }
     }
 
