@@ -177,6 +177,29 @@ def test_calls_whose_last_chunk_is_short_chain_their_conv_state(splits):
     check_prefill_every_element(shape, cpu, y, h, cs, torch.bfloat16)
 
 
+@pytest.mark.parametrize("S", [1, 2, 3, 77, 128, 129, 300])
+def test_states_updated_in_place_equal_separate_outputs(S):
+    """The final states may be written over the initial ones (conv_state_out
+    = conv_state_in, ssm_state_out = ssm_state_in): y and both states equal,
+    bit for bit, those of the same call with separate outputs -- on the
+    multi-unit kernel (S <= 128) and on the chunk kernel, and for S < W-1,
+    where the new conv state keeps rows of the old one."""
+    shape = si.Shape(batch=3, seqlen=S, nheads=16, headdim=64, dstate=128, ngroups=2)
+    _, dev = make_problem(shape, act=torch.bfloat16, seed=40 + S)
+    kw = dict(nheads=16, headdim=64, dstate=128, ngroups=2, conv_w=dev["conv_w"],
+              conv_b=dev["conv_b"], dt_bias=dev["dt_bias"], D=dev["D"], z=dev["z"])
+    y1, h1, c1 = ssd.chunk_scan(dev["xbc"], dev["dt_raw"], dev["A"], conv_state=dev["conv_state"],
+                                ssm_state=dev["ssm_state"], **kw)
+    hs, cs = dev["ssm_state"].clone(), dev["conv_state"].clone()
+    y2 = torch.empty_like(y1)
+    ssd.chunk_scan(dev["xbc"], dev["dt_raw"], dev["A"], conv_state=cs, ssm_state=hs,
+                   out=(y2, hs, cs), **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2), "y"
+    assert torch.equal(h1, hs), "ssm state written in place"
+    assert torch.equal(c1, cs), "conv state written in place"
+
+
 # ---------------------------------------------------------------------------
 # the other workloads at full size, in the calls the benchmark makes.  Inputs
 # are drawn on the GPU; the checked sequences are copied to the host and the
