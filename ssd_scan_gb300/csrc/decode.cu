@@ -28,10 +28,12 @@ constexpr int kThreads = 512;
 // the compile-time bound on K (1, 2, 4, 8 or 16) and RF the state rows a warp
 // keeps in flight; RF * KT (a power of two, at most 32) partial sums of y per
 // lane are reduced over the warp together.
-template <typename T, int KT, int RF>
+template <typename T, int KT, int RF, bool kZs>
 __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
 {
     // x [K][hpg*P] | B [K][N] | C [K][N] | dt, dA [K][hpg] | D [hpg] | silu(z) [K][hpg*P]
+    // (the last with kZs, when it fits beside the rest: else z is read by the
+    // lanes that write y)
     extern __shared__ float sm[];
     const int g = blockIdx.x, i = blockIdx.y;
     const int H = p.H, P = p.P, N = p.N, G = p.G, K = p.K;
@@ -58,7 +60,7 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
     float* dts = Cs + K * N;        // [K][hpg]
     float* dAs = dts + K * hpg;     // [K][hpg]
     float* Ds = dAs + K * hpg;      // [hpg]
-    float* zs = Ds + hpg;           // [K][XW] (with z)
+    float* zs = Ds + hpg;           // [K][XW] (kZs)
     // conv + SiLU of the group's channels over u = [conv state ; the row's K
     // tokens]: output t reads u rows t .. t+W-1 (the first W-1 rows of u from
     // the slot's conv state, the rest from the row's raw tokens).  A thread per
@@ -97,8 +99,8 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
     // the skip weights and the gate, so that no global load waits in the
     // state loop below
     for (int j = threadIdx.x; j < hpg; j += blockDim.x) Ds[j] = p.D ? p.D[h0 + j] : 0.0f;
-    if (p.flags & kHasZ) {
-        const T* zz = static_cast<const T*>(p.z);
+    const T* zz = static_cast<const T*>(p.z);
+    if (kZs && (p.flags & kHasZ)) {
         for (int e = threadIdx.x; e < K * XW; e += blockDim.x) {
             const int t = e / XW, c = e % XW;
             const float zv = to_f32(zz[((size_t)i * K + t) * H * P + h0 * P + c]);
@@ -180,7 +182,14 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(DecodeParams p)
             const int row = r0 + rr;         // j * P + pp
             const int h = h0 + j, pp = row % P;
             float yv = fmaf(Ds[j], xs[tt * XW + row], acc[0]);
-            if (p.flags & kHasZ) yv *= zs[tt * XW + row];
+            if (p.flags & kHasZ) {
+                if constexpr (kZs) {
+                    yv *= zs[tt * XW + row];
+                } else {
+                    const float zv = to_f32(zz[((size_t)i * K + tt) * H * P + h * P + pp]);
+                    yv *= zv / (1.0f + expf(-zv));
+                }
+            }
             y[(((size_t)i * K + tt) * H + h) * P + pp] = from_f32<T>(yv);
         }
     }
@@ -208,22 +217,34 @@ __global__ void decode_conv_roll_kernel(DecodeParams p)
     }
 }
 
-size_t decode_smem_bytes(const DecodeParams& p)
+// Shared memory of a decode CTA, with or without the staged SiLU(z).
+size_t decode_smem_bytes(int H, int P, int N, int G, int K, bool stage_z)
 {
-    const int hpg = p.H / p.G;
-    const size_t zb = (p.flags & kHasZ) ? (size_t)hpg * p.P : 0;
-    return sizeof(float) * ((size_t)p.K * ((size_t)hpg * p.P + 2 * (size_t)p.N + 2 * (size_t)hpg + zb) + hpg);
+    const size_t hpg = (size_t)(H / G);
+    const size_t zb = stage_z ? hpg * P : 0;
+    return sizeof(float) * ((size_t)K * (hpg * P + 2 * (size_t)N + 2 * hpg + zb) + hpg);
+}
+constexpr size_t kDecodeSmemMax = 200 * 1024;
+
+template <typename T, int KT, int RF, bool kZs>
+cudaError_t launch_kz(const DecodeParams& p, cudaStream_t st)
+{
+    const size_t smem = decode_smem_bytes(p.H, p.P, p.N, p.G, p.K, kZs);
+    cudaError_t e = cudaFuncSetAttribute(decode_step_kernel<T, KT, RF, kZs>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    decode_step_kernel<T, KT, RF, kZs><<<dim3(p.G, p.R), kThreads, smem, st>>>(p);
+    return cudaGetLastError();
 }
 
+// SiLU(z) staged in shared memory when it fits there beside the tokens' x
+// columns (every shape this library admits fits without it)
 template <typename T, int KT, int RF>
 cudaError_t launch_kt(const DecodeParams& p, cudaStream_t st)
 {
-    const size_t smem = decode_smem_bytes(p);
-    cudaError_t e = cudaFuncSetAttribute(decode_step_kernel<T, KT, RF>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    decode_step_kernel<T, KT, RF><<<dim3(p.G, p.R), kThreads, smem, st>>>(p);
-    return cudaGetLastError();
+    if ((p.flags & kHasZ) && decode_smem_bytes(p.H, p.P, p.N, p.G, p.K, true) <= kDecodeSmemMax)
+        return launch_kz<T, KT, RF, true>(p, st);
+    return launch_kz<T, KT, RF, false>(p, st);
 }
 
 template <typename T>
@@ -242,9 +263,8 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t st)
 
 bool decode_supports(int H, int P, int N, int G, int K)
 {
-    const size_t smem =
-        sizeof(float) * (size_t)K * ((size_t)(H / G) * P + 2 * (size_t)N + 2 * (size_t)(H / G));
-    return N % 4 == 0 && P % 4 == 0 && K >= 1 && K <= kDecodeMaxTokens && smem <= 200 * 1024;
+    return N % 4 == 0 && P % 4 == 0 && K >= 1 && K <= kDecodeMaxTokens &&
+           decode_smem_bytes(H, P, N, G, K, false) <= kDecodeSmemMax;
 }
 
 cudaError_t launch_decode_step(const DecodeParams& p, bool bf16, cudaStream_t st)

@@ -213,6 +213,20 @@ def test_multi_token_decode_equals_single_steps_and_oracle(K, act, conv):
     instead of in the pool), and == the oracle's K steps from the slots'
     states, within the tolerance; slots no row names stay untouched."""
     shape = si.Shape(batch=12, seqlen=1, nheads=8, headdim=64, dstate=128, ngroups=2)
+    _check_multi_token(shape, K, act, conv)
+
+
+@pytest.mark.parametrize("K", [2, 16])
+def test_multi_token_decode_wide_group(K):
+    """32 heads in one group: at K = 16 the tokens' SiLU(z) no longer fits in
+    shared memory beside their x columns and the kernel reads z in its
+    epilogue instead (at K = 2 it stages it); either way the same results as
+    K one-token calls, bit for bit, and as the oracle within the tolerance."""
+    shape = si.Shape(batch=6, seqlen=1, nheads=32, headdim=64, dstate=128, ngroups=1)
+    _check_multi_token(shape, K, torch.bfloat16, True)
+
+
+def _check_multi_token(shape, K, act, conv):
     prm, pools = _setup(shape, 40, act=act)
     slots = pools["slot_ids"]
     inp = _multi_inputs(shape, K, seed=K, act=act)
