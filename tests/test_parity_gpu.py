@@ -336,11 +336,15 @@ def test_bf16_other_head_dims_run_row_exact_kernel():
 
 
 @pytest.mark.parametrize("W", [2, 3])
-def test_bf16_short_conv_widths(W):
-    shape = si.Shape(batch=1, seqlen=260, nheads=4, headdim=64, dstate=128, ngroups=1,
+@pytest.mark.parametrize("splits", [[130, 130], [100, 1, 59, 100]])
+def test_bf16_short_conv_widths(W, splits):
+    """Conv widths below 4 on the tensor-core paths: calls of more than one
+    chunk (the chunk kernel) and of at most 128 rows (the multi-unit kernel,
+    whose taps are front-padded to 4), chained."""
+    shape = si.Shape(batch=2, seqlen=260, nheads=4, headdim=64, dstate=128, ngroups=1,
                      conv_width=W)
     cpu, dev = make_problem(shape, act=torch.bfloat16)
-    y, h, cs = gpu_prefill(shape, dev, [130, 130])
+    y, h, cs = gpu_prefill(shape, dev, splits)
     _check_prefill(shape, cpu, y, h, cs, torch.bfloat16)
 
 
