@@ -144,7 +144,7 @@ struct __align__(1024) TcSmem {
     alignas(16) float2 bconv[P / 2];
     uint64_t full_c, full_b, full_z[2], full_x[2];  // TMA landed
     uint64_t g1, g3, g4, g2, fin;   // MMA commits
-    uint64_t xready, mready, hsready;                    // compute -> control
+    uint64_t xready[2], mready, hsready;                 // compute -> control (xready by chunk parity)
     uint64_t cvready[kCv], epidone[kCv];                 // gamma warp <-> compute
     uint32_t tmem_base;
     int abort;
@@ -378,7 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&s.g4, 1);
         mbar_init(&s.g2, 1);
         mbar_init(&s.fin, 1);
-        mbar_init(&s.xready, kCompute);
+        mbar_init(&s.xready[0], kCompute);
+        mbar_init(&s.xready[1], kCompute);
         mbar_init(&s.mready, kCompute);
         mbar_init(&s.hsready, kCompute);
         for (int i = 0; i < kCv; ++i) {
@@ -484,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < nchunks && ok; ++c) {
                 const int kb = c & 1;
                 // G4(c): x rows of chunk c in place; dH read by state(c-1)
-                ok = wait_or_abort(s, &s.xready, c & 1, wlim) && wait_or_abort(s, &s.hsready, c & 1, wlim);
+                ok = wait_or_abort(s, &s.xready[c & 1], (c >> 1) & 1, wlim) && wait_or_abort(s, &s.hsready, c & 1, wlim);
                 if (!ok) break;
                 // the conv of chunk c is done with its raw tile: chunk c+2's goes there
                 if (c + 2 < nchunks) load_x(c + 2);
@@ -790,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_or_abort(s, &s.cvready[0], 0, wlim) && wait_or_abort(s, &s.full_x[0], 0, wlim);
             if (ok) conv(0);
             fence_proxy_async_smem();  // XR / XS are read by G4 / G2
-            mbar_arrive(&s.xready);
+            mbar_arrive(&s.xready[0]);
         }
 
         for (int c = 0; c < nchunks; ++c) {
@@ -897,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          wait_or_abort(s, &s.full_x[(c + 1) & 1], ((c + 1) >> 1) & 1, wlim);
                 if (ok) conv(c + 1);
                 fence_proxy_async_smem();  // XR / XS are read by G4 / G2
-                mbar_arrive(&s.xready);
+                mbar_arrive(&s.xready[(c + 1) & 1]);
             }
 
             // ---- epilogue(c): factored y = u Y; exact y = Y + u Yo; times silu(z).
