@@ -80,12 +80,16 @@ def measured_peaks() -> tuple[float, str]:
 
 
 def kernel_source_sha() -> str:
+    """Hash of the kernel sources and of the build script (its flags shape the
+    code as well)."""
     h = hashlib.sha256()
     cdir = os.path.join(ROOT, "ssd_scan_gb300", "csrc")
     for n in sorted(os.listdir(cdir)):
         if n.endswith((".cu", ".cuh")):
             with open(os.path.join(cdir, n), "rb") as f:
                 h.update(n.encode() + f.read())
+    with open(os.path.join(ROOT, "ssd_scan_gb300", "build.py"), "rb") as f:
+        h.update(b"build.py" + f.read())
     return h.hexdigest()[:16]
 
 

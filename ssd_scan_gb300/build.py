@@ -23,6 +23,12 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",
                      "-I", os.path.join(ROOT, "include")]
+# Per translation unit.  The tensor-core scan is bound by the latency of its
+# compute warps at a 96-register cap; ptxas's register-usage level 3 (of 0..10,
+# default 5) schedules it 1.4 % faster on the long prefill with the same bits
+# out (levels 0-3 alike, 4 and 5 not; on every file it slowed the multi-token
+# decode).
+FILE_FLAGS = {"scan_tc.cu": ["-Xptxas", "--register-usage-level=3"]}
 
 
 def nvcc() -> str:
@@ -56,7 +62,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [cc] + NVCC_FLAGS + ["-c", src, "-o", obj]
+        cmd = [cc] + NVCC_FLAGS + FILE_FLAGS.get(os.path.basename(src), []) + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
