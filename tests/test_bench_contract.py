@@ -27,3 +27,19 @@ def test_reference_arm_json_line():
     assert out["e2e"]["value"] == out["value"]
     assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["e2e"]["d2h_bytes_per_step"] == 0
     assert out["config"]["seq_len"] == 8
+
+
+def test_link_bound_of_a_step():
+    """The least step time the host link allows: the shorter direction's bytes
+    at the both-ways rate, beside as many of the longer one's, then the rest of
+    the longer direction alone (hand-computed cases)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    link = {"h2d_gbs": 200.0, "d2h_gbs": 100.0, "both_ways_gbs_per_direction": 50.0}
+    # 4 GB in, 1 GB out: 1 GB each way at 50 GB/s (20 ms), then 3 GB in at 200 (15 ms)
+    assert abs(bench.link_bound_ms(4_000_000_000, 1_000_000_000, link) - 35.0) < 1e-9
+    # 1 GB in, 3 GB out: 1 GB each way (20 ms), then 2 GB out at 100 (20 ms)
+    assert abs(bench.link_bound_ms(1_000_000_000, 3_000_000_000, link) - 40.0) < 1e-9
+    # one direction only: its own rate
+    assert abs(bench.link_bound_ms(2_000_000_000, 0, link) - 10.0) < 1e-9
+    assert abs(bench.link_bound_ms(0, 0, link)) < 1e-12
