@@ -915,6 +915,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float2 ss2 = make_float2(0.0f, 0.0f);  // (kNorm) sum of y^2 over this thread's columns
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {  // 8 columns at a time
+                    // z first: its shared-memory read overlaps the TMEM loads (the
+                    // TMEM wait below orders every later memory access after it)
+                    const uint32_t off = chunk_off(t, 2 * j + hh);  // row t, 8 columns (SW128)
+                    uint4 zraw = make_uint4(0u, 0u, 0u, 0u);
+                    if (has_z) zraw = at<uint4>(s.Zt[kb], off);
                     float yv[8];
                     tmem_ld8(tbase + kColY + 64 * kb + lane_off + 16 * j + 8 * hh, yv);
                     if (!fac) {
@@ -938,8 +943,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     float2 out[4], zv[4];
-                    const uint32_t off = chunk_off(t, 2 * j + hh);  // row t, 8 columns (SW128)
-                    if (has_z) unpack4x2(at<uint4>(s.Zt[kb], off), zv);
+                    if (has_z) unpack4x2(zraw, zv);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         float2 v = make_float2(yv[2 * e], yv[2 * e + 1]);
@@ -1648,6 +1652,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float2 dd = make_float2(dec, dec);
 #pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
+                    const uint32_t off = chunk_off(t, 2 * j + hh);  // z first, as in scan_tc_kernel
+                    uint4 zraw = make_uint4(0u, 0u, 0u, 0u);
+                    if (has_z) zraw = at<uint4>(s.Zt[kb], off);
                     float yv[8];
                     tmem_ld8(tbase + kColY + 64 * kb + lane_off + 16 * j + 8 * hh, yv);
                     if (!fac) {
@@ -1671,8 +1678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     float2 out[4], zv[4];
-                    const uint32_t off = chunk_off(t, 2 * j + hh);
-                    if (has_z) unpack4x2(at<uint4>(s.Zt[kb], off), zv);
+                    if (has_z) unpack4x2(zraw, zv);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         float2 v = make_float2(yv[2 * e], yv[2 * e + 1]);
