@@ -906,11 +906,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // quarter's 32 rows leave with one TMA store (rows past the end are not
             // written).  The store of chunk c-2 from this buffer finished reading it
             // before its issuer's mask(c-1) arrival. ----
+            // exp(min(gamma_t, 0)) from the chunk's values (ready since the conv
+            // of chunk c), before the waits, so its shared-memory read is not held
+            // behind them
+            const float dec = ex2_fast(fminf(cv.g2h[t] + cv.g2l[t], 0.0f));
             if (ok) ok = wait_or_abort(s, &s.g2, c & 1, wlim);
             if (ok && has_z) ok = wait_or_abort(s, &s.full_z[kb], (c >> 1) & 1, wlim);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
-                const float dec = ex2_fast(fminf(cv.g2h[t] + cv.g2l[t], 0.0f));  // exp(min(gamma_t, 0))
                 const float2 dd = make_float2(dec, dec);
                 float2 ss2 = make_float2(0.0f, 0.0f);  // (kNorm) sum of y^2 over this thread's columns
 #pragma unroll 1
